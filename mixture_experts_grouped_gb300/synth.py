@@ -1,0 +1,239 @@
+"""Seeded synthetic inputs for the grouped MoE layer.
+
+This module only draws random numbers and packs them into the storage formats
+the layer consumes; it holds none of the layer's arithmetic. It imports neither
+the CUDA binding nor the CPU oracle, and both the tests and ``bench.py`` feed
+its output to each of them.
+
+Every tensor draws from its own stream, ``PCG64(SeedSequence([seed, tensor,
+expert]))``, so a weight does not depend on the token count and experts can be
+drawn in parallel threads.
+
+Workloads (names used across the tests and the benchmark):
+
+* ``tiny``            T=16, H=128, I=64, E=8, k=2, bs=16, bf16
+* ``mixtral_prefill`` T=4096, H=4096, I=14336, E=8, k=2, bs=64, bf16
+* ``fine_grained``    H=2048, I=768, E=128, k=8, bs=64, bf16, Zipf-biased router
+* ``gptq``            H=2048, I=1408, E=64, k=6, bs=16, fp16 activations, GPTQ int4
+* ``nvfp4_lora``      T=2048, H=2048, I=768, E=128, k=8, bs=64, NVFP4 + rank-16 LoRA
+"""
+
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, replace
+from typing import Optional
+
+import numpy as np
+
+# tensor stream ids
+_X, _ROUTER, _GU, _DOWN, _LORA_A, _LORA_B, _GU_SC, _DOWN_SC, _S2 = range(9)
+
+
+@dataclass(frozen=True)
+class MoeConfig:
+    name: str
+    T: int
+    H: int
+    I: int
+    E: int
+    k: int
+    bs: int
+    act: str = "bf16"          # activation dtype: "bf16" | "f16"
+    wfmt: str = "bf16"         # weight format: "bf16" | "gptq" | "nvfp4"
+    router: str = "gemm"       # "gemm": logits = x @ Wr; "normal": N(0,1); "zipf": N(0,1) + bias
+    router_std: float = 0.02   # std of Wr for router="gemm"
+    weight_std: float = 0.02
+    renormalize: bool = True
+    lora_rank: int = 0         # 0 = no LoRA fold
+    lora_scale: float = 2.0
+    group_size: int = 128      # GPTQ group size
+    seed: int = 0
+
+    def with_T(self, T: int) -> "MoeConfig":
+        return replace(self, T=T, name=f"{self.name.split('@')[0]}@T{T}")
+
+    @property
+    def P(self) -> int:
+        return self.T * self.k
+
+
+CONFIGS = {
+    "tiny": MoeConfig("tiny", T=16, H=128, I=64, E=8, k=2, bs=16, router_std=0.1),
+    "mixtral_prefill": MoeConfig("mixtral_prefill", T=4096, H=4096, I=14336, E=8, k=2, bs=64,
+                                 router_std=0.02),
+    "fine_grained": MoeConfig("fine_grained", T=4096, H=2048, I=768, E=128, k=8, bs=64,
+                              router="zipf"),
+    "gptq": MoeConfig("gptq", T=2048, H=2048, I=1408, E=64, k=6, bs=16, act="f16",
+                      wfmt="gptq", router="normal"),
+    "nvfp4_lora": MoeConfig("nvfp4_lora", T=2048, H=2048, I=768, E=128, k=8, bs=64,
+                            wfmt="nvfp4", router="normal", lora_rank=16),
+}
+
+FINE_GRAINED_T = (1, 8, 64, 512, 4096, 16384)
+GPTQ_T = (16, 2048)
+
+
+def _rng(seed: int, tensor: int, part: int = 0) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tensor, part])))
+
+
+def _threads() -> int:
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Pack f32 samples into bf16 storage (nearest, ties to even). Input packing
+    only: finite samples from the generators below."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).copy()
+    r = (u >> np.uint32(16)) & np.uint32(1)
+    r += np.uint32(0x7FFF)
+    u += r
+    u >>= np.uint32(16)
+    return u.astype(np.uint16)
+
+
+def _normal_act(rng, shape, std, act):
+    a = rng.standard_normal(shape, dtype=np.float32)
+    if std != 1.0:
+        a *= np.float32(std)
+    return f32_to_bf16_bits(a) if act == "bf16" else a.astype(np.float16)
+
+
+def _per_expert(fn, E):
+    with ThreadPoolExecutor(_threads()) as ex:
+        return np.stack(list(ex.map(fn, range(E))))
+
+
+def _bf16_weight(seed, tensor, E, N, K, std):
+    return {"format": "bf16",
+            "w": _per_expert(lambda e: _normal_act(_rng(seed, tensor, e), (N, K), std, "bf16"), E)}
+
+
+def _gptq_weight(seed, tensor, E, N, K, G):
+    """Raw GPTQ layout: uniform 4-bit codes, fp16 scales U(0.005, 0.02), every
+    zero point 8."""
+    if K % 8 or K % G or N % 8:
+        raise ValueError("GPTQ needs K % 8 == 0, K % group_size == 0, N % 8 == 0")
+
+    def qw(e):
+        return _rng(seed, tensor, e).integers(0, 2 ** 32, size=(K // 8, N), dtype=np.uint32).view(np.int32)
+
+    def sc(e):
+        return _rng(seed, tensor + 100, e).uniform(0.005, 0.02, size=(K // G, N)).astype(np.float16)
+
+    zeros = np.full((E, K // G, N // 8), 0x88888888, dtype=np.uint32).view(np.int32)
+    return {"format": "gptq", "qweight": _per_expert(qw, E), "scales": _per_expert(sc, E),
+            "qzeros": zeros, "group_size": G}
+
+
+# magnitude-code probabilities of E2M1 codes 0..7 (values 0,.5,1,1.5,2,3,4,6),
+# shaped like a block-scaled Gaussian
+_E2M1_P = np.array([0.10, 0.16, 0.18, 0.16, 0.14, 0.12, 0.09, 0.05])
+
+
+def _nvfp4_weight(seed, tensor, E, N, K, n_scale2):
+    """NVFP4 codes drawn directly: E2M1 magnitude codes from ``_E2M1_P`` with a
+    random sign, E4M3 block scales with exponent field 5..9 and any mantissa
+    (values 0.25 .. 3.75, never NaN), fp32 ``scale2`` U(0.5, 1.5) * 2**-7."""
+    if K % 16:
+        raise ValueError("NVFP4 needs K % 16 == 0")
+
+    def packed(e):
+        r = _rng(seed, tensor, e)
+        mag = r.choice(8, size=(N, K), p=_E2M1_P).astype(np.uint8)
+        sign = r.integers(0, 2, size=(N, K), dtype=np.uint8) << 3
+        c = mag | sign
+        return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+
+    def scales(e):
+        r = _rng(seed, tensor + 100, e)
+        ex = r.integers(5, 10, size=(K // 16, N), dtype=np.uint8)
+        man = r.integers(0, 8, size=(K // 16, N), dtype=np.uint8)
+        return ((ex << 3) | man).astype(np.uint8)
+
+    s2 = (_rng(seed, _S2, tensor).uniform(0.5, 1.5, size=(n_scale2, E)) * 2.0 ** -7).astype(np.float32)
+    return {"format": "nvfp4", "packed": _per_expert(packed, E), "scales": _per_expert(scales, E),
+            "scale2": s2}
+
+
+def make_weights(cfg: MoeConfig) -> dict:
+    """Expert weights: gate/up stacked ``[E, 2I, H]`` (rows ``[0, I)`` gate,
+    ``[I, 2I)`` up) and down ``[E, H, I]`` in the config's format."""
+    E, H, I, s = cfg.E, cfg.H, cfg.I, cfg.seed
+    if cfg.wfmt == "bf16":
+        gu = _bf16_weight(s, _GU, E, 2 * I, H, cfg.weight_std)
+        dn = _bf16_weight(s, _DOWN, E, H, I, cfg.weight_std)
+    elif cfg.wfmt == "gptq":
+        gu = _gptq_weight(s, _GU, E, 2 * I, H, cfg.group_size)
+        dn = _gptq_weight(s, _DOWN, E, H, I, cfg.group_size)
+    elif cfg.wfmt == "nvfp4":
+        gu = _nvfp4_weight(s, _GU, E, 2 * I, H, 2)
+        dn = _nvfp4_weight(s, _DOWN, E, H, I, 1)
+    else:
+        raise ValueError(cfg.wfmt)
+    return {"w_gate_up": gu, "w_down": dn}
+
+
+def make_lora(cfg: MoeConfig) -> Optional[dict]:
+    """Rank-r bf16 LoRA on the down projection of the even-id experts:
+    ``A_e [r, I]``, ``B_e [H, r]`` N(0, 0.02), scale ``cfg.lora_scale``; the
+    tables run to the largest adapted id + 1."""
+    if cfg.lora_rank == 0:
+        return None
+    adapted = list(range(0, cfg.E, 2))
+    a = {e: _normal_act(_rng(cfg.seed, _LORA_A, e), (cfg.lora_rank, cfg.I), 0.02, "bf16") for e in adapted}
+    b = {e: _normal_act(_rng(cfg.seed, _LORA_B, e), (cfg.H, cfg.lora_rank), 0.02, "bf16") for e in adapted}
+    n = max(adapted) + 1
+    scale = np.zeros(n, dtype=np.float32)
+    scale[adapted] = np.float32(cfg.lora_scale)
+    return {"a": a, "b": b, "scale": scale, "n_experts": n, "rank": cfg.lora_rank,
+            "row_adapter": None}
+
+
+def make_activations(cfg: MoeConfig) -> dict:
+    """Token activations ``x [T, H]`` and router logits ``[T, E]`` (f32).
+
+    * ``gemm``: ``Wr [H, E]`` f32 N(0, router_std) and ``logits = f32(x @ Wr)``
+      with the product taken in fp64 (the router GEMM itself sits before the
+      layer and is part of the input recipe);
+    * ``normal``: logits N(0, 1);
+    * ``zipf``: logits N(0, 1) plus ``-1.1 * ln(e + 1)``, the log-probability of
+      a Zipf(s=1.1) popularity with rank e + 1.
+    """
+    T, H, E, s = cfg.T, cfg.H, cfg.E, cfg.seed
+    x = _normal_act(_rng(s, _X, T), (T, H), 1.0, cfg.act)
+    r = _rng(s, _ROUTER, T)
+    if cfg.router == "gemm":
+        wr = _rng(s, _ROUTER, 0).standard_normal((H, E), dtype=np.float32) * np.float32(cfg.router_std)
+        if cfg.act == "bf16":
+            xf = (x.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+        else:
+            xf = x.astype(np.float64)
+        logits = (xf @ wr.astype(np.float64)).astype(np.float32)
+    elif cfg.router == "normal":
+        logits = r.standard_normal((T, E), dtype=np.float32)
+    elif cfg.router == "zipf":
+        bias = -1.1 * np.log(np.arange(E, dtype=np.float64) + 1.0)
+        logits = (r.standard_normal((T, E)) + bias[None, :]).astype(np.float32)
+    else:
+        raise ValueError(cfg.router)
+    return {"x": x, "logits": logits}
+
+
+def make_inputs(cfg: MoeConfig, weights: Optional[dict] = None) -> dict:
+    """Everything one layer call consumes, as numpy arrays."""
+    d = make_activations(cfg)
+    d.update(weights if weights is not None else make_weights(cfg))
+    d["lora"] = make_lora(cfg)
+    return d
+
+
+def random_ids(seed: int, P: int, E: int, skew: float = 0.0) -> np.ndarray:
+    """Flat expert ids for align tests: uniform, or Zipf-like with ``skew`` > 0."""
+    r = _rng(seed, 50, P)
+    if skew <= 0:
+        return r.integers(0, E, size=P).astype(np.int32)
+    p = (np.arange(E) + 1.0) ** -skew
+    return r.choice(E, size=P, p=p / p.sum()).astype(np.int32)
