@@ -1,0 +1,298 @@
+"""GPU parity of every step through the C ABI against the CPU oracle.
+
+Routing and align are compared bit for bit; the FFN steps (gate/up, down, LoRA
+fold, combine) within relative Frobenius error 5e-3 and per-element
+2e-2 * (1 + |ref|). Each FFN step is checked in isolation (the oracle step is
+fed the GPU's own input to that step) and the whole layer end to end.
+"""
+import numpy as np
+import pytest
+
+import oracle as orc
+from mixture_experts_grouped_gb300 import synth
+from parity import check_route_align_exact, fetch, ffn_close, gpu_layer, valid_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from mixture_experts_grouped_gb300 import build
+    build.build()
+    return torch.device("cuda:0")
+
+
+# ---------------------------------------------------------------------------
+# a1 routing: bit-exact
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,E,k,renorm,kind", [
+    (16, 8, 2, True, "normal"), (4096, 8, 2, True, "normal"), (517, 128, 8, True, "zipf"),
+    (16384, 128, 8, True, "zipf"), (2048, 64, 6, True, "normal"), (300, 256, 16, True, "normal"),
+    (300, 256, 16, False, "normal"), (200, 33, 5, False, "ties"), (200, 64, 6, True, "ties"),
+    (64, 1, 1, True, "normal"), (1, 128, 8, True, "normal"), (100, 12, 12, False, "normal"),
+])
+def test_route_bit_exact(dev, T, E, k, renorm, kind):
+    import torch
+    from mixture_experts_grouped_gb300 import moe
+    rng = np.random.default_rng(T * 7 + E)
+    if kind == "ties":
+        logits = rng.integers(-4, 5, size=(T, E)).astype(np.float32)
+    else:
+        logits = (rng.standard_normal((T, E)) * 2).astype(np.float32)
+        if kind == "zipf":
+            logits += (-1.1 * np.log(np.arange(E) + 1.0)).astype(np.float32)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    moe.moe_route_topk_softmax(torch.from_numpy(logits).to(dev), ids, w, T, E, k, renorm)
+    torch.cuda.synchronize()
+    ref_ids, ref_w = orc.route_topk_softmax(logits, k, renorm)
+    np.testing.assert_array_equal(ids.cpu().numpy(), ref_ids)
+    got_w = w.cpu().numpy()
+    assert np.array_equal(got_w.view(np.uint32), ref_w.view(np.uint32)), \
+        f"{int(np.sum(got_w != ref_w))} weights differ; max |d| {np.max(np.abs(got_w - ref_w)):.3e}"
+
+
+# ---------------------------------------------------------------------------
+# a2 align: bit-exact
+# ---------------------------------------------------------------------------
+
+def _run_align(dev, ids_np, E, bs, max_padded=None):
+    import torch
+    from mixture_experts_grouped_gb300 import moe
+    P = ids_np.shape[0]
+    cap = moe.moe_align_capacity(P, E, bs) if max_padded is None else max_padded
+    i32 = dict(dtype=torch.int32, device=dev)
+    ids = torch.from_numpy(ids_np.astype(np.int32)).to(dev) if P else torch.empty(1, **i32)
+    st = torch.full((max(cap, 1),), -7, **i32)
+    eids = torch.full((max(cap // bs, 1),), -7, **i32)
+    off = torch.full((E + 1,), -7, **i32)
+    tot = torch.full((1,), -7, **i32)
+    p2r = torch.full((max(P, 1),), -7, **i32)
+    err = torch.zeros(1, **i32)
+    wsb = moe.moe_align_workspace_size(P, E)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    moe.moe_align_block_size(ids, P, E, bs, cap, st, eids, off, tot, p2r, err, ws, wsb)
+    torch.cuda.synchronize()
+    return (st.cpu().numpy()[:cap], eids.cpu().numpy()[:cap // bs], off.cpu().numpy(), int(tot.item()),
+            p2r.cpu().numpy()[:P], int(err.item()), cap)
+
+
+@pytest.mark.parametrize("P,E,bs,skew", [
+    (0, 8, 16, 0), (1, 8, 16, 0), (32, 8, 16, 0), (8192, 8, 64, 0), (131072, 128, 64, 1.1),
+    (12288, 64, 16, 0), (16384, 128, 64, 0), (5000, 256, 1, 0.5), (3333, 1, 64, 0), (65536, 256, 128, 2.0),
+    (2049, 7, 3, 0), (100000, 16, 256, 0.0),
+])
+def test_align_bit_exact(dev, P, E, bs, skew):
+    ids = synth.random_ids(P + E + bs, P, E, skew)
+    st, eids, off, tot, p2r, err, cap = _run_align(dev, ids, E, bs)
+    ref = orc.align_block_size(ids, E, bs, cap)
+    assert err == 0
+    np.testing.assert_array_equal(st, ref.sorted_token_ids)
+    np.testing.assert_array_equal(eids, ref.expert_ids)
+    np.testing.assert_array_equal(off, ref.expert_offsets)
+    assert tot == ref.total_tokens_post_pad
+    np.testing.assert_array_equal(p2r, ref.pair_to_row)
+
+
+def test_align_drops_and_flags_out_of_range_ids(dev):
+    from mixture_experts_grouped_gb300 import moe
+    ids = synth.random_ids(5, 3000, 16, 0)
+    ids[[7, 100, 2999]] = [16, -1, 1000]
+    st, eids, off, tot, p2r, err, cap = _run_align(dev, ids, 16, 16)
+    ref = orc.align_block_size(ids, 16, 16, cap)
+    assert err & moe.MOE_DEV_ERR_EXPERT_ID and ref.err == 1
+    np.testing.assert_array_equal(st, ref.sorted_token_ids)
+    np.testing.assert_array_equal(p2r, ref.pair_to_row)
+    np.testing.assert_array_equal(off, ref.expert_offsets)
+
+
+# ---------------------------------------------------------------------------
+# whole layers, each FFN step isolated
+# ---------------------------------------------------------------------------
+
+def _cfg(name, **kw):
+    base = synth.CONFIGS[name.split("@")[0]]
+    if "@" in name:
+        base = base.with_T(int(name.split("@T")[1]))
+    from dataclasses import replace
+    return replace(base, **kw) if kw else base
+
+
+LAYER_CASES = {
+    "tiny": _cfg("tiny"),
+    "fine_grained@T1": _cfg("fine_grained@T1"),
+    "fine_grained@T8": _cfg("fine_grained@T8"),
+    "fine_grained@T64": _cfg("fine_grained@T64"),
+    "fine_grained@T512": _cfg("fine_grained@T512"),
+    "gptq@T16": _cfg("gptq@T16"),
+    "gptq@T2048": _cfg("gptq@T2048"),
+    "nvfp4@T64": _cfg("nvfp4_lora@T64", lora_rank=0),
+    "nvfp4_lora@T2048": _cfg("nvfp4_lora"),
+    # edge shapes: one expert, ragged I (not a multiple of 128) and a span of several row tiles
+    "one_expert_ragged": synth.MoeConfig("one_expert_ragged", T=300, H=128, I=136, E=1, k=1, bs=16,
+                                         router="normal"),
+    # H below one 256-column output tile, top_k == E, block_size 1
+    "small_H_k_eq_E": synth.MoeConfig("small_H_k_eq_E", T=77, H=192, I=64, E=4, k=4, bs=1, router="normal"),
+    # skewed: most pairs on one expert (long spans crossing many 128-row tiles)
+    "skewed": synth.MoeConfig("skewed", T=1500, H=256, I=256, E=16, k=2, bs=64, router="zipf"),
+    "gptq_bf16_act": synth.MoeConfig("gptq_bf16_act", T=40, H=256, I=128, E=8, k=2, bs=16, act="bf16",
+                                     wfmt="gptq", router="normal", group_size=64),
+    "nvfp4_f16_act": synth.MoeConfig("nvfp4_f16_act", T=40, H=256, I=192, E=8, k=2, bs=16, act="f16",
+                                     wfmt="nvfp4", router="normal"),
+}
+
+
+@pytest.mark.parametrize("name", list(LAYER_CASES))
+def test_layer_steps_match_oracle(dev, name):
+    import torch
+    cfg = LAYER_CASES[name]
+    inp = synth.make_inputs(cfg)
+    lora = inp["lora"]
+    lay, x, logits = gpu_layer(cfg, inp, dev, lora=None)   # base path (no fold) first
+    g = fetch(lay)
+    ref_ids, ref_w = orc.route_topk_softmax(inp["logits"], cfg.k, cfg.renormalize)
+    al = orc.align_block_size(ref_ids.reshape(-1), cfg.E, cfg.bs, lay.max_padded)
+    check_route_align_exact(g, ref_ids, ref_w, al)
+    assert g["err"] == 0, f"device error word {g['err']:#x}"
+    P = cfg.P
+    rows = valid_rows(al.sorted_token_ids, al.total_tokens_post_pad, P)
+    # gate/up (+ silu*up) from the same x
+    h_ref = orc.grouped_gate_up(inp["x"], cfg.act, inp["w_gate_up"], al.sorted_token_ids, al.expert_offsets, P,
+                                cfg.k, cfg.I)
+    ffn_close(g["h"][rows], h_ref[rows], f"{name}: h")
+    pad = np.setdiff1d(np.arange(al.total_tokens_post_pad), rows)
+    assert not g["h"][pad].any(), "padding rows of h must be zero"
+    # down from the GPU's own h
+    y_ref = orc.grouped_down(g["h"], cfg.act, inp["w_down"], al.sorted_token_ids, al.expert_offsets, P, cfg.H)
+    ffn_close(g["y"][rows], y_ref[rows], f"{name}: y")
+    # combine from the GPU's own y
+    out_ref = orc.combine(g["y"], cfg.act, al.pair_to_row, ref_w, cfg.T, cfg.k)
+    ffn_close(g["out"], out_ref, f"{name}: combine")
+    if lora is not None:
+        # fold in place on the GPU's y, compare with the oracle fold of the same inputs
+        from mixture_experts_grouped_gb300 import layer as L
+        dl = L.upload_lora(lora, cfg.I, cfg.H, dev)
+        lay.lora = dl
+        lay.xa = torch.zeros((lay.max_padded, dl.route.max_rank), dtype=torch.bfloat16, device=dev)
+        lay.lora_fold()
+        torch.cuda.synchronize()
+        y_fold = orc.act_to_f64(L.act_numpy(lay.y, cfg.act), cfg.act)
+        ref_fold, _ = orc.lora_grouped_down(g["h_bits"], g["y_bits"], lora["a"], lora["b"], lora["scale"],
+                                            lora["n_experts"], al.expert_offsets, al.sorted_token_ids, P, cfg.k,
+                                            None, 0, al.total_tokens_post_pad)
+        ffn_close(y_fold[rows], orc.bf16_bits_to_f64(ref_fold)[rows], f"{name}: LoRA fold")
+        # rows of unadapted (odd) experts are untouched, bit for bit
+        ex = np.searchsorted(al.expert_offsets, rows, side="right") - 1
+        odd = rows[ex % 2 == 1]
+        assert np.array_equal(L.act_numpy(lay.y, cfg.act)[odd], g["y_bits"][odd])
+
+
+@pytest.mark.parametrize("name", ["tiny", "fine_grained@T64", "gptq@T16", "nvfp4_lora@T2048", "skewed"])
+def test_layer_end_to_end(dev, name):
+    cfg = LAYER_CASES[name]
+    inp = synth.make_inputs(cfg)
+    lay, _, _ = gpu_layer(cfg, inp, dev, lora=inp["lora"])
+    g = fetch(lay)
+    ref = orc.moe_layer(inp["x"], cfg.act, inp["logits"], cfg.k, cfg.E, cfg.bs, inp["w_gate_up"], inp["w_down"],
+                        cfg.I, cfg.H, cfg.renormalize, lora=inp["lora"], max_padded=lay.max_padded)
+    check_route_align_exact(g, ref.ids, ref.weights, ref.align)
+    ffn_close(g["out"], ref.out, f"{name}: layer output")
+
+
+def test_lora_windows_bit_identical_to_one_window(dev):
+    import torch
+    from mixture_experts_grouped_gb300 import layer as L
+    from mixture_experts_grouped_gb300 import moe
+    cfg = _cfg("nvfp4_lora@T256")
+    inp = synth.make_inputs(cfg)
+    lay, _, _ = gpu_layer(cfg, inp, dev, lora=None)
+    dl = L.upload_lora(inp["lora"], cfg.I, cfg.H, dev)
+    y0 = lay.y.clone()
+    total = int(lay.total_post_pad.item())
+    lay.lora, lay.xa = dl, torch.zeros((lay.max_padded, 16), dtype=torch.bfloat16, device=dev)
+    lay.lora_fold(row_offset=0, row_end=total)
+    one = lay.y.clone()
+    for cap in (1, 100, 1000):
+        lay.y.copy_(y0)
+        xa_small = torch.zeros((cap, 16), dtype=torch.bfloat16, device=dev)
+        lay.xa = xa_small
+        for lo, hi in moe.lora_windows(total, cap):
+            lay.lora_fold(row_offset=lo, row_end=hi)
+        torch.cuda.synchronize()
+        assert torch.equal(lay.y.view(torch.int16), one.view(torch.int16)), f"cap={cap}"
+
+
+def test_lora_row_adapter_and_gate_up_gather(dev):
+    """row_adapter < 0 skips a token's rows; x_gather = 1 reads token-major rows."""
+    import torch
+    from mixture_experts_grouped_gb300 import layer as L
+    from mixture_experts_grouped_gb300 import moe
+    cfg = synth.MoeConfig("lora_gather", T=50, H=128, I=128, E=8, k=2, bs=16, router="normal", lora_rank=8)
+    inp = synth.make_inputs(cfg)
+    lay, x, _ = gpu_layer(cfg, inp, dev, lora=None)
+    g = fetch(lay)
+    ra = np.zeros(cfg.T, np.int32)
+    ra[::4] = -1
+    dl = L.upload_lora(inp["lora"], cfg.I, cfg.H, dev)
+    xa = torch.zeros((lay.max_padded, 8), dtype=torch.bfloat16, device=dev)
+    ra_d = torch.from_numpy(ra).to(dev)
+    for x_gather, src, src_bits in ((0, lay.h, g["h_bits"]), (1, x, inp["x"])):
+        base = lay.y.clone()
+        moe.moe_lora_grouped_down(dl.route, src, base, lay.expert_offsets, lay.sorted_token_ids, ra_d, xa, 0,
+                                  lay.max_padded, x_gather, cfg.T, cfg.k)
+        torch.cuda.synchronize()
+        al = orc.align_block_size(g["ids"].reshape(-1), cfg.E, cfg.bs, lay.max_padded)
+        ref, _ = orc.lora_grouped_down(src_bits, g["y_bits"], inp["lora"]["a"], inp["lora"]["b"],
+                                       inp["lora"]["scale"], inp["lora"]["n_experts"], al.expert_offsets,
+                                       al.sorted_token_ids, cfg.P, cfg.k, ra, 0, lay.max_padded, x_gather)
+        rows = valid_rows(al.sorted_token_ids, al.total_tokens_post_pad, cfg.P)
+        got = L.act_numpy(base, "bf16")
+        ffn_close(orc.bf16_bits_to_f64(got)[rows], orc.bf16_bits_to_f64(ref)[rows], f"x_gather={x_gather}")
+        skipped = rows[ra[al.sorted_token_ids[rows] // cfg.k] < 0]
+        assert np.array_equal(got[skipped], g["y_bits"][skipped])
+
+
+def test_gemm_rejects_bad_offsets_on_device(dev):
+    """expert_offsets that decrease: the GEMM runs no tile and flags the error."""
+    import torch
+    from mixture_experts_grouped_gb300 import moe
+    cfg = LAYER_CASES["tiny"]
+    inp = synth.make_inputs(cfg)
+    lay, _, _ = gpu_layer(cfg, inp, dev)
+    bad = torch.tensor([0, 64, 32, 96, 96, 96, 96, 96, 96], dtype=torch.int32, device=dev)
+    lay.err.zero_()
+    y_before = lay.y.clone()
+    moe.moe_grouped_down(lay.h, lay.act_code, lay.w_down.desc, bad, cfg.H, cfg.I, cfg.E, lay.max_padded, lay.y,
+                         lay.err)
+    torch.cuda.synchronize()
+    assert int(lay.err.item()) & moe.MOE_DEV_ERR_OFFSETS
+    assert torch.equal(lay.y.view(torch.int16), y_before.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: routing/align in full, FFN on sampled tokens
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,n_sample", [("mixtral_prefill", 24), ("fine_grained@T4096", 48),
+                                           ("fine_grained@T16384", 48)])
+def test_full_size_sampled(dev, name, n_sample):
+    cfg = _cfg(name)
+    inp = synth.make_inputs(cfg)
+    lay, _, _ = gpu_layer(cfg, inp, dev)
+    g = fetch(lay)
+    ref_ids, ref_w = orc.route_topk_softmax(inp["logits"], cfg.k, cfg.renormalize)
+    al = orc.align_block_size(ref_ids.reshape(-1), cfg.E, cfg.bs, lay.max_padded)
+    check_route_align_exact(g, ref_ids, ref_w, al)
+    assert g["err"] == 0
+    rng = np.random.default_rng(11)
+    tokens = np.sort(rng.choice(cfg.T, size=n_sample, replace=False))
+    ref = orc.moe_layer(inp["x"], cfg.act, inp["logits"], cfg.k, cfg.E, cfg.bs, inp["w_gate_up"], inp["w_down"],
+                        cfg.I, cfg.H, cfg.renormalize, tokens=tokens, max_padded=lay.max_padded)
+    pairs = (tokens[:, None] * cfg.k + np.arange(cfg.k)).reshape(-1)
+    rows = al.pair_to_row[pairs]
+    ffn_close(g["h"][rows], ref.h[rows], f"{name}: sampled h")
+    ffn_close(g["y"][rows], ref.y[rows], f"{name}: sampled y")
+    ffn_close(g["out"][tokens], ref.out, f"{name}: sampled output")
