@@ -1,0 +1,431 @@
+#!/usr/bin/env python3
+"""Throughput of the grouped MoE layer on GB300, one JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one batch: route -> align ->
+gate/up (+SiLU-mul) -> down -> (LoRA fold) -> combine, through the C ABI, with
+inputs and weights resident in HBM. The default workload is the Mixtral-style
+prefill layer (T=4096, H=4096, I=14336, E=8, top_k=2, block_size=64, bf16).
+Its 2.8 GB of expert weights stream from HBM every step, far more than the
+126 MB L2, so no L2 flush is needed between steps.
+
+Under torchrun (N > 1) every rank runs an independent replica of the layer on
+its own GPU (no data-path collective); the timed region is bracketed by
+barriers and the max over ranks is reported (weak scaling).
+
+--impl reference times the CPU oracle (plain numpy, fp64) on the host cores,
+each step a small sub-batch of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s and TFLOP/s or weight GB/s vs GB300 roofline, 1 GPU"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="mixtral_prefill")
+    ap.add_argument("--override", default="", help="comma-separated field=value changes, e.g. E=2,T=1024")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline time budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    return a
+
+
+def workload(name):
+    from mixture_experts_grouped_gb300 import synth
+    if "@T" in name:
+        base, t = name.split("@T")
+        return synth.CONFIGS[base].with_T(int(t))
+    return synth.CONFIGS[name]
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic(cfg, ids):
+    """FLOPs of the two GEMMs (padding excluded) and bytes of the experts the
+    routing touched (weights incl. scales / zeros) plus activation traffic."""
+    import numpy as np
+    P, H, I = cfg.P, cfg.H, cfg.I
+    flops_gate_up = 2.0 * P * H * 2 * I
+    flops_down = 2.0 * P * I * H
+    touched = int(np.unique(ids).shape[0])
+    if cfg.wfmt == "bf16":
+        per_expert = (2 * I * H + H * I) * 2
+    elif cfg.wfmt == "gptq":
+        G = cfg.group_size
+        per_expert = sum(K * N // 2 + (K // G) * N * 2 + (K // G) * (N // 8) * 4 for K, N in ((H, 2 * I), (I, H)))
+    else:
+        per_expert = sum(K * N // 2 + (K // 16) * N + 4 for K, N in ((H, 2 * I), (I, H)))
+    act = 2
+    act_bytes = (cfg.T * H * act          # x read (gather)
+                 + P * H * act * 2        # gathered rows written + read by the GEMM
+                 + P * I * act * 2        # h written + read
+                 + P * H * act * 2        # y written + read
+                 + cfg.T * H * act)       # out written
+    return {"flops_gate_up": flops_gate_up, "flops_down": flops_down, "flops": flops_gate_up + flops_down,
+            "touched_experts": touched, "weight_bytes": touched * per_expert,
+            "bytes": touched * per_expert + act_bytes}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                pw.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm_sorted = sorted(sm)
+        return {"sm_mhz": sm_sorted[len(sm_sorted) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(pw)}
+
+
+def traffic_for(kernel_key: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, valid only while the kernel source is the one that was profiled."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f).get(kernel_key)
+    except (OSError, ValueError):
+        return None
+    if not d:
+        return None
+    src = os.path.join(ROOT, d["source"])
+    try:
+        with open(src, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return d["bytes_per_launch"] if h == d["source_sha256_16"] else None
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_setup(cfg, inp=None):
+    import oracle as orc
+    from mixture_experts_grouped_gb300 import synth
+    if inp is None:
+        inp = synth.make_inputs(cfg)
+    wgu = orc.prepare_f64(inp["w_gate_up"])
+    wd = orc.prepare_f64(inp["w_down"])
+    return inp, wgu, wd
+
+
+def oracle_step(cfg, inp, wgu, wd, t0, n_tok):
+    """The whole oracle layer on tokens [t0, t0 + n_tok) of the workload."""
+    import oracle as orc
+    x = inp["x"][t0:t0 + n_tok]
+    lg = inp["logits"][t0:t0 + n_tok]
+    return orc.moe_layer(x, cfg.act, lg, cfg.k, cfg.E, cfg.bs, wgu, wd, cfg.I, cfg.H, cfg.renormalize,
+                         lora=inp["lora"])
+
+
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 0) for i in threadpool_info()), default=0)
+        if n:
+            return n
+    except ImportError:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(cfg, budget_s, inp=None):
+    inp, wgu, wd = oracle_setup(cfg, inp)
+    n_tok = 32 if cfg.T >= 32 else cfg.T
+    oracle_step(cfg, inp, wgu, wd, 0, n_tok)          # untimed warm-up
+    done, t_start, reps = 0, time.perf_counter(), 0
+    while True:
+        t0 = (reps * n_tok) % max(1, cfg.T - n_tok + 1)
+        oracle_step(cfg, inp, wgu, wd, t0, n_tok)
+        done += n_tok
+        reps += 1
+        el = time.perf_counter() - t_start
+        if el >= budget_s or reps >= 10000:
+            break
+    return {"value": done / el, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"{reps} sub-batches of {n_tok} consecutive tokens of the {cfg.name} workload "
+                      f"(whole layer per sub-batch, fp64 weights expanded before timing), {el:.1f} s"}
+
+
+def run_reference(args, cfg, rank, world):
+    base = {"impl": "reference", "metric": METRIC, "unit": "tokens/s", "higher_is_better": True,
+            "n_gpus": world, "scaling": "weak"}
+    if rank != 0:
+        return None
+    inp, wgu, wd = oracle_setup(cfg)
+    # size each step's sub-batch so that the whole run ends within about two minutes
+    t = time.perf_counter()
+    oracle_step(cfg, inp, wgu, wd, 0, 1)
+    per_token = max(time.perf_counter() - t, 1e-4)
+    n_tok = int(max(1, min(cfg.T, 120.0 / (per_token * (args.steps + args.warmup)))))
+    for i in range(args.warmup):
+        oracle_step(cfg, inp, wgu, wd, (i * n_tok) % max(1, cfg.T - n_tok + 1), n_tok)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        oracle_step(cfg, inp, wgu, wd, (i * n_tok) % max(1, cfg.T - n_tok + 1), n_tok)
+    el = time.perf_counter() - t
+    value = args.steps * n_tok / el
+    sample = (f"each step the whole oracle layer on {n_tok} consecutive tokens of the {cfg.name} workload "
+              f"(fp64 weights expanded before timing)")
+    base.update({"value": value, "steps": args.steps, "warmup": args.warmup,
+                 "ms_per_step": 1e3 * el / args.steps, "vs_baseline": None, "dtype": "f64",
+                 "data": "synthetic (seeded)", "config": config_dict(cfg, world),
+                 "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+                                  "sample": sample},
+                 "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}})
+    return base
+
+
+def config_dict(cfg, world):
+    return {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top_k={cfg.k} block_size={cfg.bs} "
+                        f"act={cfg.act} weights={cfg.wfmt}" + (f" lora_rank={cfg.lora_rank}" if cfg.lora_rank else ""),
+            "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "top_k": cfg.k, "block_size": cfg.bs,
+            "weights": cfg.wfmt, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (all expert weights stream from HBM every step)"}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args, cfg, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from mixture_experts_grouped_gb300 import build as B
+    from mixture_experts_grouped_gb300 import layer as L
+    from mixture_experts_grouped_gb300 import moe as M
+    from mixture_experts_grouped_gb300 import synth
+
+    if not os.path.exists(M.LIB_PATH):
+        B.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    inp = synth.make_inputs(cfg)
+    wgu = L.upload_weight(inp["w_gate_up"], cfg.act, dev)
+    wd = L.upload_weight(inp["w_down"], cfg.act, dev)
+    dl = L.upload_lora(inp["lora"], cfg.I, cfg.H, dev) if inp["lora"] is not None else None
+    lay = L.MoeLayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.bs, cfg.act, wgu, wd, dev, lora=dl,
+                     renormalize=cfg.renormalize)
+    x = L.act_tensor(inp["x"], cfg.act, dev)
+    logits = torch.from_numpy(inp["logits"]).to(dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        lay.forward(x, logits)
+    torch.cuda.synchronize()
+    if int(lay.err.item()) != 0:
+        raise RuntimeError(f"device error word {int(lay.err.item()):#x} after warm-up")
+    alg = algorithmic(cfg, lay.topk_ids.cpu().numpy())
+
+    # ---- device-timed region ----
+    ev_gu = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cvd = [c for c in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if c.strip()]
+    phys = int(cvd[local_rank]) if local_rank < len(cvd) and cvd[local_rank].strip().isdigit() else local_rank
+    clocks = ClockSampler(phys)
+    barrier()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler attach
+    n_launch0 = M.moe_launch_count()
+    t_start.record(stream)
+    for i in range(args.steps):
+        lay.route(logits)
+        lay.align()
+        ev_gu[i][0].record(stream)
+        lay.gate_up(x)
+        ev_gu[i][1].record(stream)
+        lay.down()
+        lay.lora_fold()
+        lay.combine()
+    t_end.record(stream)
+    barrier()
+    n_launch = M.moe_launch_count() - n_launch0
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    gu_ms = sum(a.elapsed_time(b) for a, b in ev_gu) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    tokens_per_s = world * cfg.T * args.steps / (ms / 1e3)
+
+    # ---- end to end through the public API: pinned host in, host out ----
+    x_host = x.cpu().pin_memory()
+    lg_host = logits.cpu().pin_memory()
+    out_host = torch.empty(lay.out.shape, dtype=lay.out.dtype).pin_memory()
+    x_dev = torch.empty_like(x)
+    lg_dev = torch.empty_like(logits)
+    n_e2e = max(3, min(args.steps, 200))
+    for _ in range(3):
+        x_dev.copy_(x_host, non_blocking=True)
+        lg_dev.copy_(lg_host, non_blocking=True)
+        lay.forward(x_dev, lg_dev)
+        out_host.copy_(lay.out, non_blocking=True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        x_dev.copy_(x_host, non_blocking=True)
+        lg_dev.copy_(lg_host, non_blocking=True)
+        lay.forward(x_dev, lg_dev)
+        out_host.copy_(lay.out, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * cfg.T * n_e2e / (e2e_ms / 1e3)
+    if int(lay.err.item()) != 0:
+        raise RuntimeError(f"device error word {int(lay.err.item()):#x}")
+    if rank != 0:
+        return None
+
+    pk, pk_kind = peaks()
+    peak_tf = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    achieved_tf = alg["flops_gate_up"] / (gu_ms / 1e3) / 1e12
+    tflops = alg["flops"] / (ms_per_step / 1e3) / 1e12
+    weight_gbs = alg["weight_bytes"] / (ms_per_step / 1e3) / 1e9
+    hbm = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    layer_frac = max(tflops / peak_tf, (alg["bytes"] / (ms_per_step / 1e3) / 1e9) / hbm)
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg.act, "data": "synthetic (seeded)",
+        "config": config_dict(cfg, world),
+        "tflops": tflops, "weight_gbs": weight_gbs, "layer_roofline_frac": layer_frac,
+        "roofline": {"kernel": "moe_grouped_gate_up (activation gather + tcgen05 grouped GEMM, fused SiLU-mul)",
+                     "bound": "tensor", "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved_tf / peak_tf, "peak_kind": f"bf16 dense sustained, {pk_kind}",
+                     "traffic": traffic_for("grouped_gemm_gate_up"),
+                     "ms_per_launch": gu_ms, "flops_per_launch": alg["flops_gate_up"]},
+        "e2e": {"value": e2e_value, "unit": "tokens/s",
+                "h2d_bytes_per_step": x_host.numel() * x_host.element_size() + lg_host.numel() * 4,
+                "d2h_bytes_per_step": out_host.numel() * out_host.element_size(), "steps": n_e2e},
+        "gpu_launches": int(n_launch),
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds, inp)
+    return line
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = workload(args.workload)
+    if args.override:
+        from dataclasses import replace
+        kv = dict(item.split("=") for item in args.override.split(","))
+        cfg = replace(cfg, name=f"{cfg.name}[{args.override}]",
+                      **{k: type(getattr(cfg, k))(v) for k, v in kv.items()})
+    if args.impl == "reference":
+        line = run_reference(args, cfg, rank, world)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        line = run_ours(args, cfg, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -215,9 +215,10 @@ size_t moe_gate_up_workspace_size(int32_t max_padded, int32_t H);
  *   h_out             device act [max_padded, I] out
  *   err_word          device i32 or NULL
  *   workspace         device, >= moe_gate_up_workspace_size bytes, 128-byte aligned
- * Requirements: H % 64 == 0, I % 8 == 0, E <= MOE_MAX_EXPERTS, all tensor
- * base addresses 16-byte aligned; GPTQ: (2I) % 8 == 0 and group_size a
- * multiple of 64 dividing H; NVFP4: H % 64 == 0.
+ * Requirements: H % 8 == 0, I % 8 == 0, E <= MOE_MAX_EXPERTS, all tensor
+ * base addresses 16-byte aligned; GPTQ: group_size a multiple of 64 dividing
+ * H; NVFP4: H % 16 == 0. A contraction that is not a multiple of 64 is
+ * zero-padded on chip.
  */
 int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* w_gate_up,
                         const int32_t* sorted_token_ids, const int32_t* expert_offsets,
@@ -232,8 +233,8 @@ int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* w_gate_up,
  *   h       device act [max_padded, I]
  *   w_down  host pointer to a MoeWeight with N = H, K = I
  *   y       device act [max_padded, H] out (rows past expert_offsets[E] untouched)
- * Requirements: I % 64 == 0, H % 8 == 0, 16-byte aligned tensors; GPTQ:
- * group_size a multiple of 64 dividing I.
+ * Requirements: I % 8 == 0, H % 8 == 0, 16-byte aligned tensors; GPTQ:
+ * group_size a multiple of 64 dividing I; NVFP4: I % 16 == 0.
  */
 int moe_grouped_down(const void* h, int32_t act, const MoeWeight* w_down,
                      const int32_t* expert_offsets, int32_t H, int32_t I, int32_t E,

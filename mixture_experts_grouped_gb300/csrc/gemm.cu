@@ -188,8 +188,8 @@ __device__ __forceinline__ void dequant_stage(uint8_t* bstage, const GemmParams&
             bool valid;
             const int wr = b_row<MODE>(n, t.n0, p.n_out, p.n_w, valid);
             uint4 v = make_uint4(0, 0, 0, 0);
-            if (valid) {
-                const int k0 = kb * BK + c * 8;
+            const int k0 = kb * BK + c * 8;
+            if (valid && k0 < p.K) {
                 const uint32_t bytes = __ldg(reinterpret_cast<const uint32_t*>(pk + static_cast<size_t>(wr) * (p.K / 2) + k0 / 2));
                 const float s = e4m3_to_f32(__ldg(sc + static_cast<size_t>(k0 / 16) * p.n_w + wr));
                 const __half2 s2 = __float2half2_rn(s);  // exact: an E4M3 value is an fp16 value
@@ -304,7 +304,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = s.tmem_base;
-    const int KB = p.K / BK;
+    const int KB = (p.K + BK - 1) / BK;  // a ragged last block is zero-filled
 
     if (warp == 0) {
         if (lane == 0) {
@@ -540,6 +540,7 @@ int check_weight(const MoeWeight* w, int act, int N, int K, const char* who) {
             return MOE_OK;
         case MOE_W_NVFP4:
             MOE_REQUIRE(w->w && w->scales && w->scale2, "%s: NVFP4 packed / scales / scale2 must be non-NULL", who);
+            MOE_REQUIRE(K % 16 == 0, "%s: NVFP4 needs K=%d divisible by 16 (one E4M3 scale per 16)", who, K);
             MOE_REQUIRE((reinterpret_cast<uintptr_t>(w->w) & 3) == 0, "%s: NVFP4 packed weight not 4-byte aligned",
                         who);
             return MOE_OK;
@@ -564,7 +565,7 @@ extern "C" int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* 
     MOE_REQUIRE(E >= 1 && E <= MOE_MAX_EXPERTS, "%s: E=%d outside [1, %d]", who, E, MOE_MAX_EXPERTS);
     MOE_REQUIRE(T >= 0 && top_k >= 1 && max_padded >= 0, "%s: bad T=%d / top_k=%d / max_padded=%d", who, T, top_k,
                 max_padded);
-    MOE_REQUIRE(H > 0 && H % 64 == 0, "%s: H=%d must be a positive multiple of 64", who, H);
+    MOE_REQUIRE(H > 0 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", who, H);
     MOE_REQUIRE(I > 0 && I % 8 == 0, "%s: I=%d must be a positive multiple of 8", who, I);
     int rc = moe::check_weight(w_gate_up, act, 2 * I, H, who);
     if (rc != MOE_OK) return rc;
@@ -622,7 +623,7 @@ extern "C" int moe_grouped_down(const void* h, int32_t act, const MoeWeight* w_d
                                 void* stream) {
     const char* who = "moe_grouped_down";
     MOE_REQUIRE(E >= 1 && E <= MOE_MAX_EXPERTS, "%s: E=%d outside [1, %d]", who, E, MOE_MAX_EXPERTS);
-    MOE_REQUIRE(I > 0 && I % 64 == 0, "%s: I=%d must be a positive multiple of 64", who, I);
+    MOE_REQUIRE(I > 0 && I % 8 == 0, "%s: I=%d must be a positive multiple of 8", who, I);
     MOE_REQUIRE(H > 0 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", who, H);
     MOE_REQUIRE(max_padded >= 0, "%s: max_padded=%d is negative", who, max_padded);
     int rc = moe::check_weight(w_down, act, H, I, who);

@@ -136,7 +136,9 @@ _E2M1_P = np.array([0.10, 0.16, 0.18, 0.16, 0.14, 0.12, 0.09, 0.05])
 def _nvfp4_weight(seed, tensor, E, N, K, n_scale2):
     """NVFP4 codes drawn directly: E2M1 magnitude codes from ``_E2M1_P`` with a
     random sign, E4M3 block scales with exponent field 5..9 and any mantissa
-    (values 0.25 .. 3.75, never NaN), fp32 ``scale2`` U(0.5, 1.5) * 2**-7."""
+    (values 0.25 .. 3.75, never NaN), fp32 ``scale2`` U(0.5, 1.5) * 0.003. The
+    E2M1 codes have RMS 2.34 and the block scales RMS 2.85, so the decoded
+    weights have RMS close to 0.02, the scale of the bf16 workloads."""
     if K % 16:
         raise ValueError("NVFP4 needs K % 16 == 0")
 
@@ -153,7 +155,7 @@ def _nvfp4_weight(seed, tensor, E, N, K, n_scale2):
         man = r.integers(0, 8, size=(K // 16, N), dtype=np.uint8)
         return ((ex << 3) | man).astype(np.uint8)
 
-    s2 = (_rng(seed, _S2, tensor).uniform(0.5, 1.5, size=(n_scale2, E)) * 2.0 ** -7).astype(np.float32)
+    s2 = (_rng(seed, _S2, tensor).uniform(0.5, 1.5, size=(n_scale2, E)) * 0.003).astype(np.float32)
     return {"format": "nvfp4", "packed": _per_expert(packed, E), "scales": _per_expert(scales, E),
             "scale2": s2}
 

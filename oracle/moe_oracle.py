@@ -39,7 +39,7 @@ __all__ = [
     "align_capacity", "route_topk_softmax", "warp_order_sum_f32",
     "align_block_size", "AlignResult", "ensure_group_arrays", "GroupArrayError",
     "e2m1_value", "e4m3_value", "dequant_bf16", "dequant_gptq", "dequant_nvfp4",
-    "expert_weight", "grouped_gate_up", "grouped_down", "lora_grouped_down",
+    "expert_weight", "prepare_f64", "grouped_gate_up", "grouped_down", "lora_grouped_down",
     "combine", "moe_layer", "LayerResult",
 ]
 
@@ -53,7 +53,8 @@ _BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """bf16 bit patterns (uint16) -> exact fp64 values (bf16 is the top half of f32)."""
     u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
-    return u.view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        return u.view(np.float32).astype(np.float64)
 
 
 def round_to_bf16(x) -> np.ndarray:
@@ -364,6 +365,8 @@ def expert_weight(spec: dict, e: int) -> np.ndarray:
     Spec dicts (stacked over experts, as the pages stack them):
 
     * ``{"format": "bf16", "w": uint16 [E, N, K]}``
+    * ``{"format": "f64", "w": list of fp64 [N, K]}``: weights already expanded
+      (e.g. by :func:`prepare_f64`), used as given
     * ``{"format": "gptq", "qweight": int32 [E, K/8, N], "scales": f16 [E, K/G, N],
       "qzeros": int32 [E, K/G, N/8], "group_size": G}``
     * ``{"format": "nvfp4", "packed": uint8 [E, N, K/2], "scales": uint8 [E, K/16, N],
@@ -372,6 +375,8 @@ def expert_weight(spec: dict, e: int) -> np.ndarray:
       and ``S = 1`` otherwise.
     """
     fmt = spec["format"]
+    if fmt == "f64":
+        return spec["w"][e]
     if fmt == "bf16":
         return dequant_bf16(spec["w"][e])
     if fmt == "gptq":
@@ -386,6 +391,13 @@ def expert_weight(spec: dict, e: int) -> np.ndarray:
             row_s2 = np.full(N, s2[0, e], dtype=np.float32)
         return dequant_nvfp4(spec["packed"][e], spec["scales"][e], row_s2)
     raise ValueError(f"unknown weight format {fmt!r}")
+
+
+def prepare_f64(spec: dict) -> dict:
+    """Expand every expert of a weight spec to fp64 once (exact for all three
+    formats), so repeated layer calls skip the per-call dequantisation."""
+    E = next(v for k, v in spec.items() if k in ("w", "qweight", "packed")).__len__()
+    return {"format": "f64", "w": [expert_weight(spec, e) for e in range(E)]}
 
 
 # ----------------------------------------------------------------------------

@@ -149,3 +149,14 @@ def test_expert_weight_nvfp4_gate_up_scale2_split():
     W1 = orc.expert_weight(spec, 1)
     np.testing.assert_array_equal(W1[:2], np.full((2, K), 2.0))   # gate rows: scale2[0, 1]
     np.testing.assert_array_equal(W1[2:], np.full((2, K), 4.0))   # up rows: scale2[1, 1]
+
+
+def test_prepared_f64_weights_are_the_dequantised_values():
+    from mixture_experts_grouped_gb300 import synth
+    for wfmt, act in (("bf16", "bf16"), ("gptq", "f16"), ("nvfp4", "bf16")):
+        cfg = synth.MoeConfig("p", T=4, H=64, I=64, E=3, k=1, bs=4, wfmt=wfmt, act=act, router="normal",
+                              group_size=64)
+        w = synth.make_weights(cfg)["w_gate_up"]
+        pre = orc.prepare_f64(w)
+        for e in range(3):
+            np.testing.assert_array_equal(orc.expert_weight(pre, e), orc.expert_weight(w, e))
