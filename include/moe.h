@@ -192,6 +192,29 @@ int moe_align_block_size(const int32_t* topk_ids, int32_t P, int32_t E, int32_t 
                          int32_t* pair_to_row, int32_t* err_word, void* workspace,
                          size_t workspace_bytes, void* stream);
 
+/*
+ * moe_align_block_size without a workspace argument, for callers that cannot
+ * allocate device memory (for example an application whose framework owns
+ * the whole device memory budget and gives out no allocator, or a caller that
+ * must not make an allocation call, which can synchronise the device, on its
+ * hot path). The source pages have no counterpart of this call.
+ *
+ * Same arguments, outputs and errors as moe_align_block_size, minus the
+ * workspace. The scratch is a fixed array inside the library, sized for
+ * P <= MOE_ALIGN_NOALLOC_MAX_PAIRS pairs and E <= MOE_MAX_EXPERTS experts
+ * (about 1.1 MiB held on every GPU that loads the library until exit); a
+ * larger P is rejected with MOE_ERR_INVALID. The first call on a device looks
+ * up the array's device address with that device current, so make that first
+ * call before any stream capture. Nothing is allocated or freed. All calls on
+ * a device share the array: calls that overlap on the GPU (unordered streams)
+ * race on it. Nothing in it needs to start at zero.
+ */
+#define MOE_ALIGN_NOALLOC_MAX_PAIRS 262144
+int moe_align_block_size_noalloc(const int32_t* topk_ids, int32_t P, int32_t E, int32_t block_size,
+                                 int32_t max_padded, int32_t* sorted_token_ids, int32_t* expert_ids,
+                                 int32_t* expert_offsets, int32_t* total_tokens_post_pad,
+                                 int32_t* pair_to_row, int32_t* err_word, void* stream);
+
 /* ---- a3 / a4: grouped GEMMs ----------------------------------------------- */
 
 /* Bytes of device workspace moe_grouped_gate_up needs (the gathered copy of

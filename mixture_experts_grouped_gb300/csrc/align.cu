@@ -17,6 +17,8 @@
 //   2. scan (one block): per expert, the exclusive prefix over chunks, the
 //      padded span, the prefix over experts, expert_ids, sentinels, the tail.
 //   3. scatter: row = base[chunk][expert] + rank in chunk.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -197,4 +199,77 @@ extern "C" int moe_align_block_size(const int32_t* topk_ids, int32_t P, int32_t 
     }
     moe::count_launch(launches);
     return moe::check_launch("moe_align_block_size");
+}
+
+// ---------------------------------------------------------------------------
+// Fixed-scratch variant for callers that cannot allocate device memory.
+//
+// Some callers of this library have no way to allocate device memory for the
+// align workspace: an application whose framework has taken the whole device
+// memory budget into its own pool and hands out no allocator, or a
+// latency-critical caller that must not make an allocation call (which can
+// synchronise the device) on its hot path. For them,
+// moe_align_block_size_noalloc runs the same three align kernels with their
+// scratch in the fixed array below instead of a caller-provided workspace.
+//
+// The array is sized for MOE_ALIGN_NOALLOC_MAX_PAIRS pairs and up to
+// MOE_MAX_EXPERTS experts (about 1.1 MiB). Every GPU that loads this library
+// holds it until the process exits. All calls on a device share it and it
+// keeps the previous call's contents; the kernels overwrite every word they
+// read in the same call, so nothing needs clearing. Two calls whose work
+// overlaps on the GPU (different streams, no ordering between them) race on
+// the array and may produce wrong results.
+// ---------------------------------------------------------------------------
+
+namespace {
+constexpr size_t kNoAllocChunks =
+    (static_cast<size_t>(MOE_ALIGN_NOALLOC_MAX_PAIRS) + moe::kChunk - 1) / moe::kChunk;
+constexpr size_t kNoAllocScratchBytes =
+    (kNoAllocChunks * MOE_MAX_EXPERTS * sizeof(int32_t) + 255) / 256 * 256 +
+    static_cast<size_t>(MOE_ALIGN_NOALLOC_MAX_PAIRS) * sizeof(int32_t) + 256;
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_align_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[256] = {};  // device address of the array, per device ordinal
+
+// Looked up once per device, with that device current: in host code the
+// array's name is only a host-side stand-in, never a device address.
+int noalloc_scratch(void** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return moe::fail(MOE_ERR_CUDA, "moe_align_block_size_noalloc: cudaGetDevice: %s",
+                                           cudaGetErrorString(e));
+    if (dev < 0 || dev >= 256) return moe::fail(MOE_ERR_UNSUPPORTED, "moe_align_block_size_noalloc: device %d", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_align_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return moe::fail(MOE_ERR_CUDA, "moe_align_block_size_noalloc: cudaGetSymbolAddress: %s",
+                             cudaGetErrorString(e));
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+}  // namespace
+
+extern "C" int moe_align_block_size_noalloc(const int32_t* topk_ids, int32_t P, int32_t E, int32_t block_size,
+                                            int32_t max_padded, int32_t* sorted_token_ids, int32_t* expert_ids,
+                                            int32_t* expert_offsets, int32_t* total_tokens_post_pad,
+                                            int32_t* pair_to_row, int32_t* err_word, void* stream) {
+    MOE_REQUIRE(P >= 0 && P <= MOE_ALIGN_NOALLOC_MAX_PAIRS,
+                "moe_align_block_size_noalloc: P=%d pairs is outside [0, %d], the size of the fixed scratch; "
+                "use moe_align_block_size with a workspace",
+                P, MOE_ALIGN_NOALLOC_MAX_PAIRS);
+    MOE_REQUIRE(E >= 1 && E <= MOE_MAX_EXPERTS, "moe_align_block_size_noalloc: num_experts=%d outside [1, %d]", E,
+                MOE_MAX_EXPERTS);
+    void* scratch = nullptr;
+    const int rc = noalloc_scratch(&scratch);
+    if (rc != MOE_OK) return rc;
+    return moe_align_block_size(topk_ids, P, E, block_size, max_padded, sorted_token_ids, expert_ids, expert_offsets,
+                                total_tokens_post_pad, pair_to_row, err_word, scratch, kNoAllocScratchBytes, stream);
 }

@@ -52,6 +52,8 @@ _SIGNATURES = {
     "moe_align_workspace_size": (c_size_t, [c_int32, c_int32]),
     "moe_align_block_size": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
                                        c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "moe_align_block_size_noalloc": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p,
+                                               c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "moe_gate_up_workspace_size": (c_size_t, [c_int32, c_int32]),
     "moe_grouped_gate_up": (c_int32, [c_void_p, c_int32, POINTER(MoeWeight), c_void_p, c_void_p, c_int32, c_int32,
                                       c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_size_t,
@@ -143,6 +145,19 @@ def moe_align_block_size(topk_ids, P, E, block_size, max_padded, sorted_token_id
         _ptr(topk_ids), P, E, block_size, max_padded, _ptr(sorted_token_ids), _ptr(expert_ids),
         _ptr(expert_offsets), _ptr(total_tokens_post_pad), _ptr(pair_to_row), _ptr(err_word), _ptr(workspace),
         workspace_bytes, _stream(stream)))
+
+
+MOE_ALIGN_NOALLOC_MAX_PAIRS = 262144
+
+
+def moe_align_block_size_noalloc(topk_ids, P, E, block_size, max_padded, sorted_token_ids, expert_ids,
+                                 expert_offsets, total_tokens_post_pad, pair_to_row, err_word, stream=None):
+    """moe_align_block_size for callers that cannot allocate device memory: the
+    scratch is a fixed array inside the library (P <= 262144 pairs). Calls on
+    one device share that array, so calls that overlap on the GPU race."""
+    _check("moe_align_block_size_noalloc", lib().moe_align_block_size_noalloc(
+        _ptr(topk_ids), P, E, block_size, max_padded, _ptr(sorted_token_ids), _ptr(expert_ids),
+        _ptr(expert_offsets), _ptr(total_tokens_post_pad), _ptr(pair_to_row), _ptr(err_word), _stream(stream)))
 
 
 def moe_gate_up_workspace_size(max_padded, H) -> int:
