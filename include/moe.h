@@ -229,39 +229,51 @@ size_t moe_gate_up_workspace_size(int32_t max_padded, int32_t H);
  * For every sorted row r of expert e holding pair p != P, t = p / top_k:
  *     h[r, n] = act( silu(x[t] . Wg_e[n]) * (x[t] . Wu_e[n]) ),  n < I,
  * with fp32 accumulation on the tensor cores and silu(g) = g / (1 + exp(-g)).
- * Padding rows get h = 0; rows at or past expert_offsets[E] are not written.
- * Tiles are scheduled on the device from expert_offsets (no host sync).
+ * Padding rows are not guaranteed to be written (tiles made only of padding
+ * rows are skipped); rows at or past expert_offsets[E] are not written. Tiles
+ * are scheduled on the device from expert_offsets (no host sync). Batches
+ * with few rows per expert (T * top_k / min(E, T * top_k) < 128) use the
+ * decode form of the kernel, in which the weights are the MMA's M operand
+ * and each tile covers one align block of rows.
  *   x                 device act [T, H]
  *   act               MOE_ACT_BF16 | MOE_ACT_F16
  *   w_gate_up         host pointer to a MoeWeight with N = 2*I, K = H
  *   sorted_token_ids, expert_offsets   device, from moe_align_block_size
+ *   block_size        the block_size the align step padded spans to
  *   h_out             device act [max_padded, I] out
  *   err_word          device i32 or NULL
  *   workspace         device, >= moe_gate_up_workspace_size bytes, 128-byte aligned
  * Requirements: H % 8 == 0, I % 8 == 0, E <= MOE_MAX_EXPERTS, all tensor
  * base addresses 16-byte aligned; GPTQ: group_size a multiple of 64 dividing
- * H; NVFP4: H % 16 == 0. A contraction that is not a multiple of 64 is
- * zero-padded on chip.
+ * H and I % 32 == 0; NVFP4: H % 32 == 0 and I % 16 == 0. A contraction that
+ * is not a multiple of 64 is zero-padded on chip.
  */
 int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* w_gate_up,
                         const int32_t* sorted_token_ids, const int32_t* expert_offsets,
                         int32_t T, int32_t top_k, int32_t H, int32_t I, int32_t E,
-                        int32_t max_padded, void* h_out, int32_t* err_word, void* workspace,
-                        size_t workspace_bytes, void* stream);
+                        int32_t block_size, int32_t max_padded, void* h_out, int32_t* err_word,
+                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Grouped down GEMM ([cutlass] nvfp4_grouped_down: the intermediate is already
  * in expert order, no gather, writes c [M_total, N]).
  *     y[r, n] = act( h[r] . Wd_e[n] ),  n < H, for rows r of expert e.
- *   h       device act [max_padded, I]
- *   w_down  host pointer to a MoeWeight with N = H, K = I
- *   y       device act [max_padded, H] out (rows past expert_offsets[E] untouched)
+ *   h                 device act [max_padded, I]
+ *   w_down            host pointer to a MoeWeight with N = H, K = I
+ *   sorted_token_ids  device, from moe_align_block_size (padding-only tiles
+ *                     are skipped; T * top_k is its sentinel)
+ *   block_size        the block_size the align step padded spans to
+ *   y                 device act [max_padded, H] out (padding rows and rows past
+ *                     expert_offsets[E] are not guaranteed to be written)
  * Requirements: I % 8 == 0, H % 8 == 0, 16-byte aligned tensors; GPTQ:
- * group_size a multiple of 64 dividing I; NVFP4: I % 16 == 0.
+ * group_size a multiple of 64 dividing I and H % 32 == 0; NVFP4: I % 32 == 0
+ * and H % 16 == 0.
  */
 int moe_grouped_down(const void* h, int32_t act, const MoeWeight* w_down,
-                     const int32_t* expert_offsets, int32_t H, int32_t I, int32_t E,
-                     int32_t max_padded, void* y, int32_t* err_word, void* stream);
+                     const int32_t* sorted_token_ids, const int32_t* expert_offsets,
+                     int32_t T, int32_t top_k, int32_t H, int32_t I, int32_t E,
+                     int32_t block_size, int32_t max_padded, void* y, int32_t* err_word,
+                     void* stream);
 
 /* ---- a5: LoRA fold ----------------------------------------------------------- */
 

@@ -17,6 +17,8 @@
 //   2. scan (one block): per expert, the exclusive prefix over chunks, the
 //      padded span, the prefix over experts, expert_ids, sentinels, the tail.
 //   3. scatter: row = base[chunk][expert] + rank in chunk.
+// Batches of at most one chunk (2048 pairs) run all three steps in a single
+// block instead, with the ranks kept in registers.
 #include <mutex>
 
 #include "common.cuh"
@@ -146,6 +148,102 @@ __global__ void align_scatter_kernel(const int32_t* __restrict__ ids, int P, int
     pair_to_row[p] = row;
 }
 
+// Small batches (P <= kChunk): the three steps in one block, ranks kept in
+// registers, no workspace. Same ordering rules, so the same result.
+__global__ void __launch_bounds__(32 * kWarps)
+align_single_block_kernel(const int32_t* __restrict__ ids, int P, int E, int bs, int max_padded,
+                          int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
+                          int32_t* __restrict__ offsets, int32_t* __restrict__ total_post_pad,
+                          int32_t* __restrict__ pair_to_row, int32_t* err) {
+    __shared__ int cnt[kWarps][MOE_MAX_EXPERTS];
+    __shared__ int s_span[MOE_MAX_EXPERTS];
+    __shared__ int s_off[MOE_MAX_EXPERTS];
+    __shared__ int s_total;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, e = threadIdx.x;
+    for (int i = threadIdx.x; i < kWarps * MOE_MAX_EXPERTS; i += blockDim.x) (&cnt[0][0])[i] = 0;
+    __syncthreads();
+    // 1. stable rank of every pair among same-expert pairs of its warp
+    const int base = warp * kPairsPerWarp;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    int my_id[kSteps], my_rank[kSteps];
+#pragma unroll
+    for (int st = 0; st < kSteps; ++st) {
+        const int p = base + st * 32 + lane;
+        int id = -1;
+        if (p < P) {
+            id = ids[p];
+            if (id < 0 || id >= E) {
+                set_err(err, MOE_DEV_ERR_EXPERT_ID);
+                id = -1;
+            }
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, id);
+        const int rank = __popc(peers & lt_mask);
+        int before = 0;
+        if (id >= 0) before = cnt[warp][id];
+        __syncwarp();
+        if (id >= 0 && rank == 0) cnt[warp][id] = before + __popc(peers);
+        __syncwarp();
+        my_id[st] = id;
+        my_rank[st] = before + rank;
+    }
+    __syncthreads();
+    // 2. per expert: warp bases, count, padded span; prefix over experts
+    int count = 0;
+    if (e < E) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const int c = cnt[w][e];
+            cnt[w][e] = count;
+            count += c;
+        }
+    }
+    const int span = (count + bs - 1) / bs * bs;
+    s_span[e] = (e < E) ? span : 0;
+    __syncthreads();
+    for (int d = 1; d < MOE_MAX_EXPERTS; d <<= 1) {
+        const int add = (e >= d) ? s_span[e - d] : 0;
+        __syncthreads();
+        s_span[e] += add;
+        __syncthreads();
+    }
+    const int off = s_span[e] - ((e < E) ? span : 0);
+    s_off[e] = off;
+    if (e == MOE_MAX_EXPERTS - 1) s_total = s_span[e];
+    __syncthreads();
+    const int total = s_total;
+    if (total > max_padded) {  // cannot happen when max_padded >= the capacity bound
+        if (e == 0) set_err(err, MOE_DEV_ERR_CAPACITY);
+        return;
+    }
+    if (e < E) {
+        offsets[e] = off;
+        for (int blk = off / bs; blk < (off + span) / bs; ++blk) expert_ids[blk] = e;
+        for (int r = off + count; r < off + span; ++r) sorted_ids[r] = P;
+    }
+    if (e == 0) {
+        offsets[E] = total;
+        total_post_pad[0] = total;
+    }
+    for (int r = total + e; r < max_padded; r += blockDim.x) sorted_ids[r] = P;
+    for (int blk = total / bs + e; blk < max_padded / bs; blk += blockDim.x) expert_ids[blk] = -1;
+    // 3. scatter
+#pragma unroll
+    for (int st = 0; st < kSteps; ++st) {
+        const int p = base + st * 32 + lane;
+        if (p < P) {
+            const int id = my_id[st];
+            if (id >= 0) {
+                const int row = s_off[id] + cnt[warp][id] + my_rank[st];
+                sorted_ids[row] = p;
+                pair_to_row[p] = row;
+            } else {
+                pair_to_row[p] = -1;
+            }
+        }
+    }
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -183,19 +281,20 @@ extern "C" int moe_align_block_size(const int32_t* topk_ids, int32_t P, int32_t 
     int32_t* rank_in_chunk = reinterpret_cast<int32_t*>(
         static_cast<char*>(workspace) + (static_cast<size_t>(nchunks) * E * sizeof(int32_t) + 255) / 256 * 256);
     int launches = 0;
-    if (nchunks > 0) {
+    if (nchunks <= 1) {
+        moe::align_single_block_kernel<<<1, 32 * moe::kWarps, 0, st>>>(topk_ids, P, E, block_size, max_padded,
+                                                                      sorted_token_ids, expert_ids, expert_offsets,
+                                                                      total_tokens_post_pad, pair_to_row, err_word);
+        ++launches;
+    } else {
         moe::align_count_rank_kernel<<<nchunks, 32 * moe::kWarps, 0, st>>>(topk_ids, P, E, chunk_counts,
                                                                           rank_in_chunk, err_word);
-        ++launches;
-    }
-    moe::align_scan_kernel<<<1, MOE_MAX_EXPERTS, 0, st>>>(P, E, block_size, max_padded, nchunks, chunk_counts,
-                                                         sorted_token_ids, expert_ids, expert_offsets,
-                                                         total_tokens_post_pad, err_word);
-    ++launches;
-    if (P > 0) {
+        moe::align_scan_kernel<<<1, MOE_MAX_EXPERTS, 0, st>>>(P, E, block_size, max_padded, nchunks, chunk_counts,
+                                                             sorted_token_ids, expert_ids, expert_offsets,
+                                                             total_tokens_post_pad, err_word);
         moe::align_scatter_kernel<<<(P + 255) / 256, 256, 0, st>>>(topk_ids, P, E, chunk_counts, rank_in_chunk,
                                                                   sorted_token_ids, pair_to_row);
-        ++launches;
+        launches += 3;
     }
     moe::count_launch(launches);
     return moe::check_launch("moe_align_block_size");

@@ -37,6 +37,10 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // box_rows x 64 elements (128 bytes, the 128-byte swizzle span).
 int make_tmap_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                  uint32_t box_rows, int act);
+// Encode a plain (unswizzled) 2-D tensor map of any element type: rows x cols
+// elements of elem_bytes each, box box_rows x box_cols.
+int make_tmap_2d_raw(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t rows,
+                     uint64_t cols, uint32_t box_cols, uint32_t box_rows);
 
 // ---------------------------------------------------------------------------
 // device side

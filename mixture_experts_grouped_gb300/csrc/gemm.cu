@@ -10,21 +10,28 @@
 // in the activation type).
 //
 // Design (sm_103a):
-//   * one persistent CTA per SM walks a static tile list; the list is built on
-//     the device from expert_offsets (per expert ceil(span / 128) row tiles x
-//     the column tiles), so there is no host synchronisation and the launch
-//     shape only depends on host-known sizes;
-//   * tile = 128 rows x 256 accumulator columns, K in steps of 64 (one
-//     128-byte swizzle span). Gate/up puts 128 gate and 128 up weight rows in
-//     one 256-row B tile, so each tcgen05.mma (M=128, N=256, K=16) produces
-//     both halves of 128 output columns and the epilogue can fuse silu*up;
-//   * warp 0 issues TMA loads into a 4-stage ring, one thread of warp 1 issues
-//     tcgen05.mma into one of two TMEM accumulators (2 x 256 columns), warps
-//     2-5 drain the other accumulator (tcgen05.ld -> activation -> global);
-//   * quantised weights (GPTQ int4, NVFP4) are dequantised by warps 6-9
-//     straight into the swizzled shared-memory B tile; activations still come
-//     by TMA. The NVFP4 global scale2 is applied to the f32 accumulator;
-//   * every mbarrier wait is bounded; on a timeout the CTA records
+//   * One persistent CTA per SM walks a static tile list built on the device
+//     from expert_offsets, so nothing on the host depends on the routing and
+//     the launch shape only depends on host-known sizes. Tiles whose first row
+//     is a padding row hold padding only (valid rows are a prefix of each
+//     span) and are skipped by every role of the CTA alike.
+//   * A tile is 256 weight rows (gate/up: 128 gate + 128 up rows of the same
+//     output columns, so the epilogue can fuse silu*up; down: 256 output
+//     columns) against a block of activation rows, K in steps of 64 elements
+//     (one 128-byte swizzle span):
+//       - prefill form: 128 activation rows are the MMA's M operand and the 256
+//         weight rows its N operand (tcgen05.mma M=128, N=256, K=16);
+//       - decode form (few rows per expert): the operands swap; each half of
+//         the weight tile is an M=128 operand and the NTOK activation rows
+//         (16..128) the N operand, so a small batch does not pay for 128 rows.
+//   * Warp 0 issues TMA loads into a multi-stage ring; one thread of warp 1
+//     issues tcgen05.mma into one of two TMEM accumulators; warps 2-5 drain
+//     the other (tcgen05.ld -> activation -> global).
+//   * Quantised weights (GPTQ int4, NVFP4): warp 10 streams the raw bytes by
+//     TMA into a 6-deep ring of their own; warps 6-9 dequantise shared ->
+//     shared into the swizzled 16-bit weight tile the MMA reads. The NVFP4
+//     global scale2 is applied to the f32 accumulator.
+//   * Every mbarrier wait is bounded; on a timeout the CTA records
 //     MOE_DEV_ERR_TIMEOUT, lets in-flight copies and MMAs land, frees TMEM and
 //     returns.
 #include "common.cuh"
@@ -32,38 +39,37 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int BN = 256;  // MMA N
-constexpr int STAGES = 4;
-constexpr int A_STAGE = BM * BK * 2;  // 16 KB
-constexpr int B_STAGE = BN * BK * 2;  // 32 KB
-constexpr int ACC_COLS = 256;
-constexpr int TMEM_COLS = 512;
+constexpr int W_ROWS = 256;             // weight rows per tile
+constexpr int W_STAGE = W_ROWS * BK * 2;  // 32 KB
+constexpr int RAW_STAGE = 9216;         // raw quantised bytes of one weight stage
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_DQ_WARPS = 4;
+constexpr int MAX_STAGES = 8;
+constexpr int SMEM_LIMIT = 232448;      // dynamic shared memory per block (227 KB)
 
 enum { MODE_GATE_UP = 0, MODE_DOWN = 1 };
 
 struct GemmParams {
-    const int32_t* offsets;  // [E + 1]
+    const int32_t* offsets;     // [E + 1]
+    const int32_t* sorted_ids;  // [max_padded]: pair ids, sentinel P
+    int P;
     int E;
     int K;          // contraction length
     int n_out;      // output columns: I (gate/up) or H (down)
     int n_w;        // weight rows per expert: 2I or H
     int max_padded;
     void* out;      // [max_padded, n_out]
-    const void* qw; // quantised weight payload
-    const void* qs; // scales
-    const void* qz; // GPTQ zeros
     const float* scale2;
     int group_size;
     int32_t* err;
 };
 
 struct SmemTail {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[MAX_STAGES];
+    uint64_t empty[MAX_STAGES];
+    uint64_t raw_full[MAX_STAGES];
+    uint64_t raw_empty[MAX_STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t mma_done;
@@ -75,18 +81,42 @@ struct SmemTail {
     int tstart[MOE_MAX_EXPERTS + 1];
 };
 
-constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + static_cast<int>(sizeof(SmemTail)) + 1024;
+constexpr int TAIL_BYTES = (static_cast<int>(sizeof(SmemTail)) + 127) / 128 * 128;
 
-template <int MODE>
-__host__ __device__ constexpr int out_cols_per_tile() {
-    return MODE == MODE_GATE_UP ? 128 : 256;
+__host__ __device__ constexpr int pow2_at_least(int v) {
+    int p = 32;
+    while (p < v) p <<= 1;
+    return p;
 }
+
+// Compile-time shape of one kernel instantiation. NTOK == 0: prefill form;
+// NTOK > 0: decode form with NTOK activation rows per tile.
+template <int MODE, int WFMT, int ACT, int NTOK>
+struct Shape {
+    static constexpr bool SWAP = NTOK > 0;
+    static constexpr bool QUANT = WFMT != MOE_W_BF16;
+    static constexpr int XROWS = SWAP ? NTOK : 128;
+    static constexpr int X_STAGE = XROWS * BK * 2;
+    static constexpr int RSTAGES = QUANT ? 6 : 0;
+    static constexpr int AVAIL = SMEM_LIMIT - 1024 - TAIL_BYTES - RSTAGES * RAW_STAGE;
+    static constexpr int STAGES = (AVAIL / (X_STAGE + W_STAGE)) < MAX_STAGES ? AVAIL / (X_STAGE + W_STAGE) : MAX_STAGES;
+    static constexpr int ACC = SWAP ? 2 * NTOK : 256;  // TMEM columns per accumulator
+    static constexpr int TMEM_COLS = pow2_at_least(2 * ACC);
+    static constexpr int OUT_COLS = MODE == MODE_GATE_UP ? 128 : 256;  // output columns per tile
+    static constexpr int THREADS = 192 + (QUANT ? 32 * (NUM_DQ_WARPS + 1) : 0);
+    static constexpr int SMEM = 1024 + STAGES * (X_STAGE + W_STAGE) + RSTAGES * RAW_STAGE + TAIL_BYTES;
+    static constexpr int RAW_BYTES = WFMT == MOE_W_GPTQ_INT4 ? 8832 : 9216;
+    static_assert(STAGES >= 2, "not enough shared memory for two stages");
+    static_assert(TMEM_COLS <= 512, "accumulators exceed TMEM");
+    static_assert(SMEM <= SMEM_LIMIT, "shared memory over the limit");
+};
 
 struct TileInfo {
     int e, m0, n0, rows;
 };
 
-__device__ __forceinline__ TileInfo decode_tile(const SmemTail& s, int E, int tile, int cols_per_tile) {
+template <int XROWS>
+__device__ __forceinline__ TileInfo decode_tile(const SmemTail& s, int E, int tile, int out_cols) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -95,30 +125,40 @@ __device__ __forceinline__ TileInfo decode_tile(const SmemTail& s, int E, int ti
     TileInfo t;
     t.e = lo;
     const int span = s.off[lo + 1] - s.off[lo];
-    const int mt = (span + BM - 1) / BM;
+    const int mt = (span + XROWS - 1) / XROWS;
     const int local = tile - s.tstart[lo];
     const int n_tile = local / mt;
     const int m_tile = local - n_tile * mt;
-    t.m0 = s.off[lo] + m_tile * BM;
-    t.n0 = n_tile * cols_per_tile;
-    t.rows = min(BM, s.off[lo + 1] - t.m0);
+    t.m0 = s.off[lo] + m_tile * XROWS;
+    t.n0 = n_tile * out_cols;
+    t.rows = min(XROWS, s.off[lo + 1] - t.m0);
     return t;
 }
 
-// ---- dequantisation of one B stage (256 weight rows x 64 k) ----------------
+// a tile whose first row is a padding row holds padding only
+__device__ __forceinline__ bool tile_is_padding(const GemmParams& p, const TileInfo& t) {
+    return __ldg(p.sorted_ids + t.m0) == p.P;
+}
 
-// weight row of B-tile row n (gate/up: rows [0,128) gate, [128,256) up)
+// weight-tile row n (0..255) -> output column it feeds, and whether that column exists
 template <int MODE>
-__device__ __forceinline__ int b_row(int n, int n0, int n_out, int n_w, bool& valid) {
-    if (MODE == MODE_GATE_UP) {
-        const int c = n0 + (n & 127);
-        valid = c < n_out;
-        return (n < 128) ? c : n_out + c;
-    } else {
-        const int c = n0 + n;
-        valid = c < n_w;
-        return c;
-    }
+__device__ __forceinline__ int out_col(int n, int n0) {
+    return MODE == MODE_GATE_UP ? n0 + (n & 127) : n0 + n;
+}
+
+// global weight row (or column, for GPTQ's [K/8, N] layout) of each half of a tile
+template <int MODE>
+__device__ __forceinline__ void half_bases(const GemmParams& p, int n0, int& c0, int& c1) {
+    c0 = n0;
+    c1 = (MODE == MODE_GATE_UP) ? p.n_out + n0 : n0 + 128;
+}
+
+// ---- dequantisation: raw shared bytes -> swizzled 16-bit weight tile -------------
+
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "r"(byte));
+    return r;
 }
 
 __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
@@ -130,13 +170,6 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
     return (b & 0x80u) ? -v : v;
 }
 
-// two E2M1 codes (low nibble first) -> f16x2, low half = low nibble
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-    uint32_t r;
-    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "r"(byte));
-    return r;
-}
-
 template <int ACT>
 __device__ __forceinline__ uint32_t f16x2_to_act2(uint32_t h2) {
     if (ACT == MOE_ACT_F16) return h2;
@@ -144,65 +177,93 @@ __device__ __forceinline__ uint32_t f16x2_to_act2(uint32_t h2) {
     return Act<MOE_ACT_BF16>::pack2(f.x, f.y);
 }
 
-template <int MODE, int WFMT, int ACT>
-__device__ __forceinline__ void dequant_stage(uint8_t* bstage, const GemmParams& p, const TileInfo& t, int kb,
-                                              int dq_tid) {
-    if (WFMT == MOE_W_GPTQ_INT4) {
-        // item = (packed k-row i in 0..7, tile row n in 0..255); consecutive
-        // threads take consecutive n: coalesced along the contiguous N axis
-        const int g = (kb * BK) / p.group_size;
-        const size_t kq_rows = static_cast<size_t>(p.K / 8);
-        const int32_t* qw = static_cast<const int32_t*>(p.qw) + static_cast<size_t>(t.e) * kq_rows * p.n_w;
-        const __half* qs = static_cast<const __half*>(p.qs) +
-                           (static_cast<size_t>(t.e) * (p.K / p.group_size) + g) * p.n_w;
-        const int32_t* qz = static_cast<const int32_t*>(p.qz) +
-                            (static_cast<size_t>(t.e) * (p.K / p.group_size) + g) * (p.n_w / 8);
-#pragma unroll 4
-        for (int it = 0; it < (BN * 8) / (NUM_DQ_WARPS * 32); ++it) {
-            const int idx = it * NUM_DQ_WARPS * 32 + dq_tid;
-            const int i = idx >> 8, n = idx & 255;
-            bool valid;
-            const int wr = b_row<MODE>(n, t.n0, p.n_out, p.n_w, valid);
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (valid) {
-                const uint32_t word = static_cast<uint32_t>(__ldg(qw + (static_cast<size_t>(kb) * 8 + i) * p.n_w + wr));
-                const float s = __half2float(qs[wr]);
-                const int z = (static_cast<uint32_t>(__ldg(qz + wr / 8)) >> (4 * (wr & 7))) & 15;
-                float f[8];
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// 8 GPTQ codes of one word -> 8 weights (q - z) * s in the activation type, k order
+template <int ACT>
+__device__ __forceinline__ uint4 gptq_word(uint32_t w, int z, float s) {
+    uint4 v;
+    if (ACT == MOE_ACT_F16) {
+        // fp16 1024 + q from the code bits (exact), minus 1024 + z (exact), times s
+        // (one rounding): pairs (q0,q4), (q1,q5), (q2,q6), (q3,q7) first
+        const uint32_t m = 0x64006400u;
+        const uint32_t p0 = (w & 0x000F000Fu) | m;
+        const uint32_t p1 = ((w >> 4) & 0x000F000Fu) | m;
+        const uint32_t p2 = ((w >> 8) & 0x000F000Fu) | m;
+        const uint32_t p3 = ((w >> 12) & 0x000F000Fu) | m;
+        const __half2 zz = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400 | z)));
+        const __half2 ss = __float2half2_rn(s);
+        uint32_t r[4] = {p0, p1, p2, p3};
 #pragma unroll
-                for (int j = 0; j < 8; ++j) f[j] = static_cast<float>(static_cast<int>((word >> (4 * j)) & 15u) - z) * s;
-                v.x = Act<ACT>::pack2(f[0], f[1]);
-                v.y = Act<ACT>::pack2(f[2], f[3]);
-                v.z = Act<ACT>::pack2(f[4], f[5]);
-                v.w = Act<ACT>::pack2(f[6], f[7]);
-            }
-            *reinterpret_cast<uint4*>(bstage + n * 128 + ((i ^ (n & 7)) << 4)) = v;
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&r[i]), zz), ss);
+            r[i] = *reinterpret_cast<uint32_t*>(&h);
         }
-    } else {  // NVFP4: item = (tile row n, 8-element chunk c); 8 lanes per row
-        const uint8_t* pk = static_cast<const uint8_t*>(p.qw) + static_cast<size_t>(t.e) * p.n_w * (p.K / 2);
-        const uint8_t* sc = static_cast<const uint8_t*>(p.qs) + static_cast<size_t>(t.e) * (p.K / 16) * p.n_w;
+        v.x = prmt(r[0], r[1], 0x5410);  // (q0, q1)
+        v.y = prmt(r[2], r[3], 0x5410);  // (q2, q3)
+        v.z = prmt(r[0], r[1], 0x7632);  // (q4, q5)
+        v.w = prmt(r[2], r[3], 0x7632);  // (q6, q7)
+    } else {
+        float f[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = static_cast<float>(static_cast<int>((w >> (4 * j)) & 15u) - z) * s;
+        v.x = Act<ACT>::pack2(f[0], f[1]);
+        v.y = Act<ACT>::pack2(f[2], f[3]);
+        v.z = Act<ACT>::pack2(f[4], f[5]);
+        v.w = Act<ACT>::pack2(f[6], f[7]);
+    }
+    return v;
+}
+
+template <int MODE, int WFMT, int ACT>
+__device__ __forceinline__ void dequant_stage(uint8_t* wstage, const uint8_t* raw, const GemmParams& p,
+                                              const TileInfo& t, int dq_tid) {
+    if (WFMT == MOE_W_GPTQ_INT4) {
+        // raw: qweight [2 halves][8 packed k-rows][128 cols] int32, scales [2][128] fp16,
+        // zeros [2][16] int32. Thread = (half, column); 8 words per half.
+        const int c = dq_tid;  // column within each half
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int n = h * 128 + c;
+            const bool valid = out_col<MODE>(n, t.n0) < p.n_out;
+            const uint32_t* qw = reinterpret_cast<const uint32_t*>(raw + h * 4096);
+            const float s = __half2float(reinterpret_cast<const __half*>(raw + 8192 + h * 256)[c]);
+            const uint32_t zw = reinterpret_cast<const uint32_t*>(raw + 8704 + h * 128)[c >> 3];
+            const int z = (zw >> (4 * (c & 7))) & 15;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (valid) v = gptq_word<ACT>(qw[i * 128 + c], z, s);
+                *reinterpret_cast<uint4*>(wstage + n * 128 + ((i ^ (n & 7)) << 4)) = v;
+            }
+        }
+    } else {
+        // raw: packed [2 halves][128 rows][32 bytes], scales [2][4 k16-groups][128 rows] E4M3.
+        // Item = (half, row r, 8-element chunk cc); 8 consecutive threads read one row.
 #pragma unroll 4
-        for (int it = 0; it < (BN * 8) / (NUM_DQ_WARPS * 32); ++it) {
+        for (int it = 0; it < (W_ROWS * 8) / (NUM_DQ_WARPS * 32); ++it) {
             const int idx = it * NUM_DQ_WARPS * 32 + dq_tid;
-            const int n = idx >> 3, c = idx & 7;
-            bool valid;
-            const int wr = b_row<MODE>(n, t.n0, p.n_out, p.n_w, valid);
+            const int h = idx >> 10, r = (idx >> 3) & 127, cc = idx & 7;
+            const int n = h * 128 + r;
             uint4 v = make_uint4(0, 0, 0, 0);
-            const int k0 = kb * BK + c * 8;
-            if (valid && k0 < p.K) {
-                const uint32_t bytes = __ldg(reinterpret_cast<const uint32_t*>(pk + static_cast<size_t>(wr) * (p.K / 2) + k0 / 2));
-                const float s = e4m3_to_f32(__ldg(sc + static_cast<size_t>(k0 / 16) * p.n_w + wr));
-                const __half2 s2 = __float2half2_rn(s);  // exact: an E4M3 value is an fp16 value
+            if (out_col<MODE>(n, t.n0) < p.n_out) {
+                const uint32_t bytes = reinterpret_cast<const uint32_t*>(raw + h * 4096 + r * 32)[cc];
+                const float sc = e4m3_to_f32(raw[8192 + h * 512 + (cc >> 1) * 128 + r]);
+                const __half2 s2 = __float2half2_rn(sc);  // exact: an E4M3 value is an fp16 value
                 uint32_t o[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    uint32_t h = e2m1x2_to_f16x2((bytes >> (8 * j)) & 0xffu);
-                    __half2 prod = __hmul2(*reinterpret_cast<__half2*>(&h), s2);  // exact in fp16
+                    uint32_t e2 = e2m1x2_to_f16x2((bytes >> (8 * j)) & 0xffu);
+                    __half2 prod = __hmul2(*reinterpret_cast<__half2*>(&e2), s2);  // exact in fp16
                     o[j] = f16x2_to_act2<ACT>(*reinterpret_cast<uint32_t*>(&prod));
                 }
                 v = make_uint4(o[0], o[1], o[2], o[3]);
             }
-            *reinterpret_cast<uint4*>(bstage + n * 128 + ((c ^ (n & 7)) << 4)) = v;
+            *reinterpret_cast<uint4*>(wstage + n * 128 + ((cc ^ (n & 7)) << 4)) = v;
         }
     }
 }
@@ -219,31 +280,62 @@ __device__ __forceinline__ void store8(void* out, size_t elem_off, const float* 
     *reinterpret_cast<uint4*>(static_cast<typename Act<ACT>::T*>(out) + elem_off) = v;
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+// silu(g) * u = g / (1 + exp(-g)) * u with the fast exponential and reciprocal
+// (a few ulp of f32, far below the bf16 / fp16 rounding of the result); for
+// very negative g, exp(-g) = inf and the reciprocal is 0, so no NaN appears.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return g * __frcp_rn(1.0f + __expf(-g)) * u;
+}
+
+// Rows of the tile that hold a pair: padding rows only sit at the end of an
+// expert's span, so they are a suffix of the span's last tile. Each calling
+// warp finds the first padding row with a ballot over sorted_token_ids.
+__device__ __forceinline__ int valid_rows(const GemmParams& p, const SmemTail& s, const TileInfo& t, int lane) {
+    if (t.m0 + t.rows != s.off[t.e + 1]) return t.rows;  // not the span's last tile
+    for (int base = 0; base < t.rows; base += 32) {
+        const int r = base + lane;
+        const bool pad = r < t.rows && __ldg(p.sorted_ids + t.m0 + r) == p.P;
+        const unsigned m = __ballot_sync(0xffffffffu, pad);
+        if (m) return base + __ffs(m) - 1;
+    }
+    return t.rows;
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
 
 // ---- the kernel ------------------------------------------------------------------
 
-template <int MODE, int WFMT, int ACT>
-__global__ void __launch_bounds__(WFMT == MOE_W_BF16 ? 192 : 192 + 32 * NUM_DQ_WARPS, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const GemmParams p) {
+template <int MODE, int WFMT, int ACT, int NTOK>
+__global__ void __launch_bounds__(Shape<MODE, WFMT, ACT, NTOK>::THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                    const __grid_constant__ CUtensorMap tmR0, const __grid_constant__ CUtensorMap tmR1,
+                    const __grid_constant__ CUtensorMap tmR2, const GemmParams p) {
+    using S = Shape<MODE, WFMT, ACT, NTOK>;
+    constexpr int XROWS = S::XROWS, STAGES = S::STAGES, RSTAGES = S::RSTAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + STAGES * A_STAGE;
-    SmemTail& s = *reinterpret_cast<SmemTail*>(smem + STAGES * (A_STAGE + B_STAGE));
+    uint8_t* sX = smem;
+    uint8_t* sW = smem + STAGES * S::X_STAGE;
+    uint8_t* sR = sW + STAGES * W_STAGE;
+    SmemTail& s = *reinterpret_cast<SmemTail*>(sR + RSTAGES * RAW_STAGE);
     volatile int* abort_flag = &s.abort_flag;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int E = p.E;
-    constexpr int CPT = out_cols_per_tile<MODE>();
 
     // ---- tile list from expert_offsets ----
     for (int i = tid; i <= E; i += blockDim.x) s.off[i] = p.offsets[i];
     if (tid == 0) {
         s.abort_flag = 0;
-        s.nt = (p.n_out + CPT - 1) / CPT;
+        s.nt = (p.n_out + S::OUT_COLS - 1) / S::OUT_COLS;
     }
     __syncthreads();
     int bad = 0;
@@ -251,12 +343,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (tid == 0) bad |= (s.off[0] < 0) | (s.off[E] > p.max_padded);
     bad = __syncthreads_or(bad);
     if (warp == 0) {
-        // lane l owns experts [l * per, (l + 1) * per): local sums, warp scan, write exclusive prefix
+        // lane l owns experts [l * per, (l + 1) * per): local sums, warp scan, exclusive prefix
         const int per = (E + 31) / 32;
         int loc = 0;
         for (int j = 0; j < per; ++j) {
             const int e = lane * per + j;
-            if (e < E) loc += ((s.off[e + 1] - s.off[e] + BM - 1) / BM) * s.nt;
+            if (e < E) loc += ((s.off[e + 1] - s.off[e] + XROWS - 1) / XROWS) * s.nt;
         }
         int inc = loc;
 #pragma unroll
@@ -269,7 +361,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int e = lane * per + j;
             if (e < E) {
                 s.tstart[e] = run;
-                run += ((s.off[e + 1] - s.off[e] + BM - 1) / BM) * s.nt;
+                run += ((s.off[e + 1] - s.off[e] + XROWS - 1) / XROWS) * s.nt;
             }
         }
         if (lane == 31) s.n_tiles = bad ? 0 : inc;
@@ -278,8 +370,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (bad) set_err(p.err, MOE_DEV_ERR_OFFSETS);
 #pragma unroll
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(&s.full[i], 1 + (WFMT == MOE_W_BF16 ? 0 : NUM_DQ_WARPS));
+            mbar_init(&s.full[i], 1 + (S::QUANT ? NUM_DQ_WARPS : 0));
             mbar_init(&s.empty[i], 1);
+        }
+#pragma unroll
+        for (int i = 0; i < RSTAGES; ++i) {
+            mbar_init(&s.raw_full[i], 1);
+            mbar_init(&s.raw_empty[i], NUM_DQ_WARPS);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.tfull[i], 1);
@@ -293,12 +390,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (static_cast<int>(blockIdx.x) >= n_tiles) return;  // block-uniform: nothing allocated yet
 
     if (warp == 1) {
-        tmem_alloc(&s.tmem_base, TMEM_COLS);
+        tmem_alloc(&s.tmem_base, S::TMEM_COLS);
         tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmA);
-        if (WFMT == MOE_W_BF16) tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmX);
+        if (!S::QUANT) tma_prefetch_desc(&tmW);
     }
     tc_fence_before();
     __syncthreads();
@@ -308,55 +405,66 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer ----------------
+            // ---------------- TMA producer: activations (+ bf16 weights) ----------------
             uint32_t stage = 0, phase = 0;
             long issued = 0;
-            const uint32_t tx = (WFMT == MOE_W_BF16) ? (A_STAGE + B_STAGE) : A_STAGE;
-            for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
-                const TileInfo t = decode_tile(s, E, tile, CPT);
-                bool ok = true;
+            const uint32_t tx = S::QUANT ? S::X_STAGE : (S::X_STAGE + W_STAGE);
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+                const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
+                if (tile_is_padding(p, t)) continue;
+                int c0, c1;
+                half_bases<MODE>(p, t.n0, c0, c1);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
                     mbar_arrive_expect_tx(&s.full[stage], tx);
-                    tma_load_2d(sA + stage * A_STAGE, &tmA, kb * BK, t.m0, &s.full[stage]);
-                    if (WFMT == MOE_W_BF16) {
-                        uint8_t* b = sB + stage * B_STAGE;
-                        const int r0 = t.e * p.n_w + t.n0;
-                        const int r1 = (MODE == MODE_GATE_UP) ? r0 + p.n_out : r0 + 128;
-                        tma_load_2d(b, &tmB, kb * BK, r0, &s.full[stage]);
-                        tma_load_2d(b + B_STAGE / 2, &tmB, kb * BK, r1, &s.full[stage]);
+                    tma_load_2d(sX + stage * S::X_STAGE, &tmX, kb * BK, t.m0, &s.full[stage]);
+                    if (!S::QUANT) {
+                        uint8_t* w = sW + stage * W_STAGE;
+                        tma_load_2d(w, &tmW, kb * BK, t.e * p.n_w + c0, &s.full[stage]);
+                        tma_load_2d(w + W_STAGE / 2, &tmW, kb * BK, t.e * p.n_w + c1, &s.full[stage]);
                     }
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
-                if (!ok) break;
             }
-            // let every copy still in flight land before the CTA may exit
+            // let the copies still in flight land before the CTA may exit
             const long first = issued > STAGES ? issued - STAGES : 0;
             for (long j = first; j < issued; ++j)
-                mbar_drain(&s.full[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1), kWaitLimitNs);
+                mbar_drain(&s.full[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1), kWaitLimitNs / 8);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
-            constexpr uint32_t idesc = f16_idesc(ACT, BM, BN);
+            constexpr uint32_t idesc = S::SWAP ? f16_idesc(ACT, 128, NTOK) : f16_idesc(ACT, 128, 256);
             uint32_t stage = 0, phase = 0;
             int local = 0;
-            for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+                const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
+                if (tile_is_padding(p, t)) continue;
                 const int acc = local & 1;
                 const uint32_t aph = (local >> 1) & 1;
+                ++local;
                 if (!mbar_wait(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
-                const uint32_t d = tmem_base + acc * ACC_COLS;
-                bool ok = true;
+                const uint32_t d = tmem_base + acc * S::ACC;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&s.full[stage], phase, abort_flag, p.err)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t ad = sw128_desc(smem_u32(sA + stage * A_STAGE));
-                    const uint64_t bd = sw128_desc(smem_u32(sB + stage * B_STAGE));
+                    const uint64_t xd = sw128_desc(smem_u32(sX + stage * S::X_STAGE));
+                    const uint64_t wd = sw128_desc(smem_u32(sW + stage * W_STAGE));
+                    if (S::SWAP) {
+                        const uint64_t wd1 = sw128_desc(smem_u32(sW + stage * W_STAGE + W_STAGE / 2));
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        tc_mma(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                        for (int k = 0; k < BK / 16; ++k) {
+                            tc_mma(d, wd + 2 * k, xd + 2 * k, idesc, (kb | k) != 0);
+                            tc_mma(d + NTOK, wd1 + 2 * k, xd + 2 * k, idesc, (kb | k) != 0);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) tc_mma(d, xd + 2 * k, wd + 2 * k, idesc, (kb | k) != 0);
+                    }
                     tc_commit(&s.empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -364,68 +472,98 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 tc_commit(&s.tfull[acc]);
             }
             tc_commit(&s.mma_done);
-            mbar_drain(&s.mma_done, 0, kWaitLimitNs);
+            mbar_drain(&s.mma_done, 0, kWaitLimitNs / 8);
         }
         __syncwarp();
     } else if (warp < 2 + NUM_EPI_WARPS) {
         // ---------------- epilogue ----------------
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int row = q * 32 + lane;
-        float s2a = 1.0f, s2b = 1.0f;
+        const int lrow = q * 32 + lane;
         int local = 0;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
+            if (tile_is_padding(p, t)) continue;
             const int acc = local & 1;
             const uint32_t aph = (local >> 1) & 1;
+            ++local;
             if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
             tc_fence_after();
-            const TileInfo t = decode_tile(s, E, tile, CPT);
+            float s2a = 1.0f, s2b = 1.0f;
             if (WFMT == MOE_W_NVFP4) {
-                if (MODE == MODE_GATE_UP) {
-                    s2a = __ldg(p.scale2 + t.e);
-                    s2b = __ldg(p.scale2 + p.E + t.e);
-                } else {
-                    s2a = __ldg(p.scale2 + t.e);
-                }
+                s2a = __ldg(p.scale2 + t.e);
+                s2b = (MODE == MODE_GATE_UP) ? __ldg(p.scale2 + p.E + t.e) : s2a;
             }
-            const bool row_ok = row < t.rows;
-            const size_t orow = static_cast<size_t>(t.m0 + row) * p.n_out;
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_COLS;
-            if (MODE == MODE_GATE_UP) {
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * S::ACC;
+            const int nvalid = valid_rows(p, s, t, lane);
+            if (!S::SWAP) {
+                // lane = activation row; columns = weight rows (gate | up, or 256 outputs)
+                const bool row_ok = lrow < nvalid;
+                const size_t orow = static_cast<size_t>(t.m0 + lrow) * p.n_out;
+                if (MODE == MODE_GATE_UP) {
 #pragma unroll 1
-                for (int c = 0; c < 128; c += 32) {
-                    uint32_t g[32], u[32];
-                    tmem_ld32(taddr + c, g);
-                    tmem_ld32(taddr + 128 + c, u);
-                    tmem_ld_wait();
-                    if (row_ok) {
+                    for (int c = 0; c < 128; c += 32) {
+                        uint32_t g[32], u[32];
+                        tmem_ld32(taddr + c, g);
+                        tmem_ld32(taddr + 128 + c, u);
+                        tmem_ld_wait();
+                        if (row_ok) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 8) {
-                            const int col = t.n0 + c + j;
-                            if (col < p.n_out) {
-                                float f[8];
+                            for (int j = 0; j < 32; j += 8) {
+                                const int col = t.n0 + c + j;
+                                if (col < p.n_out) {
+                                    float f[8];
 #pragma unroll
-                                for (int i = 0; i < 8; ++i)
-                                    f[i] = silu_mul(__uint_as_float(g[j + i]) * s2a, __uint_as_float(u[j + i]) * s2b);
-                                store8<ACT>(p.out, orow + col, f);
+                                    for (int i = 0; i < 8; ++i)
+                                        f[i] = silu_mul(__uint_as_float(g[j + i]) * s2a, __uint_as_float(u[j + i]) * s2b);
+                                    store8<ACT>(p.out, orow + col, f);
+                                }
+                            }
+                        }
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c = 0; c < 256; c += 32) {
+                        uint32_t g[32];
+                        tmem_ld32(taddr + c, g);
+                        tmem_ld_wait();
+                        if (row_ok) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 8) {
+                                const int col = t.n0 + c + j;
+                                if (col < p.n_out) {
+                                    float f[8];
+#pragma unroll
+                                    for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(g[j + i]) * s2a;
+                                    store8<ACT>(p.out, orow + col, f);
+                                }
                             }
                         }
                     }
                 }
             } else {
+                // lane = weight row of each half; columns = activation rows (tokens)
+                using T = typename Act<ACT>::T;
+                T* out = static_cast<T*>(p.out);
+                const int col_a = t.n0 + lrow;                                    // gate / low half
+                const int col_b = (MODE == MODE_GATE_UP) ? col_a : t.n0 + 128 + lrow;  // up / high half
 #pragma unroll 1
-                for (int c = 0; c < 256; c += 32) {
-                    uint32_t g[32];
-                    tmem_ld32(taddr + c, g);
+                for (int c = 0; c < NTOK && c < nvalid; c += 16) {
+                    uint32_t a[16], b[16];
+                    tmem_ld16(taddr + c, a);
+                    tmem_ld16(taddr + NTOK + c, b);
                     tmem_ld_wait();
-                    if (row_ok) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 8) {
-                            const int col = t.n0 + c + j;
-                            if (col < p.n_out) {
-                                float f[8];
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(g[j + i]) * s2a;
-                                store8<ACT>(p.out, orow + col, f);
+                    for (int j = 0; j < 16; ++j) {
+                        const int r = c + j;
+                        if (r < nvalid) {
+                            const size_t orow = static_cast<size_t>(t.m0 + r) * p.n_out;
+                            if (MODE == MODE_GATE_UP) {
+                                if (col_a < p.n_out)
+                                    out[orow + col_a] = Act<ACT>::from_f(
+                                        silu_mul(__uint_as_float(a[j]) * s2a, __uint_as_float(b[j]) * s2b));
+                            } else {
+                                if (col_a < p.n_out) out[orow + col_a] = Act<ACT>::from_f(__uint_as_float(a[j]) * s2a);
+                                if (col_b < p.n_out) out[orow + col_b] = Act<ACT>::from_f(__uint_as_float(b[j]) * s2a);
                             }
                         }
                     }
@@ -435,36 +573,89 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.tempty[acc]);
         }
-    } else {
-        // ---------------- dequantising producers (quantised weights only) ----------------
-        if (WFMT != MOE_W_BF16) {
+    } else if (warp < 2 + NUM_EPI_WARPS + NUM_DQ_WARPS) {
+        // ---------------- dequantising warps (quantised weights only) ----------------
+        if constexpr (S::QUANT) {
             const int dq_tid = tid - 32 * (2 + NUM_EPI_WARPS);
-            uint32_t stage = 0, phase = 0;
+            uint32_t stage = 0, phase = 0, rstage = 0, rphase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                const TileInfo t = decode_tile(s, E, tile, CPT);
+                const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
+                if (tile_is_padding(p, t)) continue;
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
-                    dequant_stage<MODE, WFMT, ACT>(sB + stage * B_STAGE, p, t, kb, dq_tid);
+                    if (!mbar_wait(&s.raw_full[rstage], rphase, abort_flag, p.err) ||
+                        !mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    dequant_stage<MODE, WFMT, ACT>(sW + stage * W_STAGE, sR + rstage * RAW_STAGE, p, t, dq_tid);
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&s.full[stage]);
+                    if (lane == 0) {
+                        mbar_arrive(&s.full[stage]);
+                        mbar_arrive(&s.raw_empty[rstage]);
+                    }
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    if (++rstage == RSTAGES) { rstage = 0; rphase ^= 1; }
                 }
             }
+        }
+    } else {
+        // ---------------- raw quantised-weight producer (warp 10) ----------------
+        if constexpr (S::QUANT) {
+          if (lane == 0) {
+            uint32_t rstage = 0, rphase = 0;
+            long issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+                const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
+                if (tile_is_padding(p, t)) continue;
+                int c0, c1;
+                half_bases<MODE>(p, t.n0, c0, c1);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&s.raw_empty[rstage], rphase ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    uint64_t* bar = &s.raw_full[rstage];
+                    uint8_t* r = sR + rstage * RAW_STAGE;
+                    mbar_arrive_expect_tx(bar, S::RAW_BYTES);
+                    if (WFMT == MOE_W_GPTQ_INT4) {
+                        const int kq = t.e * (p.K / 8) + kb * 8;
+                        const int g = t.e * (p.K / p.group_size) + (kb * BK) / p.group_size;
+                        tma_load_2d(r, &tmR0, c0, kq, bar);
+                        tma_load_2d(r + 4096, &tmR0, c1, kq, bar);
+                        tma_load_2d(r + 8192, &tmR1, c0, g, bar);
+                        tma_load_2d(r + 8448, &tmR1, c1, g, bar);
+                        tma_load_2d(r + 8704, &tmR2, c0 / 8, g, bar);
+                        tma_load_2d(r + 8832, &tmR2, c1 / 8, g, bar);
+                    } else {
+                        tma_load_2d(r, &tmR0, kb * (BK / 2), t.e * p.n_w + c0, bar);
+                        tma_load_2d(r + 4096, &tmR0, kb * (BK / 2), t.e * p.n_w + c1, bar);
+                        const int sg = t.e * (p.K / 16) + kb * (BK / 16);
+                        tma_load_2d(r + 8192, &tmR1, c0, sg, bar);
+                        tma_load_2d(r + 8704, &tmR1, c1, sg, bar);
+                    }
+                    ++issued;
+                    if (++rstage == RSTAGES) { rstage = 0; rphase ^= 1; }
+                }
+            }
+            const long first = issued > RSTAGES ? issued - RSTAGES : 0;
+            for (long j = first; j < issued; ++j)
+                mbar_drain(&s.raw_full[j % RSTAGES], static_cast<uint32_t>((j / RSTAGES) & 1), kWaitLimitNs / 8);
+          }
         }
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+    if (warp == 1) tmem_dealloc(tmem_base, S::TMEM_COLS);
 }
 
 // ---- gather of the activations into sorted-row order ---------------------------
 
-// xs[r] = x[sorted_token_ids[r] / top_k] for r < expert_offsets[E]; padding
-// rows (sentinel) are zero-filled. One warp per row, 16-byte vectors.
+// xs[r] = x[sorted_token_ids[r] / top_k] for r < expert_offsets[E]. Padding
+// rows are left as they are: the GEMM epilogues never store a padding row,
+// and a row of the MMA only feeds its own output row (or column). One warp
+// per row, 16-byte vectors.
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_ids,
                    const int32_t* __restrict__ offsets, int E, int T, int top_k, int vec_per_row, int max_padded,
@@ -476,74 +667,122 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sort
         int tok = -1;
         if (pid >= 0 && pid < P) tok = pid / top_k;
         else if (pid != P && (threadIdx.x & 31) == 0) set_err(err, MOE_DEV_ERR_PAIR_ID);
+        if (tok < 0) continue;
         uint4* dst = xs + static_cast<size_t>(r) * vec_per_row;
-        if (tok >= 0) {
-            const uint4* src = x + static_cast<size_t>(tok) * vec_per_row;
-            for (int v = threadIdx.x & 31; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
-        } else {
-            for (int v = threadIdx.x & 31; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
-        }
+        const uint4* src = x + static_cast<size_t>(tok) * vec_per_row;
+        for (int v = threadIdx.x & 31; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
     }
 }
 
-// ---- host launchers ----------------------------------------------------------------
+// ---- host side -------------------------------------------------------------------
 
-template <int MODE, int WFMT, int ACT>
-int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, cudaStream_t st,
-                const char* who) {
-    auto kernel = grouped_gemm_kernel<MODE, WFMT, ACT>;
+struct Maps {
+    CUtensorMap x, w, r0, r1, r2;
+};
+
+// Activation rows per tile. 0 selects the prefill form (128 rows as the MMA's
+// M operand), used when experts average 128 or more rows. Otherwise the decode
+// form takes one align block per tile (rounded up to a power of two, at least
+// 16): spans are whole blocks and only a span's last block holds padding, so
+// no tile is padding only and the tiles spread evenly over the CTAs.
+int pick_ntok(long P, int E, int block_size) {
+    const long touched = P < E ? P : E;
+    const long avg = touched > 0 ? P / touched : 0;
+    if (avg >= 128) return 0;
+    int nt = 16;
+    while (nt < block_size) nt <<= 1;
+    return nt <= 128 ? nt : 0;
+}
+
+template <int MODE, int WFMT, int ACT, int NTOK>
+int launch_gemm(const Maps& m, const GemmParams& p, cudaStream_t st, const char* who) {
+    using S = Shape<MODE, WFMT, ACT, NTOK>;
+    auto kernel = grouped_gemm_kernel<MODE, WFMT, ACT, NTOK>;
     static int configured_for = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_for != dev) {
-        int rc = set_smem_limit(reinterpret_cast<const void*>(kernel), SMEM_BYTES);
+        int rc = set_smem_limit(reinterpret_cast<const void*>(kernel), S::SMEM);
         if (rc != MOE_OK) return rc;
         configured_for = dev;
     }
-    constexpr int CPT = out_cols_per_tile<MODE>();
-    const long bound = static_cast<long>((p.max_padded + BM - 1) / BM + p.E) * ((p.n_out + CPT - 1) / CPT);
+    const long bound = static_cast<long>((p.max_padded + S::XROWS - 1) / S::XROWS + p.E) *
+                       ((p.n_out + S::OUT_COLS - 1) / S::OUT_COLS);
     const int sms = sm_count();
     if (sms <= 0) return fail(MOE_ERR_CUDA, "%s: cannot query the SM count", who);
     const int grid = static_cast<int>(bound < sms ? bound : sms);
     if (grid <= 0) return MOE_OK;
-    const int threads = (WFMT == MOE_W_BF16) ? 192 : 192 + 32 * NUM_DQ_WARPS;
-    kernel<<<grid, threads, SMEM_BYTES, st>>>(tmA, tmB, p);
+    kernel<<<grid, S::THREADS, S::SMEM, st>>>(m.x, m.w, m.r0, m.r1, m.r2, p);
     count_launch();
     return check_launch(who);
 }
 
-template <int MODE>
-int dispatch(int wfmt, int act, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
-             cudaStream_t st, const char* who) {
-    if (wfmt == MOE_W_BF16) return launch_gemm<MODE, MOE_W_BF16, MOE_ACT_BF16>(tmA, tmB, p, st, who);
-    if (wfmt == MOE_W_GPTQ_INT4)
-        return act == MOE_ACT_F16 ? launch_gemm<MODE, MOE_W_GPTQ_INT4, MOE_ACT_F16>(tmA, tmB, p, st, who)
-                                  : launch_gemm<MODE, MOE_W_GPTQ_INT4, MOE_ACT_BF16>(tmA, tmB, p, st, who);
-    return act == MOE_ACT_F16 ? launch_gemm<MODE, MOE_W_NVFP4, MOE_ACT_F16>(tmA, tmB, p, st, who)
-                              : launch_gemm<MODE, MOE_W_NVFP4, MOE_ACT_BF16>(tmA, tmB, p, st, who);
+template <int MODE, int WFMT, int ACT>
+int by_ntok(int ntok, const Maps& m, const GemmParams& p, cudaStream_t st, const char* who) {
+    switch (ntok) {
+        case 0: return launch_gemm<MODE, WFMT, ACT, 0>(m, p, st, who);
+        case 16: return launch_gemm<MODE, WFMT, ACT, 16>(m, p, st, who);
+        case 32: return launch_gemm<MODE, WFMT, ACT, 32>(m, p, st, who);
+        case 64: return launch_gemm<MODE, WFMT, ACT, 64>(m, p, st, who);
+        default: return launch_gemm<MODE, WFMT, ACT, 128>(m, p, st, who);
+    }
 }
 
-int check_weight(const MoeWeight* w, int act, int N, int K, const char* who) {
+template <int MODE>
+int dispatch(int wfmt, int act, int ntok, const Maps& m, const GemmParams& p, cudaStream_t st, const char* who) {
+    if (wfmt == MOE_W_BF16) return by_ntok<MODE, MOE_W_BF16, MOE_ACT_BF16>(ntok, m, p, st, who);
+    if (wfmt == MOE_W_GPTQ_INT4)
+        return act == MOE_ACT_F16 ? by_ntok<MODE, MOE_W_GPTQ_INT4, MOE_ACT_F16>(ntok, m, p, st, who)
+                                  : by_ntok<MODE, MOE_W_GPTQ_INT4, MOE_ACT_BF16>(ntok, m, p, st, who);
+    return act == MOE_ACT_F16 ? by_ntok<MODE, MOE_W_NVFP4, MOE_ACT_F16>(ntok, m, p, st, who)
+                              : by_ntok<MODE, MOE_W_NVFP4, MOE_ACT_BF16>(ntok, m, p, st, who);
+}
+
+// Checks the weight descriptor and encodes its tensor maps. N = weight rows
+// per expert, K = contraction, n_out = output columns (I for gate/up).
+int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Maps& m, const char* who) {
     MOE_REQUIRE(w != nullptr, "%s: NULL weight descriptor", who);
     MOE_REQUIRE(act == MOE_ACT_BF16 || act == MOE_ACT_F16, "%s: unknown activation type %d", who, act);
     switch (w->format) {
-        case MOE_W_BF16:
+        case MOE_W_BF16: {
             MOE_REQUIRE(act == MOE_ACT_BF16, "%s: a bf16 weight needs bf16 activations (the tensor cores take "
                                              "one 16-bit type for both operands)", who);
-            MOE_REQUIRE(w->w && aligned16(w->w), "%s: bf16 weight pointer NULL or not 16-byte aligned", who);
+            MOE_REQUIRE(w->w != nullptr, "%s: NULL bf16 weight", who);
+            int rc = make_tmap_2d(&m.w, w->w, static_cast<uint64_t>(E) * N, K, 128, act);
+            if (rc != MOE_OK) return rc;
+            m.r0 = m.r1 = m.r2 = m.w;
             return MOE_OK;
-        case MOE_W_GPTQ_INT4:
+        }
+        case MOE_W_GPTQ_INT4: {
             MOE_REQUIRE(w->w && w->scales && w->zeros, "%s: GPTQ qweight / scales / qzeros must be non-NULL", who);
-            MOE_REQUIRE(w->group_size >= 64 && w->group_size % 64 == 0 && K % w->group_size == 0,
-                        "%s: GPTQ group_size=%d must be a multiple of 64 dividing K=%d", who, w->group_size, K);
-            MOE_REQUIRE(N % 8 == 0, "%s: GPTQ needs N=%d divisible by 8", who, N);
-            return MOE_OK;
-        case MOE_W_NVFP4:
+            const int G = w->group_size;
+            MOE_REQUIRE(G >= 64 && G % 64 == 0 && K % G == 0,
+                        "%s: GPTQ group_size=%d must be a multiple of 64 dividing K=%d", who, G, K);
+            MOE_REQUIRE(n_out % 32 == 0, "%s: GPTQ needs %d output columns divisible by 32", who, n_out);
+            int rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4,
+                                      static_cast<uint64_t>(E) * (K / 8), N, 128, 8);
+            if (rc == MOE_OK)
+                rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                                      static_cast<uint64_t>(E) * (K / G), N, 128, 1);
+            if (rc == MOE_OK)
+                rc = make_tmap_2d_raw(&m.r2, w->zeros, CU_TENSOR_MAP_DATA_TYPE_INT32, 4,
+                                      static_cast<uint64_t>(E) * (K / G), N / 8, 16, 1);
+            m.w = m.r0;
+            return rc;
+        }
+        case MOE_W_NVFP4: {
             MOE_REQUIRE(w->w && w->scales && w->scale2, "%s: NVFP4 packed / scales / scale2 must be non-NULL", who);
-            MOE_REQUIRE(K % 16 == 0, "%s: NVFP4 needs K=%d divisible by 16 (one E4M3 scale per 16)", who, K);
-            MOE_REQUIRE((reinterpret_cast<uintptr_t>(w->w) & 3) == 0, "%s: NVFP4 packed weight not 4-byte aligned",
-                        who);
-            return MOE_OK;
+            MOE_REQUIRE(K % 32 == 0, "%s: NVFP4 needs K=%d divisible by 32", who, K);
+            MOE_REQUIRE(n_out % 16 == 0, "%s: NVFP4 needs %d output columns divisible by 16", who, n_out);
+            int rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(E) * N,
+                                      K / 2, 32, 128);
+            if (rc == MOE_OK)
+                rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                                      static_cast<uint64_t>(E) * (K / 16), N, 128, 4);
+            m.r2 = m.r1;
+            m.w = m.r0;
+            return rc;
+        }
         default:
             return fail(MOE_ERR_INVALID, "%s: unknown weight format %d", who, w->format);
     }
@@ -559,15 +798,18 @@ extern "C" size_t moe_gate_up_workspace_size(int32_t max_padded, int32_t H) {
 
 extern "C" int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* w_gate_up,
                                    const int32_t* sorted_token_ids, const int32_t* expert_offsets, int32_t T,
-                                   int32_t top_k, int32_t H, int32_t I, int32_t E, int32_t max_padded, void* h_out,
-                                   int32_t* err_word, void* workspace, size_t workspace_bytes, void* stream) {
+                                   int32_t top_k, int32_t H, int32_t I, int32_t E, int32_t block_size,
+                                   int32_t max_padded, void* h_out, int32_t* err_word, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
     const char* who = "moe_grouped_gate_up";
     MOE_REQUIRE(E >= 1 && E <= MOE_MAX_EXPERTS, "%s: E=%d outside [1, %d]", who, E, MOE_MAX_EXPERTS);
+    MOE_REQUIRE(block_size >= 1, "%s: block_size=%d must be positive", who, block_size);
     MOE_REQUIRE(T >= 0 && top_k >= 1 && max_padded >= 0, "%s: bad T=%d / top_k=%d / max_padded=%d", who, T, top_k,
                 max_padded);
     MOE_REQUIRE(H > 0 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", who, H);
     MOE_REQUIRE(I > 0 && I % 8 == 0, "%s: I=%d must be a positive multiple of 8", who, I);
-    int rc = moe::check_weight(w_gate_up, act, 2 * I, H, who);
+    moe::Maps m;
+    int rc = moe::weight_maps(w_gate_up, act, E, 2 * I, H, I, m, who);
     if (rc != MOE_OK) return rc;
     if (max_padded == 0) return MOE_OK;
     MOE_REQUIRE(x && sorted_token_ids && expert_offsets && h_out, "%s: NULL pointer", who);
@@ -576,12 +818,13 @@ extern "C" int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* 
     MOE_REQUIRE(workspace && workspace_bytes >= need && (reinterpret_cast<uintptr_t>(workspace) & 127) == 0,
                 "%s: workspace of %zu bytes (128-byte aligned) required, got %zu", who, need, workspace_bytes);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long P = static_cast<long>(T) * top_k;
+    const int ntok = moe::pick_ntok(P, E, block_size);
 
     // 1. gather activations into sorted-row order
     {
         const int sms = moe::sm_count();
-        const int rows_per_block = 8;
-        int blocks = (max_padded + rows_per_block - 1) / rows_per_block;
+        int blocks = (max_padded + 7) / 8;
         const int cap = sms > 0 ? sms * 8 : 1024;
         if (blocks > cap) blocks = cap;
         moe::gather_rows_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(x), sorted_token_ids,
@@ -592,67 +835,57 @@ extern "C" int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* 
         if (rc != MOE_OK) return rc;
     }
     // 2. the grouped GEMM
-    CUtensorMap tmA, tmB;
-    rc = moe::make_tmap_2d(&tmA, workspace, max_padded, H, 128, act);
+    rc = moe::make_tmap_2d(&m.x, workspace, max_padded, H, ntok ? ntok : 128, act);
     if (rc != MOE_OK) return rc;
-    if (w_gate_up->format == MOE_W_BF16) {
-        rc = moe::make_tmap_2d(&tmB, w_gate_up->w, static_cast<uint64_t>(E) * 2 * I, H, 128, act);
-        if (rc != MOE_OK) return rc;
-    } else {
-        tmB = tmA;
-    }
     moe::GemmParams p{};
     p.offsets = expert_offsets;
+    p.sorted_ids = sorted_token_ids;
+    p.P = static_cast<int>(P);
     p.E = E;
     p.K = H;
     p.n_out = I;
     p.n_w = 2 * I;
     p.max_padded = max_padded;
     p.out = h_out;
-    p.qw = w_gate_up->w;
-    p.qs = w_gate_up->scales;
-    p.qz = w_gate_up->zeros;
     p.scale2 = w_gate_up->scale2;
     p.group_size = w_gate_up->group_size;
     p.err = err_word;
-    return moe::dispatch<moe::MODE_GATE_UP>(w_gate_up->format, act, tmA, tmB, p, st, who);
+    return moe::dispatch<moe::MODE_GATE_UP>(w_gate_up->format, act, ntok, m, p, st, who);
 }
 
-extern "C" int moe_grouped_down(const void* h, int32_t act, const MoeWeight* w_down, const int32_t* expert_offsets,
-                                int32_t H, int32_t I, int32_t E, int32_t max_padded, void* y, int32_t* err_word,
+extern "C" int moe_grouped_down(const void* h, int32_t act, const MoeWeight* w_down, const int32_t* sorted_token_ids,
+                                const int32_t* expert_offsets, int32_t T, int32_t top_k, int32_t H, int32_t I,
+                                int32_t E, int32_t block_size, int32_t max_padded, void* y, int32_t* err_word,
                                 void* stream) {
     const char* who = "moe_grouped_down";
     MOE_REQUIRE(E >= 1 && E <= MOE_MAX_EXPERTS, "%s: E=%d outside [1, %d]", who, E, MOE_MAX_EXPERTS);
+    MOE_REQUIRE(block_size >= 1, "%s: block_size=%d must be positive", who, block_size);
+    MOE_REQUIRE(T >= 0 && top_k >= 1 && max_padded >= 0, "%s: bad T=%d / top_k=%d / max_padded=%d", who, T, top_k,
+                max_padded);
     MOE_REQUIRE(I > 0 && I % 8 == 0, "%s: I=%d must be a positive multiple of 8", who, I);
     MOE_REQUIRE(H > 0 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", who, H);
-    MOE_REQUIRE(max_padded >= 0, "%s: max_padded=%d is negative", who, max_padded);
-    int rc = moe::check_weight(w_down, act, H, I, who);
+    moe::Maps m;
+    int rc = moe::weight_maps(w_down, act, E, H, I, H, m, who);
     if (rc != MOE_OK) return rc;
     if (max_padded == 0) return MOE_OK;
-    MOE_REQUIRE(h && expert_offsets && y, "%s: NULL pointer", who);
+    MOE_REQUIRE(h && sorted_token_ids && expert_offsets && y, "%s: NULL pointer", who);
     MOE_REQUIRE(moe::aligned16(h) && moe::aligned16(y), "%s: h / y must be 16-byte aligned", who);
-    CUtensorMap tmA, tmB;
-    rc = moe::make_tmap_2d(&tmA, h, max_padded, I, 128, act);
+    const long P = static_cast<long>(T) * top_k;
+    const int ntok = moe::pick_ntok(P, E, block_size);
+    rc = moe::make_tmap_2d(&m.x, h, max_padded, I, ntok ? ntok : 128, act);
     if (rc != MOE_OK) return rc;
-    if (w_down->format == MOE_W_BF16) {
-        rc = moe::make_tmap_2d(&tmB, w_down->w, static_cast<uint64_t>(E) * H, I, 128, act);
-        if (rc != MOE_OK) return rc;
-    } else {
-        tmB = tmA;
-    }
     moe::GemmParams p{};
     p.offsets = expert_offsets;
+    p.sorted_ids = sorted_token_ids;
+    p.P = static_cast<int>(P);
     p.E = E;
     p.K = I;
     p.n_out = H;
     p.n_w = H;
     p.max_padded = max_padded;
     p.out = y;
-    p.qw = w_down->w;
-    p.qs = w_down->scales;
-    p.qz = w_down->zeros;
     p.scale2 = w_down->scale2;
     p.group_size = w_down->group_size;
     p.err = err_word;
-    return moe::dispatch<moe::MODE_DOWN>(w_down->format, act, tmA, tmB, p, static_cast<cudaStream_t>(stream), who);
+    return moe::dispatch<moe::MODE_DOWN>(w_down->format, act, ntok, m, p, static_cast<cudaStream_t>(stream), who);
 }

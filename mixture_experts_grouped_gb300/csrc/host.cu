@@ -90,6 +90,27 @@ int make_tmap_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
     return MOE_OK;
 }
 
+int make_tmap_2d_raw(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t rows,
+                     uint64_t cols, uint32_t box_cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    if (!aligned16(base)) return fail(MOE_ERR_INVALID, "tensor base address %p is not 16-byte aligned", base);
+    if ((cols * elem_bytes) % 16 != 0)
+        return fail(MOE_ERR_INVALID, "row pitch of %llu x %d bytes is not a 16-byte multiple",
+                    (unsigned long long)cols, elem_bytes);
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * static_cast<uint64_t>(elem_bytes)};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(MOE_ERR_INVALID, "cuTensorMapEncodeTiled failed (%d) for a %llux%llu tensor", (int)r,
+                    (unsigned long long)rows, (unsigned long long)cols);
+    return MOE_OK;
+}
+
 }  // namespace moe
 
 extern "C" {

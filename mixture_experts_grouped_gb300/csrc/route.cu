@@ -13,7 +13,8 @@ namespace moe {
 namespace {
 
 constexpr int kPerLane = MOE_MAX_EXPERTS / 32;  // 8
-constexpr int kRowsPerBlock = 8;               // 8 warps
+constexpr int kRowsPerBlock = 1;  // one warp per block: rows spread over every SM (the fp64
+                                   // exponential runs on few units per SM)
 
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
     return va > vb || (va == vb && ia < ib);
@@ -70,13 +71,25 @@ route_topk_softmax_kernel(const float* __restrict__ logits, int32_t* __restrict_
     }
 
     const float m = sel_v[0];
+    // lane r < k holds the exponential of its selected expert: the fp64 exp is
+    // evaluated once per selected expert, in parallel across the lanes
+    float sv = 0.0f;
+    int si = 0;
+#pragma unroll
+    for (int q = 0; q < MOE_MAX_TOPK; ++q)
+        if (q == lane) {
+            sv = sel_v[q];
+            si = sel_i[q];
+        }
+    const float e_mine = (lane < k) ? __double2float_rn(exp(static_cast<double>(__fsub_rn(sv, m)))) : 0.0f;
     float denom;
     if (renorm) {
-        denom = 0.0f;
+        denom = 0.0f;  // e_0 + e_1 + ... in rank order
 #pragma unroll
-        for (int r = 0; r < MOE_MAX_TOPK; ++r)
-            if (r < k)
-                denom = __fadd_rn(denom, __double2float_rn(exp(static_cast<double>(__fsub_rn(sel_v[r], m)))));
+        for (int r = 0; r < MOE_MAX_TOPK; ++r) {
+            const float er = __shfl_sync(0xffffffffu, e_mine, r);
+            if (r < k) denom = __fadd_rn(denom, er);
+        }
     } else {
         float part = 0.0f;
 #pragma unroll
@@ -88,19 +101,9 @@ route_topk_softmax_kernel(const float* __restrict__ logits, int32_t* __restrict_
         for (int off = 16; off > 0; off >>= 1) part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, off));
         denom = part;
     }
-    for (int r = lane; r < k; r += 32) {
-        // r < k <= MOE_MAX_TOPK: select with a static index to keep the arrays in registers
-        float sv = 0.0f;
-        int si = 0;
-#pragma unroll
-        for (int q = 0; q < MOE_MAX_TOPK; ++q)
-            if (q == r) {
-                sv = sel_v[q];
-                si = sel_i[q];
-            }
-        const float e = __double2float_rn(exp(static_cast<double>(__fsub_rn(sv, m))));
-        ids[static_cast<size_t>(row) * k + r] = si;
-        w[static_cast<size_t>(row) * k + r] = __fdiv_rn(e, denom);
+    if (lane < k) {
+        ids[static_cast<size_t>(row) * k + lane] = si;
+        w[static_cast<size_t>(row) * k + lane] = __fdiv_rn(e_mine, denom);
     }
 }
 

@@ -136,12 +136,13 @@ class MoeLayer:
 
     def gate_up(self, x, stream=None):
         M.moe_grouped_gate_up(x, self.act_code, self.w_gate_up.desc, self.sorted_token_ids, self.expert_offsets,
-                              self.T, self.k, self.H, self.I, self.E, self.max_padded, self.h, self.err,
+                              self.T, self.k, self.H, self.I, self.E, self.bs, self.max_padded, self.h, self.err,
                               self.gate_up_ws, self.gate_up_ws_bytes, stream)
 
     def down(self, stream=None):
-        M.moe_grouped_down(self.h, self.act_code, self.w_down.desc, self.expert_offsets, self.H, self.I, self.E,
-                           self.max_padded, self.y, self.err, stream)
+        M.moe_grouped_down(self.h, self.act_code, self.w_down.desc, self.sorted_token_ids, self.expert_offsets,
+                           self.T, self.k, self.H, self.I, self.E, self.bs, self.max_padded, self.y, self.err,
+                           stream)
 
     def lora_fold(self, stream=None, row_offset=0, row_end=None):
         if self.lora is None:
@@ -164,7 +165,36 @@ class MoeLayer:
         self.combine(stream)
         return self.out
 
+    def capture(self, x, logits):
+        """CUDA graphs of one forward: (pre = route + align, gate_up, post =
+        down + fold + combine) and the whole layer. The buffers are fixed, so
+        replaying a graph re-runs the layer on the current contents of x and
+        logits. Returns (pre, gate_up, post, whole, kernels_per_forward)."""
+        self.forward(x, logits)          # first use on this device (attributes, descriptors)
+        torch.cuda.synchronize()
+        graphs = []
+        n0 = M.moe_launch_count()
+        for part in ("pre", "gate_up", "post"):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                if part == "pre":
+                    self.route(logits)
+                    self.align()
+                elif part == "gate_up":
+                    self.gate_up(x)
+                else:
+                    self.down()
+                    self.lora_fold()
+                    self.combine()
+            graphs.append(g)
+        per_forward = M.moe_launch_count() - n0
+        whole = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(whole):
+            self.forward(x, logits)
+        torch.cuda.synchronize()
+        return graphs[0], graphs[1], graphs[2], whole, per_forward
+
     @property
     def launches_per_forward(self) -> int:
-        align = (1 if self.P > 0 else 0) * 2 + 1
+        align = 1 if self.P <= 2048 else 3
         return 1 + align + 2 + 1 + (2 if self.lora is not None else 0) + 1

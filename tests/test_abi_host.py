@@ -84,15 +84,19 @@ def test_workspace_sizes(moe):
     lambda m: m.moe_align_block_size(16, 32, 8, 16, 168, 16, 16, 16, 16, 16, 0, 16, 1 << 20, 0),  # not bs multiple
     lambda m: m.moe_align_block_size(16, 32, 8, 16, 160, 16, 16, 16, 16, 16, 0, 16, 4, 0),        # workspace small
     lambda m: m.moe_grouped_gate_up(16, 0, m.MoeWeight(0, 0, 16, None, None, None), 16, 16, 4, 2, 100, 64, 8,
-                                    64, 16, 0, 16, 1 << 30, 0),                 # H % 8
+                                    16, 64, 16, 0, 16, 1 << 30, 0),             # H % 8
     lambda m: m.moe_grouped_gate_up(16, 1, m.MoeWeight(0, 0, 16, None, None, None), 16, 16, 4, 2, 128, 64, 8,
-                                    64, 16, 0, 16, 1 << 30, 0),                 # bf16 weight, f16 act
+                                    16, 64, 16, 0, 16, 1 << 30, 0),             # bf16 weight, f16 act
     lambda m: m.moe_grouped_gate_up(16, 1, m.MoeWeight(1, 100, 16, 16, 16, None), 16, 16, 4, 2, 128, 64, 8,
-                                    64, 16, 0, 16, 1 << 30, 0),                 # GPTQ group not /64
+                                    16, 64, 16, 0, 16, 1 << 30, 0),             # GPTQ group not /64
     lambda m: m.moe_grouped_gate_up(16, 0, m.MoeWeight(7, 0, 16, None, None, None), 16, 16, 4, 2, 128, 64, 8,
-                                    64, 16, 0, 16, 1 << 30, 0),                 # unknown format
-    lambda m: m.moe_grouped_down(16, 0, m.MoeWeight(0, 0, 16, None, None, None), 16, 128, 100, 8, 64, 16, 0, 0),
-    lambda m: m.moe_grouped_down(16, 0, m.MoeWeight(2, 0, 16, 16, None, 16), 16, 128, 72, 8, 64, 16, 0, 0),
+                                    16, 64, 16, 0, 16, 1 << 30, 0),             # unknown format
+    lambda m: m.moe_grouped_down(16, 0, m.MoeWeight(0, 0, 16, None, None, None), 16, 16, 4, 2, 128, 100, 8, 16, 64,
+                                 16, 0, 0),                                     # I % 8
+    lambda m: m.moe_grouped_down(16, 0, m.MoeWeight(2, 0, 16, 16, None, 16), 16, 16, 4, 2, 128, 72, 8, 16, 64, 16,
+                                 0, 0),                                         # NVFP4 K % 32
+    lambda m: m.moe_grouped_down(16, 1, m.MoeWeight(1, 64, 16, 16, 16, None), 16, 16, 4, 2, 200, 64, 8, 16, 64, 16,
+                                 0, 0),                                         # GPTQ H % 32
     lambda m: m.moe_combine(16, 0, 16, 16, 16, 4, 100, 2, 64, 0, 0),             # H % 8
     lambda m: m.moe_lora_grouped_down(m.MoeExpertRoute(16, 16, 16, 4, 64, 128, 65), 16, 16, 16, 16, None, 16,
                                       0, 64, 0, 8, 2, 0),                       # rank > MAX
