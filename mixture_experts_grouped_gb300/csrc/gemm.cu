@@ -19,17 +19,22 @@
 //     output columns, so the epilogue can fuse silu*up; down: 256 output
 //     columns) against a block of activation rows, K in steps of 64 elements
 //     (one 128-byte swizzle span):
-//       - prefill form: 128 activation rows are the MMA's M operand and the 256
-//         weight rows its N operand (tcgen05.mma M=128, N=256, K=16);
+//       - prefill form: 128 activation rows are the MMA's M operand and the
+//         256 weight rows its N operand (tcgen05.mma M=128, N=256, K=16); with
+//         quantised weights a tile holds 256 rows as two M=128 halves that
+//         share the dequantised weight tile (a span's last tile of at most 128
+//         rows runs one half only);
 //       - decode form (few rows per expert): the operands swap; each half of
 //         the weight tile is an M=128 operand and the NTOK activation rows
 //         (16..128) the N operand, so a small batch does not pay for 128 rows.
 //   * Warp 0 issues TMA loads into a multi-stage ring; one thread of warp 1
-//     issues tcgen05.mma into one of two TMEM accumulators; warps 2-5 drain
-//     the other (tcgen05.ld -> activation -> global).
-//   * Quantised weights (GPTQ int4, NVFP4): warp 10 streams the raw bytes by
-//     TMA into a 6-deep ring of their own; warps 6-9 dequantise shared ->
-//     shared into the swizzled 16-bit weight tile the MMA reads. The NVFP4
+//     issues tcgen05.mma into one of two TMEM accumulators while warps 2-5
+//     drain the other (tcgen05.ld -> activation -> global); 256-row tiles use
+//     one accumulator of 512 columns.
+//   * Quantised weights (GPTQ int4, NVFP4): warp 14 streams the raw bytes by
+//     TMA into a 6-deep ring of their own; warps 6-13 (two per SM
+//     sub-partition, since dequantisation is latency-bound) dequantise shared
+//     -> shared into the swizzled 16-bit weight tile the MMA reads. The NVFP4
 //     global scale2 is applied to the f32 accumulator.
 //   * Every mbarrier wait is bounded; on a timeout the CTA records
 //     MOE_DEV_ERR_TIMEOUT, lets in-flight copies and MMAs land, frees TMEM and
@@ -44,8 +49,9 @@ constexpr int W_ROWS = 256;             // weight rows per tile
 constexpr int W_STAGE = W_ROWS * BK * 2;  // 32 KB
 constexpr int RAW_STAGE = 9216;         // raw quantised bytes of one weight stage
 constexpr int NUM_EPI_WARPS = 4;
-constexpr int NUM_DQ_WARPS = 4;
+constexpr int NUM_DQ_WARPS = 8;  // two per SM sub-partition: dequantisation is latency-bound
 constexpr int MAX_STAGES = 8;
+constexpr int MAX_RSTAGES = 16;
 constexpr int SMEM_LIMIT = 232448;      // dynamic shared memory per block (227 KB)
 
 enum { MODE_GATE_UP = 0, MODE_DOWN = 1 };
@@ -68,8 +74,8 @@ struct GemmParams {
 struct SmemTail {
     uint64_t full[MAX_STAGES];
     uint64_t empty[MAX_STAGES];
-    uint64_t raw_full[MAX_STAGES];
-    uint64_t raw_empty[MAX_STAGES];
+    uint64_t raw_full[MAX_RSTAGES];
+    uint64_t raw_empty[MAX_RSTAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t mma_done;
@@ -95,18 +101,32 @@ template <int MODE, int WFMT, int ACT, int NTOK>
 struct Shape {
     static constexpr bool SWAP = NTOK > 0;
     static constexpr bool QUANT = WFMT != MOE_W_BF16;
-    static constexpr int XROWS = SWAP ? NTOK : 128;
+    // prefill form, quantised weights: 256 activation rows as two M=128 halves
+    // sharing the dequantised weight tile (half the dequantisation per FLOP);
+    // prefill form, bf16 weights: 128 rows; decode form: NTOK rows
+    static constexpr bool PAIR = !SWAP && QUANT;
+    static constexpr int XROWS = SWAP ? NTOK : (PAIR ? 256 : 128);
     static constexpr int X_STAGE = XROWS * BK * 2;
-    static constexpr int RSTAGES = QUANT ? 6 : 0;
-    static constexpr int AVAIL = SMEM_LIMIT - 1024 - TAIL_BYTES - RSTAGES * RAW_STAGE;
-    static constexpr int STAGES = (AVAIL / (X_STAGE + W_STAGE)) < MAX_STAGES ? AVAIL / (X_STAGE + W_STAGE) : MAX_STAGES;
-    static constexpr int ACC = SWAP ? 2 * NTOK : 256;  // TMEM columns per accumulator
-    static constexpr int TMEM_COLS = pow2_at_least(2 * ACC);
+    static constexpr int AVAIL = SMEM_LIMIT - 1024 - TAIL_BYTES;
+    // bf16 weights: as many TMA stages as fit. Quantised weights: the 16-bit
+    // stages are refilled on chip, so few suffice, and the rest of shared
+    // memory holds raw stages (more raw bytes in flight from HBM).
+    static constexpr int STAGES_FIT = AVAIL / (X_STAGE + W_STAGE);
+    static constexpr int STAGES = QUANT ? (SWAP ? 3 : 2) : (STAGES_FIT < MAX_STAGES ? STAGES_FIT : MAX_STAGES);
+    static constexpr int RAW_FIT = (AVAIL - STAGES * (X_STAGE + W_STAGE)) / RAW_STAGE;
+    static constexpr int RSTAGES = QUANT ? (RAW_FIT < MAX_RSTAGES ? RAW_FIT : MAX_RSTAGES) : 0;
+    // TMEM: two accumulator buffers (the epilogue drains one while the MMA
+    // fills the other), except for 256-row tiles, whose one accumulator of two
+    // 128-row halves x 256 columns takes all 512 columns
+    static constexpr int NBUF = PAIR ? 1 : 2;
+    static constexpr int ACC = SWAP ? 2 * NTOK : (PAIR ? 512 : 256);  // TMEM columns per buffer
+    static constexpr int TMEM_COLS = pow2_at_least(NBUF * ACC);
     static constexpr int OUT_COLS = MODE == MODE_GATE_UP ? 128 : 256;  // output columns per tile
     static constexpr int THREADS = 192 + (QUANT ? 32 * (NUM_DQ_WARPS + 1) : 0);
     static constexpr int SMEM = 1024 + STAGES * (X_STAGE + W_STAGE) + RSTAGES * RAW_STAGE + TAIL_BYTES;
     static constexpr int RAW_BYTES = WFMT == MOE_W_GPTQ_INT4 ? 8832 : 9216;
     static_assert(STAGES >= 2, "not enough shared memory for two stages");
+    static_assert(!QUANT || RSTAGES >= 4, "not enough shared memory for the raw ring");
     static_assert(TMEM_COLS <= 512, "accumulators exceed TMEM");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory over the limit");
 };
@@ -170,6 +190,27 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
     return (b & 0x80u) ? -v : v;
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// Four E2M1 codes (nibbles 0..3 of w) -> two bf16x2 words, with no
+// conversion instructions: a byte permute looks up the high and low byte of
+// each magnitude's bf16 value (0, .5, 1, 1.5, 2, 3, 4, 6 -> 0x0000, 0x3F00,
+// 0x3F80, 0x3FC0, 0x4000, 0x4040, 0x4080, 0x40C0), a second permute
+// interleaves them, and a sign-replicating permute carries each code's sign
+// bit (bit 3) to bit 15 of its half.
+__device__ __forceinline__ void e2m1x4_to_bf16x4(uint32_t w, uint32_t& p01, uint32_t& p23) {
+    const uint32_t sel = w & 0x7777u;
+    const uint32_t hi = prmt(0x3F3F3F00u, 0x40404040u, sel);
+    const uint32_t lo = prmt(0xC0800000u, 0xC0804000u, sel);
+    const uint32_t t = w << 4;  // byte 0 / 1 of t carry the signs of codes 0 / 2 in their top bit
+    p01 = prmt(lo, hi, 0x5140u) | (prmt(t, w, 0xC888u) & 0x80008000u);
+    p23 = prmt(lo, hi, 0x7362u) | (prmt(t, w, 0xD999u) & 0x80008000u);
+}
+
 template <int ACT>
 __device__ __forceinline__ uint32_t f16x2_to_act2(uint32_t h2) {
     if (ACT == MOE_ACT_F16) return h2;
@@ -177,15 +218,9 @@ __device__ __forceinline__ uint32_t f16x2_to_act2(uint32_t h2) {
     return Act<MOE_ACT_BF16>::pack2(f.x, f.y);
 }
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-    return r;
-}
-
 // 8 GPTQ codes of one word -> 8 weights (q - z) * s in the activation type, k order
 template <int ACT>
-__device__ __forceinline__ uint4 gptq_word(uint32_t w, int z, float s) {
+__device__ __forceinline__ uint4 gptq_word(uint32_t w, int z, float s, __half2 ss) {
     uint4 v;
     if (ACT == MOE_ACT_F16) {
         // fp16 1024 + q from the code bits (exact), minus 1024 + z (exact), times s
@@ -196,7 +231,6 @@ __device__ __forceinline__ uint4 gptq_word(uint32_t w, int z, float s) {
         const uint32_t p2 = ((w >> 8) & 0x000F000Fu) | m;
         const uint32_t p3 = ((w >> 12) & 0x000F000Fu) | m;
         const __half2 zz = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400 | z)));
-        const __half2 ss = __float2half2_rn(s);
         uint32_t r[4] = {p0, p1, p2, p3};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -222,44 +256,67 @@ __device__ __forceinline__ uint4 gptq_word(uint32_t w, int z, float s) {
 template <int MODE, int WFMT, int ACT>
 __device__ __forceinline__ void dequant_stage(uint8_t* wstage, const uint8_t* raw, const GemmParams& p,
                                               const TileInfo& t, int dq_tid) {
+    constexpr int DQ_THREADS = NUM_DQ_WARPS * 32;  // 256
     if (WFMT == MOE_W_GPTQ_INT4) {
         // raw: qweight [2 halves][8 packed k-rows][128 cols] int32, scales [2][128] fp16,
-        // zeros [2][16] int32. Thread = (half, column); 8 words per half.
-        const int c = dq_tid;  // column within each half
+        // zeros [2][16] int32. Thread = (half h, column c): the 8 words of its column.
+        const int h = dq_tid >> 7, c = dq_tid & 127;
+        const int n = h * 128 + c;
+        const bool valid = out_col<MODE>(n, t.n0) < p.n_out;
+        const uint32_t* qw = reinterpret_cast<const uint32_t*>(raw + h * 4096);
+        const __half sh = reinterpret_cast<const __half*>(raw + 8192 + h * 256)[c];
+        const float s = __half2float(sh);
+        const __half2 ss = __half2half2(sh);
+        const uint32_t zw = reinterpret_cast<const uint32_t*>(raw + 8704 + h * 128)[c >> 3];
+        const int z = (zw >> (4 * (c & 7))) & 15;
+        uint32_t words[8];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int n = h * 128 + c;
-            const bool valid = out_col<MODE>(n, t.n0) < p.n_out;
-            const uint32_t* qw = reinterpret_cast<const uint32_t*>(raw + h * 4096);
-            const float s = __half2float(reinterpret_cast<const __half*>(raw + 8192 + h * 256)[c]);
-            const uint32_t zw = reinterpret_cast<const uint32_t*>(raw + 8704 + h * 128)[c >> 3];
-            const int z = (zw >> (4 * (c & 7))) & 15;
+        for (int i = 0; i < 8; ++i) words[i] = qw[i * 128 + c];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (valid) v = gptq_word<ACT>(qw[i * 128 + c], z, s);
-                *reinterpret_cast<uint4*>(wstage + n * 128 + ((i ^ (n & 7)) << 4)) = v;
-            }
+        for (int i = 0; i < 8; ++i) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (valid) v = gptq_word<ACT>(words[i], z, s, ss);
+            *reinterpret_cast<uint4*>(wstage + n * 128 + ((i ^ (n & 7)) << 4)) = v;
         }
     } else {
         // raw: packed [2 halves][128 rows][32 bytes], scales [2][4 k16-groups][128 rows] E4M3.
         // Item = (half, row r, 8-element chunk cc); 8 consecutive threads read one row.
-#pragma unroll 4
-        for (int it = 0; it < (W_ROWS * 8) / (NUM_DQ_WARPS * 32); ++it) {
-            const int idx = it * NUM_DQ_WARPS * 32 + dq_tid;
+        constexpr int ITEMS = (W_ROWS * 8) / DQ_THREADS;  // 8
+        uint32_t bytes[ITEMS];
+        uint32_t sbyte[ITEMS];
+#pragma unroll
+        for (int it = 0; it < ITEMS; ++it) {
+            const int idx = it * DQ_THREADS + dq_tid;
+            const int h = idx >> 10, r = (idx >> 3) & 127, cc = idx & 7;
+            bytes[it] = reinterpret_cast<const uint32_t*>(raw + h * 4096 + r * 32)[cc];
+            sbyte[it] = raw[8192 + h * 512 + (cc >> 1) * 128 + r];
+        }
+#pragma unroll
+        for (int it = 0; it < ITEMS; ++it) {
+            const int idx = it * DQ_THREADS + dq_tid;
             const int h = idx >> 10, r = (idx >> 3) & 127, cc = idx & 7;
             const int n = h * 128 + r;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (out_col<MODE>(n, t.n0) < p.n_out) {
-                const uint32_t bytes = reinterpret_cast<const uint32_t*>(raw + h * 4096 + r * 32)[cc];
-                const float sc = e4m3_to_f32(raw[8192 + h * 512 + (cc >> 1) * 128 + r]);
-                const __half2 s2 = __float2half2_rn(sc);  // exact: an E4M3 value is an fp16 value
                 uint32_t o[4];
+                if (ACT == MOE_ACT_BF16) {
+                    // products of an E2M1 and an E4M3 value are exact in bf16
+                    const __nv_bfloat162 s2 = __float2bfloat162_rn(e4m3_to_f32(sbyte[it]));
+                    e2m1x4_to_bf16x4(bytes[it], o[0], o[1]);
+                    e2m1x4_to_bf16x4(bytes[it] >> 16, o[2], o[3]);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t e2 = e2m1x2_to_f16x2((bytes >> (8 * j)) & 0xffu);
-                    __half2 prod = __hmul2(*reinterpret_cast<__half2*>(&e2), s2);  // exact in fp16
-                    o[j] = f16x2_to_act2<ACT>(*reinterpret_cast<uint32_t*>(&prod));
+                    for (int j = 0; j < 4; ++j) {
+                        __nv_bfloat162 prod = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&o[j]), s2);
+                        o[j] = *reinterpret_cast<uint32_t*>(&prod);
+                    }
+                } else {
+                    const __half2 s2 = __float2half2_rn(e4m3_to_f32(sbyte[it]));  // exact: E4M3 values are fp16 values
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t e2 = e2m1x2_to_f16x2((bytes[it] >> (8 * j)) & 0xffu);
+                        __half2 prod = __hmul2(*reinterpret_cast<__half2*>(&e2), s2);  // exact in fp16
+                        o[j] = *reinterpret_cast<uint32_t*>(&prod);
+                    }
                 }
                 v = make_uint4(o[0], o[1], o[2], o[3]);
             }
@@ -408,17 +465,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             // ---------------- TMA producer: activations (+ bf16 weights) ----------------
             uint32_t stage = 0, phase = 0;
             long issued = 0;
-            const uint32_t tx = S::QUANT ? S::X_STAGE : (S::X_STAGE + W_STAGE);
             bool ok = true;
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
                 const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
                 if (tile_is_padding(p, t)) continue;
                 int c0, c1;
                 half_bases<MODE>(p, t.n0, c0, c1);
+                // prefill tiles of at most 128 rows load and multiply one half only
+                const bool two = S::PAIR && t.rows > 128;
+                const uint32_t xbytes = S::PAIR ? (two ? 2 : 1) * 128 * BK * 2 : S::X_STAGE;
+                const uint32_t tx = xbytes + (S::QUANT ? 0u : static_cast<uint32_t>(W_STAGE));
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
                     mbar_arrive_expect_tx(&s.full[stage], tx);
                     tma_load_2d(sX + stage * S::X_STAGE, &tmX, kb * BK, t.m0, &s.full[stage]);
+                    if (two) tma_load_2d(sX + stage * S::X_STAGE + 128 * BK * 2, &tmX, kb * BK, t.m0 + 128, &s.full[stage]);
                     if (!S::QUANT) {
                         uint8_t* w = sW + stage * W_STAGE;
                         tma_load_2d(w, &tmW, kb * BK, t.e * p.n_w + c0, &s.full[stage]);
@@ -443,9 +504,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
                 const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
                 if (tile_is_padding(p, t)) continue;
-                const int acc = local & 1;
-                const uint32_t aph = (local >> 1) & 1;
+                const int acc = S::NBUF == 2 ? (local & 1) : 0;
+                const uint32_t aph = S::NBUF == 2 ? ((local >> 1) & 1) : (local & 1);
                 ++local;
+                const bool two = S::PAIR && t.rows > 128;
                 if (!mbar_wait(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * S::ACC;
@@ -462,8 +524,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                             tc_mma(d + NTOK, wd1 + 2 * k, xd + 2 * k, idesc, (kb | k) != 0);
                         }
                     } else {
+                        const uint64_t xd1 = sw128_desc(smem_u32(sX + stage * S::X_STAGE + 128 * BK * 2));
 #pragma unroll
-                        for (int k = 0; k < BK / 16; ++k) tc_mma(d, xd + 2 * k, wd + 2 * k, idesc, (kb | k) != 0);
+                        for (int k = 0; k < BK / 16; ++k) {
+                            tc_mma(d, xd + 2 * k, wd + 2 * k, idesc, (kb | k) != 0);
+                            if (two) tc_mma(d + 256, xd1 + 2 * k, wd + 2 * k, idesc, (kb | k) != 0);
+                        }
                     }
                     tc_commit(&s.empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -483,8 +549,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
             const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
             if (tile_is_padding(p, t)) continue;
-            const int acc = local & 1;
-            const uint32_t aph = (local >> 1) & 1;
+            const int acc = S::NBUF == 2 ? (local & 1) : 0;
+            const uint32_t aph = S::NBUF == 2 ? ((local >> 1) & 1) : (local & 1);
             ++local;
             if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
             tc_fence_after();
@@ -496,45 +562,51 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * S::ACC;
             const int nvalid = valid_rows(p, s, t, lane);
             if (!S::SWAP) {
-                // lane = activation row; columns = weight rows (gate | up, or 256 outputs)
-                const bool row_ok = lrow < nvalid;
-                const size_t orow = static_cast<size_t>(t.m0 + lrow) * p.n_out;
-                if (MODE == MODE_GATE_UP) {
+                // lane = activation row of each 128-row half; columns = weight rows
+                // (gate | up, or 256 outputs)
+                for (int hh = 0; hh < (S::PAIR ? 2 : 1) && hh * 128 < t.rows; ++hh) {
+                    const int row = hh * 128 + lrow;
+                    const bool row_ok = row < nvalid;
+                    const size_t orow = static_cast<size_t>(t.m0 + row) * p.n_out;
+                    const uint32_t ta = taddr + hh * 256;
+                    if (MODE == MODE_GATE_UP) {
 #pragma unroll 1
-                    for (int c = 0; c < 128; c += 32) {
-                        uint32_t g[32], u[32];
-                        tmem_ld32(taddr + c, g);
-                        tmem_ld32(taddr + 128 + c, u);
-                        tmem_ld_wait();
-                        if (row_ok) {
+                        for (int c = 0; c < 128; c += 32) {
+                            uint32_t g[32], u[32];
+                            tmem_ld32(ta + c, g);
+                            tmem_ld32(ta + 128 + c, u);
+                            tmem_ld_wait();
+                            if (row_ok) {
 #pragma unroll
-                            for (int j = 0; j < 32; j += 8) {
-                                const int col = t.n0 + c + j;
-                                if (col < p.n_out) {
-                                    float f[8];
+                                for (int j = 0; j < 32; j += 8) {
+                                    const int col = t.n0 + c + j;
+                                    if (col < p.n_out) {
+                                        float f[8];
 #pragma unroll
-                                    for (int i = 0; i < 8; ++i)
-                                        f[i] = silu_mul(__uint_as_float(g[j + i]) * s2a, __uint_as_float(u[j + i]) * s2b);
-                                    store8<ACT>(p.out, orow + col, f);
+                                        for (int i = 0; i < 8; ++i)
+                                            f[i] = silu_mul(__uint_as_float(g[j + i]) * s2a,
+                                                            __uint_as_float(u[j + i]) * s2b);
+                                        store8<ACT>(p.out, orow + col, f);
+                                    }
                                 }
                             }
                         }
-                    }
-                } else {
+                    } else {
 #pragma unroll 1
-                    for (int c = 0; c < 256; c += 32) {
-                        uint32_t g[32];
-                        tmem_ld32(taddr + c, g);
-                        tmem_ld_wait();
-                        if (row_ok) {
+                        for (int c = 0; c < 256; c += 32) {
+                            uint32_t g[32];
+                            tmem_ld32(ta + c, g);
+                            tmem_ld_wait();
+                            if (row_ok) {
 #pragma unroll
-                            for (int j = 0; j < 32; j += 8) {
-                                const int col = t.n0 + c + j;
-                                if (col < p.n_out) {
-                                    float f[8];
+                                for (int j = 0; j < 32; j += 8) {
+                                    const int col = t.n0 + c + j;
+                                    if (col < p.n_out) {
+                                        float f[8];
 #pragma unroll
-                                    for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(g[j + i]) * s2a;
-                                    store8<ACT>(p.out, orow + col, f);
+                                        for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(g[j + i]) * s2a;
+                                        store8<ACT>(p.out, orow + col, f);
+                                    }
                                 }
                             }
                         }
@@ -601,7 +673,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             }
         }
     } else {
-        // ---------------- raw quantised-weight producer (warp 10) ----------------
+        // ---------------- raw quantised-weight producer (last warp) ----------------
         if constexpr (S::QUANT) {
           if (lane == 0) {
             uint32_t rstage = 0, rphase = 0;
