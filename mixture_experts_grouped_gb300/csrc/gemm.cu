@@ -722,6 +722,247 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     if (warp == 1) tmem_dealloc(tmem_base, S::TMEM_COLS);
 }
 
+// ---- CTA-pair prefill kernel (bf16 weights) -------------------------------------
+//
+// The prefill form on a pair of SMs: tcgen05.mma.cta_group::2 with M=256
+// (each CTA holds 128 activation rows) and N=256 (each CTA holds half of the
+// 256 weight rows). Every SM then moves 32 KB through shared memory per
+// 64-deep k block instead of 48 KB for the same MMA work, and holds six
+// stages instead of four. One thread of the even CTA (the leader) issues the
+// MMAs; both CTAs' TMA loads complete on the leader's full barrier; the
+// leader's commits arrive on both CTAs' barriers; the follower's epilogue
+// warps release the accumulator through the leader's barrier.
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_A = 128 * BK * 2;  // this CTA's 128 activation rows
+constexpr int PAIR_B = 128 * BK * 2;  // this CTA's half of the weight tile
+constexpr int PAIR_SMEM = 1024 + PAIR_STAGES * (PAIR_A + PAIR_B) + TAIL_BYTES;
+static_assert(PAIR_SMEM <= SMEM_LIMIT, "pair kernel shared memory over the limit");
+
+template <int MODE>
+__global__ void __launch_bounds__(192, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                         const GemmParams p) {
+    constexpr int ACT = MOE_ACT_BF16;
+    constexpr int XROWS = 256;
+    constexpr int OUT_COLS = MODE == MODE_GATE_UP ? 128 : 256;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + PAIR_STAGES * PAIR_A;
+    SmemTail& s = *reinterpret_cast<SmemTail*>(sB + PAIR_STAGES * PAIR_B);
+    volatile int* abort_flag = &s.abort_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: leader, 1: follower
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int E = p.E;
+
+    // ---- tile list from expert_offsets (identical in both CTAs) ----
+    for (int i = tid; i <= E; i += blockDim.x) s.off[i] = p.offsets[i];
+    if (tid == 0) {
+        s.abort_flag = 0;
+        s.nt = (p.n_out + OUT_COLS - 1) / OUT_COLS;
+    }
+    __syncthreads();
+    int bad = 0;
+    for (int i = tid; i < E; i += blockDim.x) bad |= (s.off[i + 1] < s.off[i]);
+    if (tid == 0) bad |= (s.off[0] < 0) | (s.off[E] > p.max_padded);
+    bad = __syncthreads_or(bad);
+    if (warp == 0) {
+        const int per = (E + 31) / 32;
+        int loc = 0;
+        for (int j = 0; j < per; ++j) {
+            const int e = lane * per + j;
+            if (e < E) loc += ((s.off[e + 1] - s.off[e] + XROWS - 1) / XROWS) * s.nt;
+        }
+        int inc = loc;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, inc, d);
+            if (lane >= d) inc += o;
+        }
+        int run = inc - loc;
+        for (int j = 0; j < per; ++j) {
+            const int e = lane * per + j;
+            if (e < E) {
+                s.tstart[e] = run;
+                run += ((s.off[e + 1] - s.off[e] + XROWS - 1) / XROWS) * s.nt;
+            }
+        }
+        if (lane == 31) s.n_tiles = bad ? 0 : inc;
+    }
+    if (tid == 0) {
+        if (bad && rank == 0) set_err(p.err, MOE_DEV_ERR_OFFSETS);
+        for (int i = 0; i < PAIR_STAGES; ++i) {
+            mbar_init(&s.full[i], 1);
+            mbar_init(&s.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.tfull[i], 1);
+            mbar_init(&s.tempty[i], 2 * NUM_EPI_WARPS);
+        }
+        mbar_init(&s.mma_done, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int n_tiles = s.n_tiles;
+    if (pair >= n_tiles) return;  // the same in both CTAs of the pair: nothing allocated yet
+
+    if (warp == 1) {
+        tmem_alloc_pair(&s.tmem_base, 512);
+        tmem_relinquish_pair();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW);
+    }
+    tc_fence_before();
+    cluster_sync_all();  // both CTAs' barriers initialised and TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem_base = s.tmem_base;
+    const uint32_t leader_full0 = mapa_shared(smem_u32(&s.full[0]), 0);
+    const uint32_t leader_tempty0 = mapa_shared(smem_u32(&s.tempty[0]), 0);
+    const int KB = (p.K + BK - 1) / BK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (both CTAs) ----------------
+            uint32_t stage = 0, phase = 0;
+            long issued = 0;
+            bool ok = true;
+            for (int tile = pair; tile < n_tiles && ok; tile += npairs) {
+                const TileInfo t = decode_tile<XROWS>(s, E, tile, OUT_COLS);
+                if (tile_is_padding(p, t)) continue;
+                int c0, c1;
+                half_bases<MODE>(p, t.n0, c0, c1);
+                const int wrow = t.e * p.n_w + (rank == 0 ? c0 : c1);
+                const int arow = t.m0 + static_cast<int>(rank) * 128;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2 * (PAIR_A + PAIR_B));
+                    const uint32_t bar = leader_full0 + stage * 8;
+                    tma_load_2d_pair(sA + stage * PAIR_A, &tmX, kb * BK, arow, bar);
+                    tma_load_2d_pair(sB + stage * PAIR_B, &tmW, kb * BK, wrow, bar);
+                    ++issued;
+                    if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (rank == 0) {  // let every copy of the pair land before either CTA may exit
+                const long first = issued > PAIR_STAGES ? issued - PAIR_STAGES : 0;
+                for (long j = first; j < issued; ++j)
+                    mbar_drain(&s.full[j % PAIR_STAGES], static_cast<uint32_t>((j / PAIR_STAGES) & 1),
+                               kWaitLimitNs / 8);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // ---------------- MMA issuer (leader) ----------------
+            constexpr uint32_t idesc = f16_idesc(ACT, 256, 256);
+            uint32_t stage = 0, phase = 0;
+            int local = 0;
+            bool ok = true;
+            for (int tile = pair; tile < n_tiles && ok; tile += npairs) {
+                const TileInfo t = decode_tile<XROWS>(s, E, tile, OUT_COLS);
+                if (tile_is_padding(p, t)) continue;
+                const int acc = local & 1;
+                const uint32_t aph = (local >> 1) & 1;
+                ++local;
+                if (!mbar_wait(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + acc * 256;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&s.full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t ad = sw128_desc(smem_u32(sA + stage * PAIR_A));
+                    const uint64_t bd = sw128_desc(smem_u32(sB + stage * PAIR_B));
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) tc_mma_pair(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                    tc_commit_pair(&s.empty[stage], 0x3);
+                    if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc_commit_pair(&s.tfull[acc], 0x3);
+            }
+            tc_commit_pair(&s.mma_done, 0x1);
+            mbar_drain(&s.mma_done, 0, kWaitLimitNs / 8);
+        }
+        __syncwarp();
+    } else if (warp < 2 + NUM_EPI_WARPS) {
+        // ---------------- epilogue (both CTAs, each its own 128 rows) ----------------
+        const int q = warp & 3;
+        const int lrow = q * 32 + lane;
+        int local = 0;
+        for (int tile = pair; tile < n_tiles; tile += npairs) {
+            const TileInfo t = decode_tile<XROWS>(s, E, tile, OUT_COLS);
+            if (tile_is_padding(p, t)) continue;
+            const int acc = local & 1;
+            const uint32_t aph = (local >> 1) & 1;
+            ++local;
+            if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
+            tc_fence_after();
+            const int nvalid = valid_rows(p, s, t, lane);
+            const int row = static_cast<int>(rank) * 128 + lrow;
+            const bool row_ok = row < nvalid;
+            const size_t orow = static_cast<size_t>(t.m0 + row) * p.n_out;
+            const uint32_t ta = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 256;
+            if (MODE == MODE_GATE_UP) {
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 32) {
+                    uint32_t g[32], u[32];
+                    tmem_ld32(ta + c, g);
+                    tmem_ld32(ta + 128 + c, u);
+                    tmem_ld_wait();
+                    if (row_ok) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 8) {
+                            const int col = t.n0 + c + j;
+                            if (col < p.n_out) {
+                                float f[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    f[i] = silu_mul(__uint_as_float(g[j + i]), __uint_as_float(u[j + i]));
+                                store8<ACT>(p.out, orow + col, f);
+                            }
+                        }
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < 256; c += 32) {
+                    uint32_t g[32];
+                    tmem_ld32(ta + c, g);
+                    tmem_ld_wait();
+                    if (row_ok) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 8) {
+                            const int col = t.n0 + c + j;
+                            if (col < p.n_out) {
+                                float f[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(g[j + i]);
+                                store8<ACT>(p.out, orow + col, f);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (rank == 0) mbar_arrive(&s.tempty[acc]);
+                else mbar_arrive_cluster(leader_tempty0 + acc * 8);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // the leader's MMAs read this CTA's shared memory and write its TMEM
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, 512);
+}
+
 // ---- gather of the activations into sorted-row order ---------------------------
 
 // xs[r] = x[sorted_token_ids[r] / top_k] for r < expert_offsets[E]. Padding
@@ -801,8 +1042,52 @@ int by_ntok(int ntok, const Maps& m, const GemmParams& p, cudaStream_t st, const
 }
 
 template <int MODE>
+int launch_pair(const Maps& m, const GemmParams& p, cudaStream_t st, const char* who) {
+    auto kernel = grouped_gemm_pair_kernel<MODE>;
+    static int configured_for = -1;
+    static int max_pairs = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = PAIR_SMEM;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (configured_for != dev) {
+        int rc = set_smem_limit(reinterpret_cast<const void*>(kernel), PAIR_SMEM);
+        if (rc != MOE_OK) return rc;
+        const int sms = sm_count();
+        cfg.gridDim = dim3(sms > 0 ? (sms / 2) * 2 : 2, 1, 1);
+        int n = 0;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+        if (e != cudaSuccess || n <= 0)
+            return fail(MOE_ERR_CUDA, "%s: cannot place pairs of CTAs: %s", who, cudaGetErrorString(e));
+        max_pairs = n;
+        configured_for = dev;
+    }
+    constexpr int OUT_COLS = MODE == MODE_GATE_UP ? 128 : 256;
+    const long bound = static_cast<long>((p.max_padded + 255) / 256 + p.E) * ((p.n_out + OUT_COLS - 1) / OUT_COLS);
+    const long pairs = bound < max_pairs ? bound : max_pairs;
+    if (pairs <= 0) return MOE_OK;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, m.x, m.w, p);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
+    count_launch();
+    return check_launch(who);
+}
+
+template <int MODE>
 int dispatch(int wfmt, int act, int ntok, const Maps& m, const GemmParams& p, cudaStream_t st, const char* who) {
-    if (wfmt == MOE_W_BF16) return by_ntok<MODE, MOE_W_BF16, MOE_ACT_BF16>(ntok, m, p, st, who);
+    if (wfmt == MOE_W_BF16) {
+        if (ntok == 0) return launch_pair<MODE>(m, p, st, who);
+        return by_ntok<MODE, MOE_W_BF16, MOE_ACT_BF16>(ntok, m, p, st, who);
+    }
     if (wfmt == MOE_W_GPTQ_INT4)
         return act == MOE_ACT_F16 ? by_ntok<MODE, MOE_W_GPTQ_INT4, MOE_ACT_F16>(ntok, m, p, st, who)
                                   : by_ntok<MODE, MOE_W_GPTQ_INT4, MOE_ACT_BF16>(ntok, m, p, st, who);

@@ -254,14 +254,15 @@ def test_lora_row_adapter_and_gate_up_gather(dev):
         assert np.array_equal(got[skipped], g["y_bits"][skipped])
 
 
-def test_gemm_rejects_bad_offsets_on_device(dev):
+@pytest.mark.parametrize("name", ["tiny", "skewed"])   # decode form, CTA-pair prefill form
+def test_gemm_rejects_bad_offsets_on_device(dev, name):
     """expert_offsets that decrease: the GEMM runs no tile and flags the error."""
     import torch
     from mixture_experts_grouped_gb300 import moe
-    cfg = LAYER_CASES["tiny"]
+    cfg = LAYER_CASES[name]
     inp = synth.make_inputs(cfg)
     lay, _, _ = gpu_layer(cfg, inp, dev)
-    bad = torch.tensor([0, 64, 32, 96, 96, 96, 96, 96, 96], dtype=torch.int32, device=dev)
+    bad = torch.tensor([0, 64, 32] + [96] * (cfg.E - 2), dtype=torch.int32, device=dev)
     lay.err.zero_()
     y_before = lay.y.clone()
     moe.moe_grouped_down(lay.h, lay.act_code, lay.w_down.desc, lay.sorted_token_ids, bad, cfg.T, cfg.k, cfg.H, cfg.I,
