@@ -50,7 +50,7 @@ constexpr int W_STAGE = W_ROWS * BK * 2;  // 32 KB
 constexpr int RAW_STAGE = 9216;         // raw quantised bytes of one weight stage
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_DQ_WARPS = 8;  // two per SM sub-partition: dequantisation is latency-bound
-constexpr int MAX_STAGES = 8;
+constexpr int MAX_STAGES = 16;
 constexpr int MAX_RSTAGES = 16;
 constexpr int SMEM_LIMIT = 232448;      // dynamic shared memory per block (227 KB)
 
@@ -69,6 +69,8 @@ struct GemmParams {
     const float* scale2;
     int group_size;
     int32_t* err;
+    int block_size;  // align block size: spans are multiples of it, padding is a span's last < block_size rows
+    int pad_free;    // the kernel's tile height is a multiple of block_size: no tile holds padding only
 };
 
 struct SmemTail {
@@ -76,6 +78,8 @@ struct SmemTail {
     uint64_t empty[MAX_STAGES];
     uint64_t raw_full[MAX_RSTAGES];
     uint64_t raw_empty[MAX_RSTAGES];
+    uint64_t afull[4];   // TMEM weight stages (TS form)
+    uint64_t aempty[4];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t mma_done;
@@ -88,6 +92,9 @@ struct SmemTail {
 };
 
 constexpr int TAIL_BYTES = (static_cast<int>(sizeof(SmemTail)) + 127) / 128 * 128;
+
+// split accumulators per half for a swapped tile of ntok tokens (see load_swapped)
+__host__ __device__ constexpr int swapped_nacc(int ntok) { return ntok <= 32 ? 4 : (ntok <= 64 ? 2 : 1); }
 
 __host__ __device__ constexpr int pow2_at_least(int v) {
     int p = 32;
@@ -119,7 +126,8 @@ struct Shape {
     // fills the other), except for 256-row tiles, whose one accumulator of two
     // 128-row halves x 256 columns takes all 512 columns
     static constexpr int NBUF = PAIR ? 1 : 2;
-    static constexpr int ACC = SWAP ? 2 * NTOK : (PAIR ? 512 : 256);  // TMEM columns per buffer
+    static constexpr int NACC = SWAP ? swapped_nacc(NTOK) : 1;  // split accumulators per half
+    static constexpr int ACC = SWAP ? 2 * NTOK * NACC : (PAIR ? 512 : 256);  // TMEM columns per buffer
     static constexpr int TMEM_COLS = pow2_at_least(NBUF * ACC);
     static constexpr int OUT_COLS = MODE == MODE_GATE_UP ? 128 : 256;  // output columns per tile
     static constexpr int THREADS = 192 + (QUANT ? 32 * (NUM_DQ_WARPS + 1) : 0);
@@ -155,9 +163,12 @@ __device__ __forceinline__ TileInfo decode_tile(const SmemTail& s, int E, int ti
     return t;
 }
 
-// a tile whose first row is a padding row holds padding only
+// A tile whose first row is a padding row holds padding only. That cannot
+// happen when the tile height is a multiple of the block size: a span is
+// whole blocks and its padding is less than one block, so every tile of a
+// span starts on a real row.
 __device__ __forceinline__ bool tile_is_padding(const GemmParams& p, const TileInfo& t) {
-    return __ldg(p.sorted_ids + t.m0) == p.P;
+    return !p.pad_free && __ldg(p.sorted_ids + t.m0) == p.P;
 }
 
 // weight-tile row n (0..255) -> output column it feeds, and whether that column exists
@@ -171,6 +182,52 @@ template <int MODE>
 __device__ __forceinline__ void half_bases(const GemmParams& p, int n0, int& c0, int& c1) {
     c0 = n0;
     c1 = (MODE == MODE_GATE_UP) ? p.n_out + n0 : n0 + 128;
+}
+
+// Every CTA builds the tile list from expert_offsets in shared memory: the
+// offsets, and per expert the index of its first tile (row tiles of XROWS
+// fastest, then column tiles of out_cols). Offsets that are negative,
+// decreasing or beyond max_padded yield an empty list. Returns nonzero for
+// bad offsets (the caller records the error once).
+template <int XROWS>
+__device__ __forceinline__ int build_tile_list(SmemTail& s, const GemmParams& p, int out_cols) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int E = p.E;
+    for (int i = tid; i <= E; i += blockDim.x) s.off[i] = p.offsets[i];
+    if (tid == 0) {
+        s.abort_flag = 0;
+        s.nt = (p.n_out + out_cols - 1) / out_cols;
+    }
+    __syncthreads();
+    int bad = 0;
+    for (int i = tid; i < E; i += blockDim.x) bad |= (s.off[i + 1] < s.off[i]);
+    if (tid == 0) bad |= (s.off[0] < 0) | (s.off[E] > p.max_padded);
+    bad = __syncthreads_or(bad);
+    if (warp == 0) {
+        // lane l owns experts [l * per, (l + 1) * per): local sums, warp scan, exclusive prefix
+        const int per = (E + 31) / 32;
+        int loc = 0;
+        for (int j = 0; j < per; ++j) {
+            const int e = lane * per + j;
+            if (e < E) loc += ((s.off[e + 1] - s.off[e] + XROWS - 1) / XROWS) * s.nt;
+        }
+        int inc = loc;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, inc, d);
+            if (lane >= d) inc += o;
+        }
+        int run = inc - loc;
+        for (int j = 0; j < per; ++j) {
+            const int e = lane * per + j;
+            if (e < E) {
+                s.tstart[e] = run;
+                run += ((s.off[e + 1] - s.off[e] + XROWS - 1) / XROWS) * s.nt;
+            }
+        }
+        if (lane == 31) s.n_tiles = bad ? 0 : inc;
+    }
+    return bad;
 }
 
 // ---- dequantisation: raw shared bytes -> swizzled 16-bit weight tile -------------
@@ -345,11 +402,12 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 }
 
 // Rows of the tile that hold a pair: padding rows only sit at the end of an
-// expert's span, so they are a suffix of the span's last tile. Each calling
-// warp finds the first padding row with a ballot over sorted_token_ids.
+// expert's span, fewer than block_size of them, so they are a suffix of the
+// span's last tile within its last block_size - 1 rows. Each calling warp
+// finds the first padding row with ballots over those sorted_token_ids.
 __device__ __forceinline__ int valid_rows(const GemmParams& p, const SmemTail& s, const TileInfo& t, int lane) {
     if (t.m0 + t.rows != s.off[t.e + 1]) return t.rows;  // not the span's last tile
-    for (int base = 0; base < t.rows; base += 32) {
+    for (int base = max(0, t.rows - (p.block_size - 1)); base < t.rows; base += 32) {
         const int r = base + lane;
         const bool pad = r < t.rows && __ldg(p.sorted_ids + t.m0 + r) == p.P;
         const unsigned m = __ballot_sync(0xffffffffu, pad);
@@ -367,6 +425,37 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 
+// Swapped forms (D = weight row x token): each half's accumulator is split
+// into NACC accumulators of NTOK columns that take the K=16 steps in turn,
+// so consecutive MMAs of a half do not depend on each other and the tensor
+// core overlaps them (a single accumulator makes every MMA wait for the one
+// before it, which dominates when N is small). Half 0 owns columns
+// [0, NACC*NTOK), half 1 the next NACC*NTOK. This loads tokens [c, c+16) of
+// both halves and sums the split accumulators in f32.
+template <int NTOK, int NACC>
+__device__ __forceinline__ void load_swapped(uint32_t taddr, int c, float (&fa)[16], float (&fb)[16]) {
+    uint32_t a[16], b[16];
+    tmem_ld16(taddr + c, a);
+    tmem_ld16(taddr + NACC * NTOK + c, b);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        fa[j] = __uint_as_float(a[j]);
+        fb[j] = __uint_as_float(b[j]);
+    }
+#pragma unroll
+    for (int q = 1; q < NACC; ++q) {
+        tmem_ld16(taddr + q * NTOK + c, a);
+        tmem_ld16(taddr + (NACC + q) * NTOK + c, b);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            fa[j] += __uint_as_float(a[j]);
+            fb[j] += __uint_as_float(b[j]);
+        }
+    }
+}
+
 // ---- the kernel ------------------------------------------------------------------
 
 template <int MODE, int WFMT, int ACT, int NTOK>
@@ -377,7 +466,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     using S = Shape<MODE, WFMT, ACT, NTOK>;
     constexpr int XROWS = S::XROWS, STAGES = S::STAGES, RSTAGES = S::RSTAGES;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = align1024_shared(smem_raw);
     uint8_t* sX = smem;
     uint8_t* sW = smem + STAGES * S::X_STAGE;
     uint8_t* sR = sW + STAGES * W_STAGE;
@@ -388,41 +477,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     const int warp = tid >> 5, lane = tid & 31;
     const int E = p.E;
 
-    // ---- tile list from expert_offsets ----
-    for (int i = tid; i <= E; i += blockDim.x) s.off[i] = p.offsets[i];
-    if (tid == 0) {
-        s.abort_flag = 0;
-        s.nt = (p.n_out + S::OUT_COLS - 1) / S::OUT_COLS;
-    }
-    __syncthreads();
-    int bad = 0;
-    for (int i = tid; i < E; i += blockDim.x) bad |= (s.off[i + 1] < s.off[i]);
-    if (tid == 0) bad |= (s.off[0] < 0) | (s.off[E] > p.max_padded);
-    bad = __syncthreads_or(bad);
-    if (warp == 0) {
-        // lane l owns experts [l * per, (l + 1) * per): local sums, warp scan, exclusive prefix
-        const int per = (E + 31) / 32;
-        int loc = 0;
-        for (int j = 0; j < per; ++j) {
-            const int e = lane * per + j;
-            if (e < E) loc += ((s.off[e + 1] - s.off[e] + XROWS - 1) / XROWS) * s.nt;
-        }
-        int inc = loc;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, inc, d);
-            if (lane >= d) inc += o;
-        }
-        int run = inc - loc;
-        for (int j = 0; j < per; ++j) {
-            const int e = lane * per + j;
-            if (e < E) {
-                s.tstart[e] = run;
-                run += ((s.off[e + 1] - s.off[e] + XROWS - 1) / XROWS) * s.nt;
-            }
-        }
-        if (lane == 31) s.n_tiles = bad ? 0 : inc;
-    }
+    const int bad = build_tile_list<XROWS>(s, p, S::OUT_COLS);
     if (tid == 0) {
         if (bad) set_err(p.err, MOE_DEV_ERR_OFFSETS);
 #pragma unroll
@@ -520,8 +575,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                         const uint64_t wd1 = sw128_desc(smem_u32(sW + stage * W_STAGE + W_STAGE / 2));
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k) {
-                            tc_mma(d, wd + 2 * k, xd + 2 * k, idesc, (kb | k) != 0);
-                            tc_mma(d + NTOK, wd1 + 2 * k, xd + 2 * k, idesc, (kb | k) != 0);
+                            const int a = k % S::NACC;
+                            const uint32_t en = kb > 0 || k >= S::NACC;
+                            tc_mma(d + a * NTOK, wd + 2 * k, xd + 2 * k, idesc, en);
+                            tc_mma(d + (S::NACC + a) * NTOK, wd1 + 2 * k, xd + 2 * k, idesc, en);
                         }
                     } else {
                         const uint64_t xd1 = sw128_desc(smem_u32(sX + stage * S::X_STAGE + 128 * BK * 2));
@@ -552,15 +609,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             const int acc = S::NBUF == 2 ? (local & 1) : 0;
             const uint32_t aph = S::NBUF == 2 ? ((local >> 1) & 1) : (local & 1);
             ++local;
-            if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
-            tc_fence_after();
+            // tile metadata first: its loads overlap the wait for the accumulator
+            const int nvalid = valid_rows(p, s, t, lane);
             float s2a = 1.0f, s2b = 1.0f;
             if (WFMT == MOE_W_NVFP4) {
                 s2a = __ldg(p.scale2 + t.e);
                 s2b = (MODE == MODE_GATE_UP) ? __ldg(p.scale2 + p.E + t.e) : s2a;
             }
+            if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
+            tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * S::ACC;
-            const int nvalid = valid_rows(p, s, t, lane);
             if (!S::SWAP) {
                 // lane = activation row of each 128-row half; columns = weight rows
                 // (gate | up, or 256 outputs)
@@ -620,10 +678,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 const int col_b = (MODE == MODE_GATE_UP) ? col_a : t.n0 + 128 + lrow;  // up / high half
 #pragma unroll 1
                 for (int c = 0; c < NTOK && c < nvalid; c += 16) {
-                    uint32_t a[16], b[16];
-                    tmem_ld16(taddr + c, a);
-                    tmem_ld16(taddr + NTOK + c, b);
-                    tmem_ld_wait();
+                    float a[16], b[16];
+                    load_swapped<(NTOK > 0 ? NTOK : 16), S::NACC>(taddr, c, a, b);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int r = c + j;
@@ -631,11 +687,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                             const size_t orow = static_cast<size_t>(t.m0 + r) * p.n_out;
                             if (MODE == MODE_GATE_UP) {
                                 if (col_a < p.n_out)
-                                    out[orow + col_a] = Act<ACT>::from_f(
-                                        silu_mul(__uint_as_float(a[j]) * s2a, __uint_as_float(b[j]) * s2b));
+                                    out[orow + col_a] = Act<ACT>::from_f(silu_mul(a[j] * s2a, b[j] * s2b));
                             } else {
-                                if (col_a < p.n_out) out[orow + col_a] = Act<ACT>::from_f(__uint_as_float(a[j]) * s2a);
-                                if (col_b < p.n_out) out[orow + col_b] = Act<ACT>::from_f(__uint_as_float(b[j]) * s2a);
+                                if (col_a < p.n_out) out[orow + col_a] = Act<ACT>::from_f(a[j] * s2a);
+                                if (col_b < p.n_out) out[orow + col_b] = Act<ACT>::from_f(b[j] * s2a);
                             }
                         }
                     }
@@ -746,7 +801,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
     constexpr int XROWS = 256;
     constexpr int OUT_COLS = MODE == MODE_GATE_UP ? 128 : 256;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = align1024_shared(smem_raw);
     uint8_t* sA = smem;
     uint8_t* sB = smem + PAIR_STAGES * PAIR_A;
     SmemTail& s = *reinterpret_cast<SmemTail*>(sB + PAIR_STAGES * PAIR_B);
@@ -758,40 +813,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     const int E = p.E;
 
-    // ---- tile list from expert_offsets (identical in both CTAs) ----
-    for (int i = tid; i <= E; i += blockDim.x) s.off[i] = p.offsets[i];
-    if (tid == 0) {
-        s.abort_flag = 0;
-        s.nt = (p.n_out + OUT_COLS - 1) / OUT_COLS;
-    }
-    __syncthreads();
-    int bad = 0;
-    for (int i = tid; i < E; i += blockDim.x) bad |= (s.off[i + 1] < s.off[i]);
-    if (tid == 0) bad |= (s.off[0] < 0) | (s.off[E] > p.max_padded);
-    bad = __syncthreads_or(bad);
-    if (warp == 0) {
-        const int per = (E + 31) / 32;
-        int loc = 0;
-        for (int j = 0; j < per; ++j) {
-            const int e = lane * per + j;
-            if (e < E) loc += ((s.off[e + 1] - s.off[e] + XROWS - 1) / XROWS) * s.nt;
-        }
-        int inc = loc;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, inc, d);
-            if (lane >= d) inc += o;
-        }
-        int run = inc - loc;
-        for (int j = 0; j < per; ++j) {
-            const int e = lane * per + j;
-            if (e < E) {
-                s.tstart[e] = run;
-                run += ((s.off[e + 1] - s.off[e] + XROWS - 1) / XROWS) * s.nt;
-            }
-        }
-        if (lane == 31) s.n_tiles = bad ? 0 : inc;
-    }
+    const int bad = build_tile_list<XROWS>(s, p, OUT_COLS);  // identical in both CTAs
     if (tid == 0) {
         if (bad && rank == 0) set_err(p.err, MOE_DEV_ERR_OFFSETS);
         for (int i = 0; i < PAIR_STAGES; ++i) {
@@ -899,9 +921,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
             const int acc = local & 1;
             const uint32_t aph = (local >> 1) & 1;
             ++local;
+            const int nvalid = valid_rows(p, s, t, lane);  // its loads overlap the wait
             if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
             tc_fence_after();
-            const int nvalid = valid_rows(p, s, t, lane);
             const int row = static_cast<int>(rank) * 128 + lrow;
             const bool row_ok = row < nvalid;
             const size_t orow = static_cast<size_t>(t.m0 + row) * p.n_out;
@@ -963,16 +985,474 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
     if (warp == 1) tmem_dealloc_pair(tmem_base, 512);
 }
 
+// ---- TS form: quantised weights dequantised into TMEM ----------------------------
+//
+// For GPTQ and NVFP4 weights the weight tile is the MMA's A operand and lives
+// in TMEM: eight dequantising warps each own 32 weight rows (TMEM lanes) of
+// one 128-row half and write a row's 64 k values of a k block as 32 columns
+// with tcgen05.st. The activations (NTOK token rows) are the B operand in
+// shared memory, fed by TMA. D is (weight row x token), two halves (gate |
+// up, or two 128-column halves of the output) of NTOK columns each. Shared
+// memory then carries only the raw quantised bytes and the activations; the
+// 16-bit weights never touch it.
+constexpr int TS_STAGES = 4;   // weight stages in TMEM
+constexpr int TS_A_COL = 256;  // first TMEM column of the weight stages (64 columns each)
+
+template <int MODE, int WFMT, int ACT, int NTOK>
+struct TsShape {
+    static constexpr int X_STAGE = NTOK * BK * 2;
+    static constexpr int NACC = swapped_nacc(NTOK);  // split accumulators per half
+    static constexpr int ACC = 2 * NTOK * NACC;     // TMEM columns per accumulator buffer
+    static constexpr int NBUF = 2 * ACC <= TS_A_COL ? 2 : 1;
+    static constexpr int OUT_COLS = MODE == MODE_GATE_UP ? 128 : 256;
+    // MMA-issuing warps. One thread issues a tcgen05.mma about every 100
+    // cycles whatever its N, so at small N the issue rate, not the tensor
+    // core, bounds a single issuer; several issuers, each owning its own
+    // accumulators (half h, split a: issuer (h * NACC + a) % NI), multiply it.
+    static constexpr int NI = 2 * NACC >= 4 ? 4 : 2;
+    static constexpr int EPI0 = 1 + NI;                 // first epilogue warp
+    static constexpr int DQ0 = EPI0 + NUM_EPI_WARPS;    // first dequantising warp
+    static constexpr int RAWW = DQ0 + NUM_DQ_WARPS;     // raw producer warp
+    static constexpr int THREADS = 32 * (RAWW + 1);
+    static constexpr int AVAIL = SMEM_LIMIT - 1024 - TAIL_BYTES;
+    // The activation ring is its own, deeper than the TMEM weight ring: its
+    // loads queue behind the raw weight stream, so they need as much time in
+    // flight as the raw bytes do. At least 8 raw stages are kept.
+    static constexpr int X_FIT = (AVAIL - 8 * RAW_STAGE) / X_STAGE;
+    static constexpr int XSTAGES = X_FIT < 12 ? X_FIT : 12;
+    static constexpr int RAW_FIT = (AVAIL - XSTAGES * X_STAGE) / RAW_STAGE;
+    static constexpr int RSTAGES = RAW_FIT < MAX_RSTAGES ? RAW_FIT : MAX_RSTAGES;
+    static constexpr int SMEM = 1024 + XSTAGES * X_STAGE + RSTAGES * RAW_STAGE + TAIL_BYTES;
+    static constexpr int RAW_BYTES = WFMT == MOE_W_GPTQ_INT4 ? 8832 : 9216;
+    // GPTQ gate/up writes each group of 8 k values in the order 0,4,1,5,2,6,3,7
+    // (the order the int4 -> fp16 conversion produces them in); the gather
+    // kernel stores the activations in the same order, so the products match
+    static constexpr bool PERM = WFMT == MOE_W_GPTQ_INT4 && MODE == MODE_GATE_UP;
+    static_assert(NBUF * ACC <= TS_A_COL, "accumulators overlap the weight stages");
+    static_assert(TS_A_COL + TS_STAGES * 64 <= 512, "weight stages exceed TMEM");
+    static_assert(XSTAGES >= 4 && XSTAGES <= MAX_STAGES, "activation ring size");
+    static_assert(RSTAGES >= 8, "not enough shared memory for the raw ring");
+    static_assert(SMEM <= SMEM_LIMIT, "shared memory over the limit");
+};
+
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t mask, uint32_t bits) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(mask), "r"(bits));  // (a & mask) | bits
+    return r;
+}
+
+// One GPTQ weight row for a 64-deep k block: word i holds the codes of k =
+// 8i .. 8i+7 (4 bits each, k order from the low bits), z the zero point and
+// sh the fp16 scale of the row's group. Writes (q - z) * s as 32 columns of
+// two 16-bit values. fp16: 1024 + q and 1024 + 16q come from the code bits
+// by one mask-or each (exact), subtracting the zero point is exact, and the
+// product with s is the only rounding.
+template <int ACT, bool PERM>
+__device__ __forceinline__ void gptq_row(const uint32_t (&w)[8], int z, __half sh, uint32_t (&o)[32]) {
+    if (ACT == MOE_ACT_F16) {
+        const __half2 s2 = __half2half2(sh);
+        const __half2 z1 = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400 | z)));      // 1024 + z
+        const __half2 c16 = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x2C00)));         // 1/16
+        const __half2 nz16 = __half2half2(__ushort_as_half(static_cast<unsigned short>(0xD400 | (z << 4))));  // -(64 + z)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w8 = w[i] >> 8;
+            uint32_t q[4] = {and_or(w[i], 0x000F000Fu, 0x64006400u),   // (k0, k4): 1024 + q
+                             and_or(w[i], 0x00F000F0u, 0x64006400u),   // (k1, k5): 1024 + 16 q
+                             and_or(w8, 0x000F000Fu, 0x64006400u),     // (k2, k6)
+                             and_or(w8, 0x00F000F0u, 0x64006400u)};    // (k3, k7)
+            uint32_t d[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const __half2 h = *reinterpret_cast<__half2*>(&q[j]);
+                const __half2 qz = (j & 1) ? __hfma2(h, c16, nz16) : __hsub2(h, z1);  // q - z, exact
+                __half2 v = __hmul2(qz, s2);
+                d[j] = *reinterpret_cast<uint32_t*>(&v);
+            }
+            if (PERM) {
+                o[4 * i + 0] = d[0];
+                o[4 * i + 1] = d[1];
+                o[4 * i + 2] = d[2];
+                o[4 * i + 3] = d[3];
+            } else {
+                o[4 * i + 0] = prmt(d[0], d[1], 0x5410);  // (k0, k1)
+                o[4 * i + 1] = prmt(d[2], d[3], 0x5410);  // (k2, k3)
+                o[4 * i + 2] = prmt(d[0], d[1], 0x7632);  // (k4, k5)
+                o[4 * i + 3] = prmt(d[2], d[3], 0x7632);  // (k6, k7)
+            }
+        }
+    } else {
+        // bf16 activations: (q - z) * s is exact in f32 (a 5-bit integer times
+        // an fp16 value) and rounds once to bf16
+        const float s = __half2float(sh);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = static_cast<float>(static_cast<int>((w[i] >> (4 * j)) & 15u) - z) * s;
+            if (PERM) {
+                o[4 * i + 0] = Act<ACT>::pack2(f[0], f[4]);
+                o[4 * i + 1] = Act<ACT>::pack2(f[1], f[5]);
+                o[4 * i + 2] = Act<ACT>::pack2(f[2], f[6]);
+                o[4 * i + 3] = Act<ACT>::pack2(f[3], f[7]);
+            } else {
+                o[4 * i + 0] = Act<ACT>::pack2(f[0], f[1]);
+                o[4 * i + 1] = Act<ACT>::pack2(f[2], f[3]);
+                o[4 * i + 2] = Act<ACT>::pack2(f[4], f[5]);
+                o[4 * i + 3] = Act<ACT>::pack2(f[6], f[7]);
+            }
+        }
+    }
+}
+
+// One NVFP4 weight row for a 64-deep k block: word i holds the E2M1 codes of
+// k = 8i .. 8i+7 (low nibble first), sc[g] the E4M3 scale of k = 16g ..
+// 16g+15. E2M1 x E4M3 products are exact in bf16 and fp16.
+template <int ACT>
+__device__ __forceinline__ void nvfp4_row(const uint32_t (&w)[8], const uint32_t (&sc)[4], uint32_t (&o)[32]) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if (ACT == MOE_ACT_BF16) {
+            const __nv_bfloat162 s2 = __float2bfloat162_rn(e4m3_to_f32(sc[g]));
+#pragma unroll
+            for (int ii = 0; ii < 2; ++ii) {
+                const int i = 2 * g + ii;
+                uint32_t a[4];
+                e2m1x4_to_bf16x4(w[i], a[0], a[1]);
+                e2m1x4_to_bf16x4(w[i] >> 16, a[2], a[3]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    __nv_bfloat162 v = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a[j]), s2);
+                    o[4 * i + j] = *reinterpret_cast<uint32_t*>(&v);
+                }
+            }
+        } else {
+            const __half2 s2 = __float2half2_rn(e4m3_to_f32(sc[g]));
+#pragma unroll
+            for (int ii = 0; ii < 2; ++ii) {
+                const int i = 2 * g + ii;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t e2 = e2m1x2_to_f16x2((w[i] >> (8 * j)) & 0xffu);
+                    __half2 v = __hmul2(*reinterpret_cast<__half2*>(&e2), s2);
+                    o[4 * i + j] = *reinterpret_cast<uint32_t*>(&v);
+                }
+            }
+        }
+    }
+}
+
+// One weight row's raw bytes for a k block, in registers: GPTQ 8 words, the
+// fp16 scale bits and the packed zero-point word; NVFP4 8 words and 4 scale
+// bytes.
+struct RawRow {
+    uint32_t w[8];
+    uint32_t s, z;
+    uint32_t sc[4];
+};
+
+template <int WFMT>
+__device__ __forceinline__ void load_raw_row(const uint8_t* raw, int h, int r, RawRow& x) {
+    if (WFMT == MOE_W_GPTQ_INT4) {
+        // qweight [2 halves][8 packed k rows][128 cols] int32, scales [2][128] fp16, zeros [2][16] int32
+        const uint32_t* qw = reinterpret_cast<const uint32_t*>(raw + h * 4096);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x.w[i] = qw[i * 128 + r];
+        x.s = reinterpret_cast<const unsigned short*>(raw + 8192 + h * 256)[r];
+        x.z = reinterpret_cast<const uint32_t*>(raw + 8704 + h * 128)[r >> 3];
+    } else {
+        // packed [2 halves][128 rows][32 bytes], scales [2][4 k16 groups][128 rows] E4M3
+        const uint4* row = reinterpret_cast<const uint4*>(raw + h * 4096 + r * 32);
+        const uint4 v0 = row[0], v1 = row[1];
+        x.w[0] = v0.x; x.w[1] = v0.y; x.w[2] = v0.z; x.w[3] = v0.w;
+        x.w[4] = v1.x; x.w[5] = v1.y; x.w[6] = v1.z; x.w[7] = v1.w;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) x.sc[g] = raw[8192 + h * 512 + g * 128 + r];
+    }
+}
+
+template <int MODE, int WFMT, int ACT, int NTOK>
+__global__ void __launch_bounds__(TsShape<MODE, WFMT, ACT, NTOK>::THREADS, 1)
+grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmR0,
+                       const __grid_constant__ CUtensorMap tmR1, const __grid_constant__ CUtensorMap tmR2,
+                       const GemmParams p) {
+    using S = TsShape<MODE, WFMT, ACT, NTOK>;
+    constexpr int XROWS = NTOK, XSTAGES = S::XSTAGES, ASTAGES = TS_STAGES, RSTAGES = S::RSTAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024_shared(smem_raw);
+    uint8_t* sX = smem;
+    uint8_t* sR = sX + XSTAGES * S::X_STAGE;
+    SmemTail& s = *reinterpret_cast<SmemTail*>(sR + RSTAGES * RAW_STAGE);
+    volatile int* abort_flag = &s.abort_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int E = p.E;
+
+    const int bad = build_tile_list<XROWS>(s, p, S::OUT_COLS);
+    if (tid == 0) {
+        if (bad) set_err(p.err, MOE_DEV_ERR_OFFSETS);
+#pragma unroll
+        for (int i = 0; i < XSTAGES; ++i) {
+            mbar_init(&s.full[i], 1);  // activation bytes
+            mbar_init(&s.empty[i], S::NI);
+        }
+#pragma unroll
+        for (int i = 0; i < ASTAGES; ++i) {
+            mbar_init(&s.afull[i], NUM_DQ_WARPS);  // every dequantising warp has written its rows
+            mbar_init(&s.aempty[i], S::NI);
+        }
+#pragma unroll
+        for (int i = 0; i < RSTAGES; ++i) {
+            mbar_init(&s.raw_full[i], 1);
+            mbar_init(&s.raw_empty[i], NUM_DQ_WARPS);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.tfull[i], S::NI);
+            mbar_init(&s.tempty[i], NUM_EPI_WARPS);
+        }
+        mbar_init(&s.mma_done, S::NI);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int n_tiles = s.n_tiles;
+    if (static_cast<int>(blockIdx.x) >= n_tiles) return;  // block-uniform: nothing allocated yet
+
+    if (warp == 1) {
+        tmem_alloc(&s.tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&tmX);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = s.tmem_base;
+    const int KB = (p.K + BK - 1) / BK;  // a ragged last block is zero-filled
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer: activations ----------------
+            uint32_t stage = 0, phase = 0;
+            long issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+                const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
+                if (tile_is_padding(p, t)) continue;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&s.full[stage], S::X_STAGE);
+                    tma_load_2d(sX + stage * S::X_STAGE, &tmX, kb * BK, t.m0, &s.full[stage]);
+                    ++issued;
+                    if (++stage == XSTAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            const long first = issued > XSTAGES ? issued - XSTAGES : 0;
+            for (long j = first; j < issued; ++j)
+                mbar_drain(&s.full[j % XSTAGES], static_cast<uint32_t>((j / XSTAGES) & 1), kWaitLimitNs / 8);
+        }
+    } else if (warp < S::EPI0) {
+        if (lane == 0) {
+            // ---------------- MMA issuers: A = weights (TMEM), B = activations ----------------
+            const int mi = warp - 1;  // this issuer's accumulators: (h * NACC + a) % NI == mi
+            constexpr uint32_t idesc = f16_idesc(ACT, 128, NTOK);
+            uint32_t stage = 0, phase = 0, astage = 0, aphase = 0;
+            int local = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+                const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
+                if (tile_is_padding(p, t)) continue;
+                const int acc = S::NBUF == 2 ? (local & 1) : 0;
+                const uint32_t aph = S::NBUF == 2 ? ((local >> 1) & 1) : (local & 1);
+                ++local;
+                if (!mbar_wait(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + acc * S::ACC;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&s.full[stage], phase, abort_flag, p.err) ||
+                        !mbar_wait(&s.afull[astage], aphase, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t xd = sw128_desc(smem_u32(sX + stage * S::X_STAGE));
+                    const uint32_t a0 = tmem_base + TS_A_COL + astage * 64;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const int a = k % S::NACC;
+                        const uint32_t en = kb > 0 || k >= S::NACC;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            if ((h * S::NACC + a) % S::NI == mi)
+                                tc_mma_ts(d + (h * S::NACC + a) * NTOK, a0 + 32 * h + 8 * k, xd + 2 * k, idesc, en);
+                    }
+                    tc_commit(&s.empty[stage]);
+                    tc_commit(&s.aempty[astage]);
+                    if (++stage == XSTAGES) { stage = 0; phase ^= 1; }
+                    if (++astage == ASTAGES) { astage = 0; aphase ^= 1; }
+                }
+                if (!ok) break;
+                tc_commit(&s.tfull[acc]);
+            }
+            tc_commit(&s.mma_done);
+            mbar_drain(&s.mma_done, 0, kWaitLimitNs / 8);
+        }
+        __syncwarp();
+    } else if (warp < S::DQ0) {
+        // ---------------- epilogue: lane = weight row of a half, columns = tokens ----------------
+        const int q = warp & 3;
+        const int lrow = q * 32 + lane;
+        using T = typename Act<ACT>::T;
+        T* out = static_cast<T*>(p.out);
+        int local = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
+            if (tile_is_padding(p, t)) continue;
+            const int acc = S::NBUF == 2 ? (local & 1) : 0;
+            const uint32_t aph = S::NBUF == 2 ? ((local >> 1) & 1) : (local & 1);
+            ++local;
+            // tile metadata first: its loads overlap the wait for the accumulator
+            const int nvalid = valid_rows(p, s, t, lane);
+            float s2a = 1.0f, s2b = 1.0f;
+            if (WFMT == MOE_W_NVFP4) {
+                s2a = __ldg(p.scale2 + t.e);
+                s2b = (MODE == MODE_GATE_UP) ? __ldg(p.scale2 + p.E + t.e) : s2a;
+            }
+            if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * S::ACC;
+            const int col_a = t.n0 + lrow;                                          // gate / low half
+            const int col_b = (MODE == MODE_GATE_UP) ? col_a : t.n0 + 128 + lrow;  // up / high half
+#pragma unroll 1
+            for (int c = 0; c < NTOK && c < nvalid; c += 16) {
+                float a[16], b[16];
+                load_swapped<NTOK, S::NACC>(taddr, c, a, b);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int r = c + j;
+                    if (r < nvalid) {
+                        const size_t orow = static_cast<size_t>(t.m0 + r) * p.n_out;
+                        if (MODE == MODE_GATE_UP) {
+                            if (col_a < p.n_out)
+                                out[orow + col_a] = Act<ACT>::from_f(silu_mul(a[j] * s2a, b[j] * s2b));
+                        } else {
+                            if (col_a < p.n_out) out[orow + col_a] = Act<ACT>::from_f(a[j] * s2a);
+                            if (col_b < p.n_out) out[orow + col_b] = Act<ACT>::from_f(b[j] * s2a);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.tempty[acc]);
+        }
+    } else if (warp < S::RAWW) {
+        // ---------------- dequantising warps: raw shared bytes -> TMEM ----------------
+        // The raw stages arrive in order, one per k block of every non-padding
+        // tile of this CTA; the next stage's bytes are loaded into registers
+        // before the current one is converted, to hide the shared-memory latency.
+        const int h = (warp - S::DQ0) >> 2;  // weight half
+        const int sp = warp & 3;                          // TMEM lane quarter this warp may access
+        const int r = sp * 32 + lane;                     // weight row within the half
+        const uint32_t trow = tmem_base + (static_cast<uint32_t>(sp * 32) << 16) + TS_A_COL + h * 32;
+        long items = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x)
+            if (!tile_is_padding(p, decode_tile<XROWS>(s, E, tile, S::OUT_COLS))) items += KB;
+        RawRow cur, nxt;
+        uint32_t stage = 0, phase = 0, rstage = 0, rphase = 0;
+        bool ok = items > 0 && mbar_wait(&s.raw_full[0], 0, abort_flag, p.err);
+        if (ok) {
+            load_raw_row<WFMT>(sR, h, r, cur);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.raw_empty[0]);
+            if (++rstage == RSTAGES) { rstage = 0; rphase ^= 1; }
+        }
+        for (long it = 0; it < items && ok; ++it) {
+            if (it + 1 < items) {
+                if (!mbar_wait(&s.raw_full[rstage], rphase, abort_flag, p.err)) break;
+                load_raw_row<WFMT>(sR + rstage * RAW_STAGE, h, r, nxt);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.raw_empty[rstage]);
+                if (++rstage == RSTAGES) { rstage = 0; rphase ^= 1; }
+            }
+            uint32_t o[32];
+            if (WFMT == MOE_W_GPTQ_INT4)
+                gptq_row<ACT, S::PERM>(cur.w, (cur.z >> (4 * (r & 7))) & 15, __ushort_as_half(static_cast<unsigned short>(cur.s)), o);
+            else
+                nvfp4_row<ACT>(cur.w, cur.sc, o);
+            if (!mbar_wait(&s.aempty[stage], phase ^ 1, abort_flag, p.err)) break;
+            tc_fence_after();  // the MMAs that read this TMEM stage have completed
+            tmem_st32(trow + stage * 64, o);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.afull[stage]);
+            if (++stage == ASTAGES) { stage = 0; phase ^= 1; }
+            cur = nxt;
+        }
+    } else {
+        // ---------------- raw quantised-weight producer (last warp) ----------------
+        if (lane == 0) {
+            uint32_t rstage = 0, rphase = 0;
+            long issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+                const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
+                if (tile_is_padding(p, t)) continue;
+                int c0, c1;
+                half_bases<MODE>(p, t.n0, c0, c1);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&s.raw_empty[rstage], rphase ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    uint64_t* bar = &s.raw_full[rstage];
+                    uint8_t* rw = sR + rstage * RAW_STAGE;
+                    mbar_arrive_expect_tx(bar, S::RAW_BYTES);
+                    if (WFMT == MOE_W_GPTQ_INT4) {
+                        const int kq = t.e * (p.K / 8) + kb * 8;
+                        const int g = t.e * (p.K / p.group_size) + (kb * BK) / p.group_size;
+                        tma_load_2d(rw, &tmR0, c0, kq, bar);
+                        tma_load_2d(rw + 4096, &tmR0, c1, kq, bar);
+                        tma_load_2d(rw + 8192, &tmR1, c0, g, bar);
+                        tma_load_2d(rw + 8448, &tmR1, c1, g, bar);
+                        tma_load_2d(rw + 8704, &tmR2, c0 / 8, g, bar);
+                        tma_load_2d(rw + 8832, &tmR2, c1 / 8, g, bar);
+                    } else {
+                        tma_load_2d(rw, &tmR0, kb * (BK / 2), t.e * p.n_w + c0, bar);
+                        tma_load_2d(rw + 4096, &tmR0, kb * (BK / 2), t.e * p.n_w + c1, bar);
+                        const int sg = t.e * (p.K / 16) + kb * (BK / 16);
+                        tma_load_2d(rw + 8192, &tmR1, c0, sg, bar);
+                        tma_load_2d(rw + 8704, &tmR1, c1, sg, bar);
+                    }
+                    ++issued;
+                    if (++rstage == RSTAGES) { rstage = 0; rphase ^= 1; }
+                }
+            }
+            const long first = issued > RSTAGES ? issued - RSTAGES : 0;
+            for (long j = first; j < issued; ++j)
+                mbar_drain(&s.raw_full[j % RSTAGES], static_cast<uint32_t>((j / RSTAGES) & 1), kWaitLimitNs / 8);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
 // ---- gather of the activations into sorted-row order ---------------------------
 
 // xs[r] = x[sorted_token_ids[r] / top_k] for r < expert_offsets[E]. Padding
 // rows are left as they are: the GEMM epilogues never store a padding row,
 // and a row of the MMA only feeds its own output row (or column). One warp
-// per row, 16-byte vectors.
+// per row, 16-byte vectors. With perm set, each group of 8 elements is stored
+// in the order 0,4,1,5,2,6,3,7 (the k order of the GPTQ gate/up weights).
+__device__ __forceinline__ uint4 perm8(uint4 v) {
+    return make_uint4(prmt(v.x, v.z, 0x5410), prmt(v.x, v.z, 0x7632), prmt(v.y, v.w, 0x5410),
+                      prmt(v.y, v.w, 0x7632));
+}
+
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_ids,
                    const int32_t* __restrict__ offsets, int E, int T, int top_k, int vec_per_row, int max_padded,
-                   uint4* __restrict__ xs, int32_t* err) {
+                   int perm, uint4* __restrict__ xs, int32_t* err) {
     const int total = min(__ldg(offsets + E), max_padded);
     const int P = T * top_k;
     for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < total; r += gridDim.x * 8) {
@@ -983,7 +1463,10 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sort
         if (tok < 0) continue;
         uint4* dst = xs + static_cast<size_t>(r) * vec_per_row;
         const uint4* src = x + static_cast<size_t>(tok) * vec_per_row;
-        for (int v = threadIdx.x & 31; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+        if (perm)
+            for (int v = threadIdx.x & 31; v < vec_per_row; v += 32) dst[v] = perm8(__ldg(src + v));
+        else
+            for (int v = threadIdx.x & 31; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
     }
 }
 
@@ -1025,7 +1508,9 @@ int launch_gemm(const Maps& m, const GemmParams& p, cudaStream_t st, const char*
     if (sms <= 0) return fail(MOE_ERR_CUDA, "%s: cannot query the SM count", who);
     const int grid = static_cast<int>(bound < sms ? bound : sms);
     if (grid <= 0) return MOE_OK;
-    kernel<<<grid, S::THREADS, S::SMEM, st>>>(m.x, m.w, m.r0, m.r1, m.r2, p);
+    GemmParams q = p;
+    q.pad_free = S::XROWS % p.block_size == 0;
+    kernel<<<grid, S::THREADS, S::SMEM, st>>>(m.x, m.w, m.r0, m.r1, m.r2, q);
     count_launch();
     return check_launch(who);
 }
@@ -1038,6 +1523,42 @@ int by_ntok(int ntok, const Maps& m, const GemmParams& p, cudaStream_t st, const
         case 32: return launch_gemm<MODE, WFMT, ACT, 32>(m, p, st, who);
         case 64: return launch_gemm<MODE, WFMT, ACT, 64>(m, p, st, who);
         default: return launch_gemm<MODE, WFMT, ACT, 128>(m, p, st, who);
+    }
+}
+
+template <int MODE, int WFMT, int ACT, int NTOK>
+int launch_ts(const Maps& m, const GemmParams& p, cudaStream_t st, const char* who) {
+    using S = TsShape<MODE, WFMT, ACT, NTOK>;
+    auto kernel = grouped_gemm_ts_kernel<MODE, WFMT, ACT, NTOK>;
+    static int configured_for = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_for != dev) {
+        int rc = set_smem_limit(reinterpret_cast<const void*>(kernel), S::SMEM);
+        if (rc != MOE_OK) return rc;
+        configured_for = dev;
+    }
+    const long bound = static_cast<long>((p.max_padded + NTOK - 1) / NTOK + p.E) *
+                       ((p.n_out + S::OUT_COLS - 1) / S::OUT_COLS);
+    const int sms = sm_count();
+    if (sms <= 0) return fail(MOE_ERR_CUDA, "%s: cannot query the SM count", who);
+    const int grid = static_cast<int>(bound < sms ? bound : sms);
+    if (grid <= 0) return MOE_OK;
+    GemmParams q = p;
+    q.pad_free = NTOK % p.block_size == 0;
+    kernel<<<grid, S::THREADS, S::SMEM, st>>>(m.x, m.r0, m.r1, m.r2, q);
+    count_launch();
+    return check_launch(who);
+}
+
+// quantised weights: the TS form, NTOK tokens per tile (128 for the prefill form)
+template <int MODE, int WFMT, int ACT>
+int ts_by_ntok(int ntok, const Maps& m, const GemmParams& p, cudaStream_t st, const char* who) {
+    switch (ntok) {
+        case 16: return launch_ts<MODE, WFMT, ACT, 16>(m, p, st, who);
+        case 32: return launch_ts<MODE, WFMT, ACT, 32>(m, p, st, who);
+        case 64: return launch_ts<MODE, WFMT, ACT, 64>(m, p, st, who);
+        default: return launch_ts<MODE, WFMT, ACT, 128>(m, p, st, who);
     }
 }
 
@@ -1076,7 +1597,9 @@ int launch_pair(const Maps& m, const GemmParams& p, cudaStream_t st, const char*
     const long pairs = bound < max_pairs ? bound : max_pairs;
     if (pairs <= 0) return MOE_OK;
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, m.x, m.w, p);
+    GemmParams q = p;
+    q.pad_free = 256 % p.block_size == 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, m.x, m.w, q);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
     count_launch();
     return check_launch(who);
@@ -1088,11 +1611,12 @@ int dispatch(int wfmt, int act, int ntok, const Maps& m, const GemmParams& p, cu
         if (ntok == 0) return launch_pair<MODE>(m, p, st, who);
         return by_ntok<MODE, MOE_W_BF16, MOE_ACT_BF16>(ntok, m, p, st, who);
     }
+    const int nt = ntok ? ntok : 128;
     if (wfmt == MOE_W_GPTQ_INT4)
-        return act == MOE_ACT_F16 ? by_ntok<MODE, MOE_W_GPTQ_INT4, MOE_ACT_F16>(ntok, m, p, st, who)
-                                  : by_ntok<MODE, MOE_W_GPTQ_INT4, MOE_ACT_BF16>(ntok, m, p, st, who);
-    return act == MOE_ACT_F16 ? by_ntok<MODE, MOE_W_NVFP4, MOE_ACT_F16>(ntok, m, p, st, who)
-                              : by_ntok<MODE, MOE_W_NVFP4, MOE_ACT_BF16>(ntok, m, p, st, who);
+        return act == MOE_ACT_F16 ? ts_by_ntok<MODE, MOE_W_GPTQ_INT4, MOE_ACT_F16>(nt, m, p, st, who)
+                                  : ts_by_ntok<MODE, MOE_W_GPTQ_INT4, MOE_ACT_BF16>(nt, m, p, st, who);
+    return act == MOE_ACT_F16 ? ts_by_ntok<MODE, MOE_W_NVFP4, MOE_ACT_F16>(nt, m, p, st, who)
+                              : ts_by_ntok<MODE, MOE_W_NVFP4, MOE_ACT_BF16>(nt, m, p, st, who);
 }
 
 // Checks the weight descriptor and encodes its tensor maps. N = weight rows
@@ -1186,6 +1710,7 @@ extern "C" int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* 
         if (blocks > cap) blocks = cap;
         moe::gather_rows_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(x), sorted_token_ids,
                                                         expert_offsets, E, T, top_k, H / 8, max_padded,
+                                                        w_gate_up->format == MOE_W_GPTQ_INT4 ? 1 : 0,
                                                         static_cast<uint4*>(workspace), err_word);
         moe::count_launch();
         rc = moe::check_launch("moe_grouped_gate_up (gather)");
@@ -1207,6 +1732,7 @@ extern "C" int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* 
     p.scale2 = w_gate_up->scale2;
     p.group_size = w_gate_up->group_size;
     p.err = err_word;
+    p.block_size = block_size;
     return moe::dispatch<moe::MODE_GATE_UP>(w_gate_up->format, act, ntok, m, p, st, who);
 }
 
@@ -1244,5 +1770,6 @@ extern "C" int moe_grouped_down(const void* h, int32_t act, const MoeWeight* w_d
     p.scale2 = w_down->scale2;
     p.group_size = w_down->group_size;
     p.err = err_word;
+    p.block_size = block_size;
     return moe::dispatch<moe::MODE_DOWN>(w_down->format, act, ntok, m, p, static_cast<cudaStream_t>(stream), who);
 }

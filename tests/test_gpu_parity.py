@@ -143,6 +143,12 @@ LAYER_CASES = {
                                      wfmt="gptq", router="normal", group_size=64),
     "nvfp4_f16_act": synth.MoeConfig("nvfp4_f16_act", T=40, H=256, I=192, E=8, k=2, bs=16, act="f16",
                                      wfmt="nvfp4", router="normal"),
+    # a block size that does not divide the tile height: tiles may start on padding rows
+    # (decode form with 64-token tiles, CTA-pair prefill form, GPTQ with 128-token tiles)
+    "block48_decode": synth.MoeConfig("block48_decode", T=200, H=256, I=128, E=8, k=2, bs=48, router="normal"),
+    "block48_prefill": synth.MoeConfig("block48_prefill", T=500, H=256, I=256, E=4, k=2, bs=48, router="normal"),
+    "block48_gptq": synth.MoeConfig("block48_gptq", T=300, H=256, I=256, E=4, k=2, bs=48, act="f16",
+                                    wfmt="gptq", router="normal"),
 }
 
 
