@@ -10,32 +10,26 @@
 // in the activation type).
 //
 // Design (sm_103a):
-//   * One persistent CTA per SM walks a static tile list built on the device
-//     from expert_offsets, so nothing on the host depends on the routing and
-//     the launch shape only depends on host-known sizes. Tiles whose first row
-//     is a padding row hold padding only (valid rows are a prefix of each
-//     span) and are skipped by every role of the CTA alike.
-//   * A tile is 256 weight rows (gate/up: 128 gate + 128 up rows of the same
-//     output columns, so the epilogue can fuse silu*up; down: 256 output
-//     columns) against a block of activation rows, K in steps of 64 elements
-//     (one 128-byte swizzle span):
-//       - prefill form: 128 activation rows are the MMA's M operand and the
-//         256 weight rows its N operand (tcgen05.mma M=128, N=256, K=16); with
-//         quantised weights a tile holds 256 rows as two M=128 halves that
-//         share the dequantised weight tile (a span's last tile of at most 128
-//         rows runs one half only);
-//       - decode form (few rows per expert): the operands swap; each half of
-//         the weight tile is an M=128 operand and the NTOK activation rows
-//         (16..128) the N operand, so a small batch does not pay for 128 rows.
-//   * Warp 0 issues TMA loads into a multi-stage ring; one thread of warp 1
-//     issues tcgen05.mma into one of two TMEM accumulators while warps 2-5
-//     drain the other (tcgen05.ld -> activation -> global); 256-row tiles use
-//     one accumulator of 512 columns.
-//   * Quantised weights (GPTQ int4, NVFP4): warp 14 streams the raw bytes by
-//     TMA into a 6-deep ring of their own; warps 6-13 (two per SM
-//     sub-partition, since dequantisation is latency-bound) dequantise shared
-//     -> shared into the swizzled 16-bit weight tile the MMA reads. The NVFP4
-//     global scale2 is applied to the f32 accumulator.
+//   * Persistent CTAs walk a static tile list built on the device from
+//     expert_offsets, so nothing on the host depends on the routing and the
+//     launch shape only depends on host-known sizes. A tile is 256 weight rows
+//     (gate/up: 128 gate + 128 up rows of the same output columns, so the
+//     epilogue fuses silu(gate) * up; down: 256 output columns) against a
+//     block of activation rows, K in steps of 64 elements.
+//   * Three kernels, chosen on the host from the average rows per touched
+//     expert and the weight format:
+//       - bf16 prefill (>= 128 rows per expert): grouped_gemm_pair_kernel, a
+//         cluster of two CTAs issuing tcgen05.mma.cta_group::2 M=256 (128
+//         activation rows per CTA) x N=256 (half the weight tile per CTA);
+//       - bf16 decode: grouped_gemm_decode_kernel, operands swapped: each
+//         weight half is an M=128 operand and NTOK tokens (16..128, one align
+//         block) the N operand;
+//       - GPTQ / NVFP4, any size: grouped_gemm_ts_kernel, weights dequantised
+//         by eight warps into TMEM and used as the M=128 A operand, NTOK tokens
+//         (128 for prefill) the N operand from shared memory.
+//   * Roles: TMA producer warps feed multi-stage rings; MMA issues go to
+//     double-buffered TMEM accumulators where TMEM allows; four epilogue warps
+//     drain them (tcgen05.ld -> activation -> global).
 //   * Every mbarrier wait is bounded; on a timeout the CTA records
 //     MOE_DEV_ERR_TIMEOUT, lets in-flight copies and MMAs land, frees TMEM and
 //     returns.
@@ -102,39 +96,26 @@ __host__ __device__ constexpr int pow2_at_least(int v) {
     return p;
 }
 
-// Compile-time shape of one kernel instantiation. NTOK == 0: prefill form;
-// NTOK > 0: decode form with NTOK activation rows per tile.
-template <int MODE, int WFMT, int ACT, int NTOK>
-struct Shape {
-    static constexpr bool SWAP = NTOK > 0;
-    static constexpr bool QUANT = WFMT != MOE_W_BF16;
-    // prefill form, quantised weights: 256 activation rows as two M=128 halves
-    // sharing the dequantised weight tile (half the dequantisation per FLOP);
-    // prefill form, bf16 weights: 128 rows; decode form: NTOK rows
-    static constexpr bool PAIR = !SWAP && QUANT;
-    static constexpr int XROWS = SWAP ? NTOK : (PAIR ? 256 : 128);
-    static constexpr int X_STAGE = XROWS * BK * 2;
-    static constexpr int AVAIL = SMEM_LIMIT - 1024 - TAIL_BYTES;
-    // bf16 weights: as many TMA stages as fit. Quantised weights: the 16-bit
-    // stages are refilled on chip, so few suffice, and the rest of shared
-    // memory holds raw stages (more raw bytes in flight from HBM).
-    static constexpr int STAGES_FIT = AVAIL / (X_STAGE + W_STAGE);
-    static constexpr int STAGES = QUANT ? (SWAP ? 3 : 2) : (STAGES_FIT < MAX_STAGES ? STAGES_FIT : MAX_STAGES);
-    static constexpr int RAW_FIT = (AVAIL - STAGES * (X_STAGE + W_STAGE)) / RAW_STAGE;
-    static constexpr int RSTAGES = QUANT ? (RAW_FIT < MAX_RSTAGES ? RAW_FIT : MAX_RSTAGES) : 0;
-    // TMEM: two accumulator buffers (the epilogue drains one while the MMA
-    // fills the other), except for 256-row tiles, whose one accumulator of two
-    // 128-row halves x 256 columns takes all 512 columns
-    static constexpr int NBUF = PAIR ? 1 : 2;
-    static constexpr int NACC = SWAP ? swapped_nacc(NTOK) : 1;  // split accumulators per half
-    static constexpr int ACC = SWAP ? 2 * NTOK * NACC : (PAIR ? 512 : 256);  // TMEM columns per buffer
-    static constexpr int TMEM_COLS = pow2_at_least(NBUF * ACC);
+// Compile-time shape of the bf16 decode form: NTOK activation rows (tokens)
+// per tile are the MMA's N operand, the 256 weight rows of the tile two M=128
+// A operands (gate | up halves, or two 128-column halves of the output).
+template <int MODE, int NTOK>
+struct DecodeShape {
+    static constexpr int X_STAGE = NTOK * BK * 2;
     static constexpr int OUT_COLS = MODE == MODE_GATE_UP ? 128 : 256;  // output columns per tile
-    static constexpr int THREADS = 192 + (QUANT ? 32 * (NUM_DQ_WARPS + 1) : 0);
-    static constexpr int SMEM = 1024 + STAGES * (X_STAGE + W_STAGE) + RSTAGES * RAW_STAGE + TAIL_BYTES;
-    static constexpr int RAW_BYTES = WFMT == MOE_W_GPTQ_INT4 ? 8832 : 9216;
+    // epilogue staging: per epilogue warp 2 halves x 16 tokens x 32 columns
+    static constexpr int STG_BYTES = NUM_EPI_WARPS * 2 * 16 * 32 * 2;
+    static constexpr int AVAIL = SMEM_LIMIT - 1024 - TAIL_BYTES - STG_BYTES;
+    static constexpr int STAGES_FIT = AVAIL / (X_STAGE + W_STAGE);
+    static constexpr int STAGES = STAGES_FIT < MAX_STAGES ? STAGES_FIT : MAX_STAGES;
+    // two accumulator buffers (the epilogue drains one while the MMA fills the
+    // other), each two halves x NACC split accumulators x NTOK columns
+    static constexpr int NACC = swapped_nacc(NTOK);
+    static constexpr int ACC = 2 * NTOK * NACC;
+    static constexpr int TMEM_COLS = pow2_at_least(2 * ACC);
+    static constexpr int THREADS = 32 * (2 + NUM_EPI_WARPS);
+    static constexpr int SMEM = 1024 + STAGES * (X_STAGE + W_STAGE) + STG_BYTES + TAIL_BYTES;
     static_assert(STAGES >= 2, "not enough shared memory for two stages");
-    static_assert(!QUANT || RSTAGES >= 4, "not enough shared memory for the raw ring");
     static_assert(TMEM_COLS <= 512, "accumulators exceed TMEM");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory over the limit");
 };
@@ -171,13 +152,7 @@ __device__ __forceinline__ bool tile_is_padding(const GemmParams& p, const TileI
     return !p.pad_free && __ldg(p.sorted_ids + t.m0) == p.P;
 }
 
-// weight-tile row n (0..255) -> output column it feeds, and whether that column exists
-template <int MODE>
-__device__ __forceinline__ int out_col(int n, int n0) {
-    return MODE == MODE_GATE_UP ? n0 + (n & 127) : n0 + n;
-}
-
-// global weight row (or column, for GPTQ's [K/8, N] layout) of each half of a tile
+// first global weight row of each 128-row half of a tile (expert offset added by the caller)
 template <int MODE>
 __device__ __forceinline__ void half_bases(const GemmParams& p, int n0, int& c0, int& c1) {
     c0 = n0;
@@ -230,7 +205,7 @@ __device__ __forceinline__ int build_tile_list(SmemTail& s, const GemmParams& p,
     return bad;
 }
 
-// ---- dequantisation: raw shared bytes -> swizzled 16-bit weight tile -------------
+// ---- number conversions for the quantised formats ---------------------------------
 
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
     uint32_t r;
@@ -266,120 +241,6 @@ __device__ __forceinline__ void e2m1x4_to_bf16x4(uint32_t w, uint32_t& p01, uint
     const uint32_t t = w << 4;  // byte 0 / 1 of t carry the signs of codes 0 / 2 in their top bit
     p01 = prmt(lo, hi, 0x5140u) | (prmt(t, w, 0xC888u) & 0x80008000u);
     p23 = prmt(lo, hi, 0x7362u) | (prmt(t, w, 0xD999u) & 0x80008000u);
-}
-
-template <int ACT>
-__device__ __forceinline__ uint32_t f16x2_to_act2(uint32_t h2) {
-    if (ACT == MOE_ACT_F16) return h2;
-    const float2 f = __half22float2(*reinterpret_cast<__half2*>(&h2));
-    return Act<MOE_ACT_BF16>::pack2(f.x, f.y);
-}
-
-// 8 GPTQ codes of one word -> 8 weights (q - z) * s in the activation type, k order
-template <int ACT>
-__device__ __forceinline__ uint4 gptq_word(uint32_t w, int z, float s, __half2 ss) {
-    uint4 v;
-    if (ACT == MOE_ACT_F16) {
-        // fp16 1024 + q from the code bits (exact), minus 1024 + z (exact), times s
-        // (one rounding): pairs (q0,q4), (q1,q5), (q2,q6), (q3,q7) first
-        const uint32_t m = 0x64006400u;
-        const uint32_t p0 = (w & 0x000F000Fu) | m;
-        const uint32_t p1 = ((w >> 4) & 0x000F000Fu) | m;
-        const uint32_t p2 = ((w >> 8) & 0x000F000Fu) | m;
-        const uint32_t p3 = ((w >> 12) & 0x000F000Fu) | m;
-        const __half2 zz = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400 | z)));
-        uint32_t r[4] = {p0, p1, p2, p3};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            __half2 h = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&r[i]), zz), ss);
-            r[i] = *reinterpret_cast<uint32_t*>(&h);
-        }
-        v.x = prmt(r[0], r[1], 0x5410);  // (q0, q1)
-        v.y = prmt(r[2], r[3], 0x5410);  // (q2, q3)
-        v.z = prmt(r[0], r[1], 0x7632);  // (q4, q5)
-        v.w = prmt(r[2], r[3], 0x7632);  // (q6, q7)
-    } else {
-        float f[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = static_cast<float>(static_cast<int>((w >> (4 * j)) & 15u) - z) * s;
-        v.x = Act<ACT>::pack2(f[0], f[1]);
-        v.y = Act<ACT>::pack2(f[2], f[3]);
-        v.z = Act<ACT>::pack2(f[4], f[5]);
-        v.w = Act<ACT>::pack2(f[6], f[7]);
-    }
-    return v;
-}
-
-template <int MODE, int WFMT, int ACT>
-__device__ __forceinline__ void dequant_stage(uint8_t* wstage, const uint8_t* raw, const GemmParams& p,
-                                              const TileInfo& t, int dq_tid) {
-    constexpr int DQ_THREADS = NUM_DQ_WARPS * 32;  // 256
-    if (WFMT == MOE_W_GPTQ_INT4) {
-        // raw: qweight [2 halves][8 packed k-rows][128 cols] int32, scales [2][128] fp16,
-        // zeros [2][16] int32. Thread = (half h, column c): the 8 words of its column.
-        const int h = dq_tid >> 7, c = dq_tid & 127;
-        const int n = h * 128 + c;
-        const bool valid = out_col<MODE>(n, t.n0) < p.n_out;
-        const uint32_t* qw = reinterpret_cast<const uint32_t*>(raw + h * 4096);
-        const __half sh = reinterpret_cast<const __half*>(raw + 8192 + h * 256)[c];
-        const float s = __half2float(sh);
-        const __half2 ss = __half2half2(sh);
-        const uint32_t zw = reinterpret_cast<const uint32_t*>(raw + 8704 + h * 128)[c >> 3];
-        const int z = (zw >> (4 * (c & 7))) & 15;
-        uint32_t words[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) words[i] = qw[i * 128 + c];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (valid) v = gptq_word<ACT>(words[i], z, s, ss);
-            *reinterpret_cast<uint4*>(wstage + n * 128 + ((i ^ (n & 7)) << 4)) = v;
-        }
-    } else {
-        // raw: packed [2 halves][128 rows][32 bytes], scales [2][4 k16-groups][128 rows] E4M3.
-        // Item = (half, row r, 8-element chunk cc); 8 consecutive threads read one row.
-        constexpr int ITEMS = (W_ROWS * 8) / DQ_THREADS;  // 8
-        uint32_t bytes[ITEMS];
-        uint32_t sbyte[ITEMS];
-#pragma unroll
-        for (int it = 0; it < ITEMS; ++it) {
-            const int idx = it * DQ_THREADS + dq_tid;
-            const int h = idx >> 10, r = (idx >> 3) & 127, cc = idx & 7;
-            bytes[it] = reinterpret_cast<const uint32_t*>(raw + h * 4096 + r * 32)[cc];
-            sbyte[it] = raw[8192 + h * 512 + (cc >> 1) * 128 + r];
-        }
-#pragma unroll
-        for (int it = 0; it < ITEMS; ++it) {
-            const int idx = it * DQ_THREADS + dq_tid;
-            const int h = idx >> 10, r = (idx >> 3) & 127, cc = idx & 7;
-            const int n = h * 128 + r;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (out_col<MODE>(n, t.n0) < p.n_out) {
-                uint32_t o[4];
-                if (ACT == MOE_ACT_BF16) {
-                    // products of an E2M1 and an E4M3 value are exact in bf16
-                    const __nv_bfloat162 s2 = __float2bfloat162_rn(e4m3_to_f32(sbyte[it]));
-                    e2m1x4_to_bf16x4(bytes[it], o[0], o[1]);
-                    e2m1x4_to_bf16x4(bytes[it] >> 16, o[2], o[3]);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        __nv_bfloat162 prod = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&o[j]), s2);
-                        o[j] = *reinterpret_cast<uint32_t*>(&prod);
-                    }
-                } else {
-                    const __half2 s2 = __float2half2_rn(e4m3_to_f32(sbyte[it]));  // exact: E4M3 values are fp16 values
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t e2 = e2m1x2_to_f16x2((bytes[it] >> (8 * j)) & 0xffu);
-                        __half2 prod = __hmul2(*reinterpret_cast<__half2*>(&e2), s2);  // exact in fp16
-                        o[j] = *reinterpret_cast<uint32_t*>(&prod);
-                    }
-                }
-                v = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-            *reinterpret_cast<uint4*>(wstage + n * 128 + ((cc ^ (n & 7)) << 4)) = v;
-        }
-    }
 }
 
 // ---- epilogue helpers ----------------------------------------------------------
@@ -456,21 +317,21 @@ __device__ __forceinline__ void load_swapped(uint32_t taddr, int c, float (&fa)[
     }
 }
 
-// ---- the kernel ------------------------------------------------------------------
+// ---- bf16 decode form -------------------------------------------------------------
 
-template <int MODE, int WFMT, int ACT, int NTOK>
-__global__ void __launch_bounds__(Shape<MODE, WFMT, ACT, NTOK>::THREADS, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                    const __grid_constant__ CUtensorMap tmR0, const __grid_constant__ CUtensorMap tmR1,
-                    const __grid_constant__ CUtensorMap tmR2, const GemmParams p) {
-    using S = Shape<MODE, WFMT, ACT, NTOK>;
-    constexpr int XROWS = S::XROWS, STAGES = S::STAGES, RSTAGES = S::RSTAGES;
+template <int MODE, int NTOK>
+__global__ void __launch_bounds__(DecodeShape<MODE, NTOK>::THREADS, 1)
+grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                           const GemmParams p) {
+    using S = DecodeShape<MODE, NTOK>;
+    constexpr int ACT = MOE_ACT_BF16;
+    constexpr int XROWS = NTOK, STAGES = S::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024_shared(smem_raw);
     uint8_t* sX = smem;
     uint8_t* sW = smem + STAGES * S::X_STAGE;
-    uint8_t* sR = sW + STAGES * W_STAGE;
-    SmemTail& s = *reinterpret_cast<SmemTail*>(sR + RSTAGES * RAW_STAGE);
+    uint8_t* sStg = sW + STAGES * W_STAGE;
+    SmemTail& s = *reinterpret_cast<SmemTail*>(sStg + S::STG_BYTES);
     volatile int* abort_flag = &s.abort_flag;
 
     const int tid = threadIdx.x;
@@ -482,13 +343,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         if (bad) set_err(p.err, MOE_DEV_ERR_OFFSETS);
 #pragma unroll
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(&s.full[i], 1 + (S::QUANT ? NUM_DQ_WARPS : 0));
+            mbar_init(&s.full[i], 1);
             mbar_init(&s.empty[i], 1);
-        }
-#pragma unroll
-        for (int i = 0; i < RSTAGES; ++i) {
-            mbar_init(&s.raw_full[i], 1);
-            mbar_init(&s.raw_empty[i], NUM_DQ_WARPS);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.tfull[i], 1);
@@ -507,7 +363,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmX);
-        if (!S::QUANT) tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmW);
     }
     tc_fence_before();
     __syncthreads();
@@ -517,7 +373,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer: activations (+ bf16 weights) ----------------
+            // ---------------- TMA producer: activations and weights ----------------
             uint32_t stage = 0, phase = 0;
             long issued = 0;
             bool ok = true;
@@ -526,20 +382,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 if (tile_is_padding(p, t)) continue;
                 int c0, c1;
                 half_bases<MODE>(p, t.n0, c0, c1);
-                // prefill tiles of at most 128 rows load and multiply one half only
-                const bool two = S::PAIR && t.rows > 128;
-                const uint32_t xbytes = S::PAIR ? (two ? 2 : 1) * 128 * BK * 2 : S::X_STAGE;
-                const uint32_t tx = xbytes + (S::QUANT ? 0u : static_cast<uint32_t>(W_STAGE));
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&s.full[stage], tx);
+                    mbar_arrive_expect_tx(&s.full[stage], S::X_STAGE + W_STAGE);
                     tma_load_2d(sX + stage * S::X_STAGE, &tmX, kb * BK, t.m0, &s.full[stage]);
-                    if (two) tma_load_2d(sX + stage * S::X_STAGE + 128 * BK * 2, &tmX, kb * BK, t.m0 + 128, &s.full[stage]);
-                    if (!S::QUANT) {
-                        uint8_t* w = sW + stage * W_STAGE;
-                        tma_load_2d(w, &tmW, kb * BK, t.e * p.n_w + c0, &s.full[stage]);
-                        tma_load_2d(w + W_STAGE / 2, &tmW, kb * BK, t.e * p.n_w + c1, &s.full[stage]);
-                    }
+                    uint8_t* w = sW + stage * W_STAGE;
+                    tma_load_2d(w, &tmW, kb * BK, t.e * p.n_w + c0, &s.full[stage]);
+                    tma_load_2d(w + W_STAGE / 2, &tmW, kb * BK, t.e * p.n_w + c1, &s.full[stage]);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -551,18 +400,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // ---------------- MMA issuer ----------------
-            constexpr uint32_t idesc = S::SWAP ? f16_idesc(ACT, 128, NTOK) : f16_idesc(ACT, 128, 256);
+            // ---------------- MMA issuer: A = weight halves, B = tokens ----------------
+            constexpr uint32_t idesc = f16_idesc(ACT, 128, NTOK);
             uint32_t stage = 0, phase = 0;
             int local = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
                 const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
                 if (tile_is_padding(p, t)) continue;
-                const int acc = S::NBUF == 2 ? (local & 1) : 0;
-                const uint32_t aph = S::NBUF == 2 ? ((local >> 1) & 1) : (local & 1);
+                const int acc = local & 1;
+                const uint32_t aph = (local >> 1) & 1;
                 ++local;
-                const bool two = S::PAIR && t.rows > 128;
                 if (!mbar_wait(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * S::ACC;
@@ -571,22 +419,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     tc_fence_after();
                     const uint64_t xd = sw128_desc(smem_u32(sX + stage * S::X_STAGE));
                     const uint64_t wd = sw128_desc(smem_u32(sW + stage * W_STAGE));
-                    if (S::SWAP) {
-                        const uint64_t wd1 = sw128_desc(smem_u32(sW + stage * W_STAGE + W_STAGE / 2));
+                    const uint64_t wd1 = sw128_desc(smem_u32(sW + stage * W_STAGE + W_STAGE / 2));
 #pragma unroll
-                        for (int k = 0; k < BK / 16; ++k) {
-                            const int a = k % S::NACC;
-                            const uint32_t en = kb > 0 || k >= S::NACC;
-                            tc_mma(d + a * NTOK, wd + 2 * k, xd + 2 * k, idesc, en);
-                            tc_mma(d + (S::NACC + a) * NTOK, wd1 + 2 * k, xd + 2 * k, idesc, en);
-                        }
-                    } else {
-                        const uint64_t xd1 = sw128_desc(smem_u32(sX + stage * S::X_STAGE + 128 * BK * 2));
-#pragma unroll
-                        for (int k = 0; k < BK / 16; ++k) {
-                            tc_mma(d, xd + 2 * k, wd + 2 * k, idesc, (kb | k) != 0);
-                            if (two) tc_mma(d + 256, xd1 + 2 * k, wd + 2 * k, idesc, (kb | k) != 0);
-                        }
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const int a = k % S::NACC;
+                        const uint32_t en = kb > 0 || k >= S::NACC;
+                        tc_mma(d + a * NTOK, wd + 2 * k, xd + 2 * k, idesc, en);
+                        tc_mma(d + (S::NACC + a) * NTOK, wd1 + 2 * k, xd + 2 * k, idesc, en);
                     }
                     tc_commit(&s.empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -598,176 +437,55 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             mbar_drain(&s.mma_done, 0, kWaitLimitNs / 8);
         }
         __syncwarp();
-    } else if (warp < 2 + NUM_EPI_WARPS) {
-        // ---------------- epilogue ----------------
+    } else {
+        // ---------------- epilogue: lane = weight row of a half, columns = tokens ----------------
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int lrow = q * 32 + lane;
+        using T = typename Act<ACT>::T;
+        T* out = static_cast<T*>(p.out);
+        T* stg = reinterpret_cast<T*>(sStg) + (warp - 2) * (2 * 16 * 32);
+        constexpr int HALVES = MODE == MODE_GATE_UP ? 1 : 2;
         int local = 0;
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
             const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
             if (tile_is_padding(p, t)) continue;
-            const int acc = S::NBUF == 2 ? (local & 1) : 0;
-            const uint32_t aph = S::NBUF == 2 ? ((local >> 1) & 1) : (local & 1);
+            const int acc = local & 1;
+            const uint32_t aph = (local >> 1) & 1;
             ++local;
-            // tile metadata first: its loads overlap the wait for the accumulator
-            const int nvalid = valid_rows(p, s, t, lane);
-            float s2a = 1.0f, s2b = 1.0f;
-            if (WFMT == MOE_W_NVFP4) {
-                s2a = __ldg(p.scale2 + t.e);
-                s2b = (MODE == MODE_GATE_UP) ? __ldg(p.scale2 + p.E + t.e) : s2a;
-            }
+            const int nvalid = valid_rows(p, s, t, lane);  // its loads overlap the wait
             if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * S::ACC;
-            if (!S::SWAP) {
-                // lane = activation row of each 128-row half; columns = weight rows
-                // (gate | up, or 256 outputs)
-                for (int hh = 0; hh < (S::PAIR ? 2 : 1) && hh * 128 < t.rows; ++hh) {
-                    const int row = hh * 128 + lrow;
-                    const bool row_ok = row < nvalid;
-                    const size_t orow = static_cast<size_t>(t.m0 + row) * p.n_out;
-                    const uint32_t ta = taddr + hh * 256;
+            const int colw = t.n0 + q * 32;  // this warp's first column (half 0)
+#pragma unroll 1
+            for (int c = 0; c < NTOK && c < nvalid; c += 16) {
+                float a[16], b[16];
+                load_swapped<NTOK, S::NACC>(taddr, c, a, b);
+                // through this warp's staging area ([half][token][32 columns]),
+                // so that the chunk leaves as 16-byte stores of 8 columns
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
                     if (MODE == MODE_GATE_UP) {
-#pragma unroll 1
-                        for (int c = 0; c < 128; c += 32) {
-                            uint32_t g[32], u[32];
-                            tmem_ld32(ta + c, g);
-                            tmem_ld32(ta + 128 + c, u);
-                            tmem_ld_wait();
-                            if (row_ok) {
-#pragma unroll
-                                for (int j = 0; j < 32; j += 8) {
-                                    const int col = t.n0 + c + j;
-                                    if (col < p.n_out) {
-                                        float f[8];
-#pragma unroll
-                                        for (int i = 0; i < 8; ++i)
-                                            f[i] = silu_mul(__uint_as_float(g[j + i]) * s2a,
-                                                            __uint_as_float(u[j + i]) * s2b);
-                                        store8<ACT>(p.out, orow + col, f);
-                                    }
-                                }
-                            }
-                        }
+                        stg[j * 32 + lane] = Act<ACT>::from_f(silu_mul(a[j], b[j]));
                     } else {
-#pragma unroll 1
-                        for (int c = 0; c < 256; c += 32) {
-                            uint32_t g[32];
-                            tmem_ld32(ta + c, g);
-                            tmem_ld_wait();
-                            if (row_ok) {
-#pragma unroll
-                                for (int j = 0; j < 32; j += 8) {
-                                    const int col = t.n0 + c + j;
-                                    if (col < p.n_out) {
-                                        float f[8];
-#pragma unroll
-                                        for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(g[j + i]) * s2a;
-                                        store8<ACT>(p.out, orow + col, f);
-                                    }
-                                }
-                            }
-                        }
+                        stg[j * 32 + lane] = Act<ACT>::from_f(a[j]);
+                        stg[512 + j * 32 + lane] = Act<ACT>::from_f(b[j]);
                     }
                 }
-            } else {
-                // lane = weight row of each half; columns = activation rows (tokens)
-                using T = typename Act<ACT>::T;
-                T* out = static_cast<T*>(p.out);
-                const int col_a = t.n0 + lrow;                                    // gate / low half
-                const int col_b = (MODE == MODE_GATE_UP) ? col_a : t.n0 + 128 + lrow;  // up / high half
-#pragma unroll 1
-                for (int c = 0; c < NTOK && c < nvalid; c += 16) {
-                    float a[16], b[16];
-                    load_swapped<(NTOK > 0 ? NTOK : 16), S::NACC>(taddr, c, a, b);
+                __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int r = c + j;
-                        if (r < nvalid) {
-                            const size_t orow = static_cast<size_t>(t.m0 + r) * p.n_out;
-                            if (MODE == MODE_GATE_UP) {
-                                if (col_a < p.n_out)
-                                    out[orow + col_a] = Act<ACT>::from_f(silu_mul(a[j] * s2a, b[j] * s2b));
-                            } else {
-                                if (col_a < p.n_out) out[orow + col_a] = Act<ACT>::from_f(a[j] * s2a);
-                                if (col_b < p.n_out) out[orow + col_b] = Act<ACT>::from_f(b[j] * s2a);
-                            }
-                        }
-                    }
+                for (int i = 0; i < 2 * HALVES; ++i) {
+                    const int pc = i * 32 + lane;  // [half][16 tokens][4 pieces of 8 columns]
+                    const int hh = pc >> 6, row = (pc >> 2) & 15, pq = pc & 3;
+                    const int col = colw + hh * 128 + pq * 8;
+                    if (c + row < nvalid && col < p.n_out)
+                        *reinterpret_cast<uint4*>(out + static_cast<size_t>(t.m0 + c + row) * p.n_out + col) =
+                            *reinterpret_cast<const uint4*>(stg + hh * 512 + row * 32 + pq * 8);
                 }
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.tempty[acc]);
-        }
-    } else if (warp < 2 + NUM_EPI_WARPS + NUM_DQ_WARPS) {
-        // ---------------- dequantising warps (quantised weights only) ----------------
-        if constexpr (S::QUANT) {
-            const int dq_tid = tid - 32 * (2 + NUM_EPI_WARPS);
-            uint32_t stage = 0, phase = 0, rstage = 0, rphase = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
-                if (tile_is_padding(p, t)) continue;
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&s.raw_full[rstage], rphase, abort_flag, p.err) ||
-                        !mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    dequant_stage<MODE, WFMT, ACT>(sW + stage * W_STAGE, sR + rstage * RAW_STAGE, p, t, dq_tid);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(&s.full[stage]);
-                        mbar_arrive(&s.raw_empty[rstage]);
-                    }
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
-                    if (++rstage == RSTAGES) { rstage = 0; rphase ^= 1; }
-                }
-            }
-        }
-    } else {
-        // ---------------- raw quantised-weight producer (last warp) ----------------
-        if constexpr (S::QUANT) {
-          if (lane == 0) {
-            uint32_t rstage = 0, rphase = 0;
-            long issued = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
-                if (tile_is_padding(p, t)) continue;
-                int c0, c1;
-                half_bases<MODE>(p, t.n0, c0, c1);
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&s.raw_empty[rstage], rphase ^ 1, abort_flag, p.err)) { ok = false; break; }
-                    uint64_t* bar = &s.raw_full[rstage];
-                    uint8_t* r = sR + rstage * RAW_STAGE;
-                    mbar_arrive_expect_tx(bar, S::RAW_BYTES);
-                    if (WFMT == MOE_W_GPTQ_INT4) {
-                        const int kq = t.e * (p.K / 8) + kb * 8;
-                        const int g = t.e * (p.K / p.group_size) + (kb * BK) / p.group_size;
-                        tma_load_2d(r, &tmR0, c0, kq, bar);
-                        tma_load_2d(r + 4096, &tmR0, c1, kq, bar);
-                        tma_load_2d(r + 8192, &tmR1, c0, g, bar);
-                        tma_load_2d(r + 8448, &tmR1, c1, g, bar);
-                        tma_load_2d(r + 8704, &tmR2, c0 / 8, g, bar);
-                        tma_load_2d(r + 8832, &tmR2, c1 / 8, g, bar);
-                    } else {
-                        tma_load_2d(r, &tmR0, kb * (BK / 2), t.e * p.n_w + c0, bar);
-                        tma_load_2d(r + 4096, &tmR0, kb * (BK / 2), t.e * p.n_w + c1, bar);
-                        const int sg = t.e * (p.K / 16) + kb * (BK / 16);
-                        tma_load_2d(r + 8192, &tmR1, c0, sg, bar);
-                        tma_load_2d(r + 8704, &tmR1, c1, sg, bar);
-                    }
-                    ++issued;
-                    if (++rstage == RSTAGES) { rstage = 0; rphase ^= 1; }
-                }
-            }
-            const long first = issued > RSTAGES ? issued - RSTAGES : 0;
-            for (long j = first; j < issued; ++j)
-                mbar_drain(&s.raw_full[j % RSTAGES], static_cast<uint32_t>((j / RSTAGES) & 1), kWaitLimitNs / 8);
-          }
         }
     }
 
@@ -1014,7 +732,9 @@ struct TsShape {
     static constexpr int DQ0 = EPI0 + NUM_EPI_WARPS;    // first dequantising warp
     static constexpr int RAWW = DQ0 + NUM_DQ_WARPS;     // raw producer warp
     static constexpr int THREADS = 32 * (RAWW + 1);
-    static constexpr int AVAIL = SMEM_LIMIT - 1024 - TAIL_BYTES;
+    // epilogue staging: per epilogue warp 2 halves x 16 tokens x 32 columns
+    static constexpr int STG_BYTES = NUM_EPI_WARPS * 2 * 16 * 32 * 2;
+    static constexpr int AVAIL = SMEM_LIMIT - 1024 - TAIL_BYTES - STG_BYTES;
     // The activation ring is its own, deeper than the TMEM weight ring: its
     // loads queue behind the raw weight stream, so they need as much time in
     // flight as the raw bytes do. At least 8 raw stages are kept.
@@ -1022,7 +742,7 @@ struct TsShape {
     static constexpr int XSTAGES = X_FIT < 12 ? X_FIT : 12;
     static constexpr int RAW_FIT = (AVAIL - XSTAGES * X_STAGE) / RAW_STAGE;
     static constexpr int RSTAGES = RAW_FIT < MAX_RSTAGES ? RAW_FIT : MAX_RSTAGES;
-    static constexpr int SMEM = 1024 + XSTAGES * X_STAGE + RSTAGES * RAW_STAGE + TAIL_BYTES;
+    static constexpr int SMEM = 1024 + XSTAGES * X_STAGE + RSTAGES * RAW_STAGE + STG_BYTES + TAIL_BYTES;
     static constexpr int RAW_BYTES = WFMT == MOE_W_GPTQ_INT4 ? 8832 : 9216;
     // GPTQ gate/up writes each group of 8 k values in the order 0,4,1,5,2,6,3,7
     // (the order the int4 -> fp16 conversion produces them in); the gather
@@ -1154,20 +874,20 @@ struct RawRow {
 template <int WFMT>
 __device__ __forceinline__ void load_raw_row(const uint8_t* raw, int h, int r, RawRow& x) {
     if (WFMT == MOE_W_GPTQ_INT4) {
-        // qweight [2 halves][8 packed k rows][128 cols] int32, scales [2][128] fp16, zeros [2][16] int32
-        const uint32_t* qw = reinterpret_cast<const uint32_t*>(raw + h * 4096);
+        // qweight [8 packed k rows][2 halves][128 cols] int32, scales [2][128] fp16, zeros [2][16] int32
+        const uint32_t* qw = reinterpret_cast<const uint32_t*>(raw);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) x.w[i] = qw[i * 128 + r];
+        for (int i = 0; i < 8; ++i) x.w[i] = qw[(i * 2 + h) * 128 + r];
         x.s = reinterpret_cast<const unsigned short*>(raw + 8192 + h * 256)[r];
-        x.z = reinterpret_cast<const uint32_t*>(raw + 8704 + h * 128)[r >> 3];
+        x.z = reinterpret_cast<const uint32_t*>(raw + 8704 + h * 64)[r >> 3];
     } else {
-        // packed [2 halves][128 rows][32 bytes], scales [2][4 k16 groups][128 rows] E4M3
+        // packed [2 halves][128 rows][32 bytes], scales [4 k16 groups][2 halves][128 rows] E4M3
         const uint4* row = reinterpret_cast<const uint4*>(raw + h * 4096 + r * 32);
         const uint4 v0 = row[0], v1 = row[1];
         x.w[0] = v0.x; x.w[1] = v0.y; x.w[2] = v0.z; x.w[3] = v0.w;
         x.w[4] = v1.x; x.w[5] = v1.y; x.w[6] = v1.z; x.w[7] = v1.w;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) x.sc[g] = raw[8192 + h * 512 + g * 128 + r];
+        for (int g = 0; g < 4; ++g) x.sc[g] = raw[8192 + g * 256 + h * 128 + r];
     }
 }
 
@@ -1182,7 +902,8 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
     uint8_t* smem = align1024_shared(smem_raw);
     uint8_t* sX = smem;
     uint8_t* sR = sX + XSTAGES * S::X_STAGE;
-    SmemTail& s = *reinterpret_cast<SmemTail*>(sR + RSTAGES * RAW_STAGE);
+    uint8_t* sStg = sR + RSTAGES * RAW_STAGE;
+    SmemTail& s = *reinterpret_cast<SmemTail*>(sStg + S::STG_BYTES);
     volatile int* abort_flag = &s.abort_flag;
 
     const int tid = threadIdx.x;
@@ -1320,26 +1041,36 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
             if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * S::ACC;
-            const int col_a = t.n0 + lrow;                                          // gate / low half
-            const int col_b = (MODE == MODE_GATE_UP) ? col_a : t.n0 + 128 + lrow;  // up / high half
+            // Each chunk of 16 tokens goes through this warp's staging area
+            // ([half][token][32 columns]) so that it leaves as 16-byte stores
+            // of 8 columns instead of one 2-byte store per token and column.
+            T* stg = reinterpret_cast<T*>(sStg) + (warp - S::EPI0) * (2 * 16 * 32);
+            const int colw = t.n0 + q * 32;  // this warp's first column (half 0)
+            constexpr int HALVES = MODE == MODE_GATE_UP ? 1 : 2;
 #pragma unroll 1
             for (int c = 0; c < NTOK && c < nvalid; c += 16) {
                 float a[16], b[16];
                 load_swapped<NTOK, S::NACC>(taddr, c, a, b);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const int r = c + j;
-                    if (r < nvalid) {
-                        const size_t orow = static_cast<size_t>(t.m0 + r) * p.n_out;
-                        if (MODE == MODE_GATE_UP) {
-                            if (col_a < p.n_out)
-                                out[orow + col_a] = Act<ACT>::from_f(silu_mul(a[j] * s2a, b[j] * s2b));
-                        } else {
-                            if (col_a < p.n_out) out[orow + col_a] = Act<ACT>::from_f(a[j] * s2a);
-                            if (col_b < p.n_out) out[orow + col_b] = Act<ACT>::from_f(b[j] * s2a);
-                        }
+                    if (MODE == MODE_GATE_UP) {
+                        stg[j * 32 + lane] = Act<ACT>::from_f(silu_mul(a[j] * s2a, b[j] * s2b));
+                    } else {
+                        stg[j * 32 + lane] = Act<ACT>::from_f(a[j] * s2a);
+                        stg[512 + j * 32 + lane] = Act<ACT>::from_f(b[j] * s2a);
                     }
                 }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 2 * HALVES; ++i) {
+                    const int pc = i * 32 + lane;  // [half][16 tokens][4 pieces of 8 columns]
+                    const int hh = pc >> 6, row = (pc >> 2) & 15, pq = pc & 3;
+                    const int col = colw + hh * 128 + pq * 8;
+                    if (c + row < nvalid && col < p.n_out)
+                        *reinterpret_cast<uint4*>(out + static_cast<size_t>(t.m0 + c + row) * p.n_out + col) =
+                            *reinterpret_cast<const uint4*>(stg + hh * 512 + row * 32 + pq * 8);
+                }
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();
@@ -1391,6 +1122,9 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
         }
     } else {
         // ---------------- raw quantised-weight producer (last warp) ----------------
+        // A TMA copy costs its engine a roughly fixed time however small it
+        // is, so a stage is fetched with as few copies as the layouts allow:
+        // GPTQ codes + scales + zero points (3), NVFP4 codes + scales (2).
         if (lane == 0) {
             uint32_t rstage = 0, rphase = 0;
             long issued = 0;
@@ -1398,8 +1132,6 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
                 const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
                 if (tile_is_padding(p, t)) continue;
-                int c0, c1;
-                half_bases<MODE>(p, t.n0, c0, c1);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&s.raw_empty[rstage], rphase ^ 1, abort_flag, p.err)) { ok = false; break; }
                     uint64_t* bar = &s.raw_full[rstage];
@@ -1408,18 +1140,24 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
                     if (WFMT == MOE_W_GPTQ_INT4) {
                         const int kq = t.e * (p.K / 8) + kb * 8;
                         const int g = t.e * (p.K / p.group_size) + (kb * BK) / p.group_size;
-                        tma_load_2d(rw, &tmR0, c0, kq, bar);
-                        tma_load_2d(rw + 4096, &tmR0, c1, kq, bar);
-                        tma_load_2d(rw + 8192, &tmR1, c0, g, bar);
-                        tma_load_2d(rw + 8448, &tmR1, c1, g, bar);
-                        tma_load_2d(rw + 8704, &tmR2, c0 / 8, g, bar);
-                        tma_load_2d(rw + 8832, &tmR2, c1 / 8, g, bar);
+                        if (MODE == MODE_GATE_UP) {
+                            tma_load_3d(rw, &tmR0, t.n0, 0, kq, bar);
+                            tma_load_3d(rw + 8192, &tmR1, t.n0, 0, g, bar);
+                            tma_load_3d(rw + 8704, &tmR2, t.n0 / 8, 0, g, bar);
+                        } else {
+                            tma_load_2d(rw, &tmR0, t.n0, kq, bar);
+                            tma_load_2d(rw + 8192, &tmR1, t.n0, g, bar);
+                            tma_load_2d(rw + 8704, &tmR2, t.n0 / 8, g, bar);
+                        }
                     } else {
-                        tma_load_2d(rw, &tmR0, kb * (BK / 2), t.e * p.n_w + c0, bar);
-                        tma_load_2d(rw + 4096, &tmR0, kb * (BK / 2), t.e * p.n_w + c1, bar);
                         const int sg = t.e * (p.K / 16) + kb * (BK / 16);
-                        tma_load_2d(rw + 8192, &tmR1, c0, sg, bar);
-                        tma_load_2d(rw + 8704, &tmR1, c1, sg, bar);
+                        if (MODE == MODE_GATE_UP) {
+                            tma_load_3d(rw, &tmR0, kb * (BK / 2), t.n0, 2 * t.e, bar);
+                            tma_load_3d(rw + 8192, &tmR1, t.n0, 0, sg, bar);
+                        } else {
+                            tma_load_2d(rw, &tmR0, kb * (BK / 2), t.e * p.n_w + t.n0, bar);
+                            tma_load_2d(rw + 8192, &tmR1, t.n0, sg, bar);
+                        }
                     }
                     ++issued;
                     if (++rstage == RSTAGES) { rstage = 0; rphase ^= 1; }
@@ -1490,10 +1228,10 @@ int pick_ntok(long P, int E, int block_size) {
     return nt <= 128 ? nt : 0;
 }
 
-template <int MODE, int WFMT, int ACT, int NTOK>
-int launch_gemm(const Maps& m, const GemmParams& p, cudaStream_t st, const char* who) {
-    using S = Shape<MODE, WFMT, ACT, NTOK>;
-    auto kernel = grouped_gemm_kernel<MODE, WFMT, ACT, NTOK>;
+template <int MODE, int NTOK>
+int launch_decode(const Maps& m, const GemmParams& p, cudaStream_t st, const char* who) {
+    using S = DecodeShape<MODE, NTOK>;
+    auto kernel = grouped_gemm_decode_kernel<MODE, NTOK>;
     static int configured_for = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1502,27 +1240,27 @@ int launch_gemm(const Maps& m, const GemmParams& p, cudaStream_t st, const char*
         if (rc != MOE_OK) return rc;
         configured_for = dev;
     }
-    const long bound = static_cast<long>((p.max_padded + S::XROWS - 1) / S::XROWS + p.E) *
+    const long bound = static_cast<long>((p.max_padded + NTOK - 1) / NTOK + p.E) *
                        ((p.n_out + S::OUT_COLS - 1) / S::OUT_COLS);
     const int sms = sm_count();
     if (sms <= 0) return fail(MOE_ERR_CUDA, "%s: cannot query the SM count", who);
     const int grid = static_cast<int>(bound < sms ? bound : sms);
     if (grid <= 0) return MOE_OK;
     GemmParams q = p;
-    q.pad_free = S::XROWS % p.block_size == 0;
-    kernel<<<grid, S::THREADS, S::SMEM, st>>>(m.x, m.w, m.r0, m.r1, m.r2, q);
+    q.pad_free = NTOK % p.block_size == 0;
+    kernel<<<grid, S::THREADS, S::SMEM, st>>>(m.x, m.w, q);
     count_launch();
     return check_launch(who);
 }
 
-template <int MODE, int WFMT, int ACT>
-int by_ntok(int ntok, const Maps& m, const GemmParams& p, cudaStream_t st, const char* who) {
+// bf16 weights, fewer than 128 rows per touched expert: the decode form
+template <int MODE>
+int decode_by_ntok(int ntok, const Maps& m, const GemmParams& p, cudaStream_t st, const char* who) {
     switch (ntok) {
-        case 0: return launch_gemm<MODE, WFMT, ACT, 0>(m, p, st, who);
-        case 16: return launch_gemm<MODE, WFMT, ACT, 16>(m, p, st, who);
-        case 32: return launch_gemm<MODE, WFMT, ACT, 32>(m, p, st, who);
-        case 64: return launch_gemm<MODE, WFMT, ACT, 64>(m, p, st, who);
-        default: return launch_gemm<MODE, WFMT, ACT, 128>(m, p, st, who);
+        case 16: return launch_decode<MODE, 16>(m, p, st, who);
+        case 32: return launch_decode<MODE, 32>(m, p, st, who);
+        case 64: return launch_decode<MODE, 64>(m, p, st, who);
+        default: return launch_decode<MODE, 128>(m, p, st, who);
     }
 }
 
@@ -1609,7 +1347,7 @@ template <int MODE>
 int dispatch(int wfmt, int act, int ntok, const Maps& m, const GemmParams& p, cudaStream_t st, const char* who) {
     if (wfmt == MOE_W_BF16) {
         if (ntok == 0) return launch_pair<MODE>(m, p, st, who);
-        return by_ntok<MODE, MOE_W_BF16, MOE_ACT_BF16>(ntok, m, p, st, who);
+        return decode_by_ntok<MODE>(ntok, m, p, st, who);
     }
     const int nt = ntok ? ntok : 128;
     if (wfmt == MOE_W_GPTQ_INT4)
@@ -1640,14 +1378,27 @@ int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Map
             MOE_REQUIRE(G >= 64 && G % 64 == 0 && K % G == 0,
                         "%s: GPTQ group_size=%d must be a multiple of 64 dividing K=%d", who, G, K);
             MOE_REQUIRE(n_out % 32 == 0, "%s: GPTQ needs %d output columns divisible by 32", who, n_out);
-            int rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4,
-                                      static_cast<uint64_t>(E) * (K / 8), N, 128, 8);
-            if (rc == MOE_OK)
-                rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                                      static_cast<uint64_t>(E) * (K / G), N, 128, 1);
-            if (rc == MOE_OK)
-                rc = make_tmap_2d_raw(&m.r2, w->zeros, CU_TENSOR_MAP_DATA_TYPE_INT32, 4,
-                                      static_cast<uint64_t>(E) * (K / G), N / 8, 16, 1);
+            // One copy per k block fetches both 128-column halves of a tile: for
+            // gate/up a 3-D map whose middle dimension steps from the gate to the
+            // up columns (n_out apart), for down a 256-column box.
+            const uint64_t kq = static_cast<uint64_t>(E) * (K / 8), kg = static_cast<uint64_t>(E) * (K / G);
+            int rc;
+            if (N == 2 * n_out) {
+                const uint64_t I = n_out;
+                rc = make_tmap_3d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, I, 2, kq, I * 4, 2 * I * 4, 128, 2, 8);
+                if (rc == MOE_OK)
+                    rc = make_tmap_3d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, I, 2, kg, I * 2,
+                                          2 * I * 2, 128, 2, 1);
+                if (rc == MOE_OK)
+                    rc = make_tmap_3d_raw(&m.r2, w->zeros, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, I / 8, 2, kg, I / 8 * 4,
+                                          2 * I / 8 * 4, 16, 2, 1);
+            } else {
+                rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, kq, N, 256, 8);
+                if (rc == MOE_OK)
+                    rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kg, N, 256, 1);
+                if (rc == MOE_OK)
+                    rc = make_tmap_2d_raw(&m.r2, w->zeros, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, kg, N / 8, 32, 1);
+            }
             m.w = m.r0;
             return rc;
         }
@@ -1655,11 +1406,23 @@ int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Map
             MOE_REQUIRE(w->w && w->scales && w->scale2, "%s: NVFP4 packed / scales / scale2 must be non-NULL", who);
             MOE_REQUIRE(K % 32 == 0, "%s: NVFP4 needs K=%d divisible by 32", who, K);
             MOE_REQUIRE(n_out % 16 == 0, "%s: NVFP4 needs %d output columns divisible by 16", who, n_out);
-            int rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(E) * N,
-                                      K / 2, 32, 128);
-            if (rc == MOE_OK)
-                rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                                      static_cast<uint64_t>(E) * (K / 16), N, 128, 4);
+            // one copy per k block for the packed codes and one for the scales
+            // (3-D maps over the gate and up halves for gate/up, 256-wide boxes
+            // for down)
+            const uint64_t kg = static_cast<uint64_t>(E) * (K / 16);
+            int rc;
+            if (N == 2 * n_out) {
+                const uint64_t I = n_out;
+                rc = make_tmap_3d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, I,
+                                      2 * static_cast<uint64_t>(E), K / 2, I * (K / 2), 32, 128, 2);
+                if (rc == MOE_OK)
+                    rc = make_tmap_3d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, I, 2, kg, I, 2 * I, 128,
+                                          2, 4);
+            } else {
+                rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(E) * N,
+                                      K / 2, 32, 256);
+                if (rc == MOE_OK) rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kg, N, 256, 4);
+            }
             m.r2 = m.r1;
             m.w = m.r0;
             return rc;

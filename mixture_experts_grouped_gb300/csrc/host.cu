@@ -111,6 +111,28 @@ int make_tmap_2d_raw(CUtensorMap* map, const void* base, CUtensorMapDataType dt,
     return MOE_OK;
 }
 
+int make_tmap_3d_raw(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t d0,
+                     uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+    auto fn = encode_fn();
+    if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    if (!aligned16(base)) return fail(MOE_ERR_INVALID, "tensor base address %p is not 16-byte aligned", base);
+    if (s1 % 16 != 0 || s2 % 16 != 0)
+        return fail(MOE_ERR_INVALID, "tensor strides %llu / %llu bytes are not 16-byte multiples",
+                    (unsigned long long)s1, (unsigned long long)s2);
+    (void)elem_bytes;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {s1, s2};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(MOE_ERR_INVALID, "cuTensorMapEncodeTiled failed (%d) for a %llux%llux%llu tensor", (int)r,
+                    (unsigned long long)d0, (unsigned long long)d1, (unsigned long long)d2);
+    return MOE_OK;
+}
+
 }  // namespace moe
 
 extern "C" {
