@@ -41,7 +41,6 @@ namespace {
 constexpr int BK = 64;
 constexpr int W_ROWS = 256;             // weight rows per tile
 constexpr int W_STAGE = W_ROWS * BK * 2;  // 32 KB
-constexpr int RAW_STAGE = 9216;         // raw quantised bytes of one weight stage
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_DQ_WARPS = 8;  // two per SM sub-partition: dequantisation is latency-bound
 constexpr int MAX_STAGES = 16;
@@ -287,17 +286,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 
 // Swapped forms (D = weight row x token): each half's accumulator is split
-// into NACC accumulators of NTOK columns that take the K=16 steps in turn,
-// so consecutive MMAs of a half do not depend on each other and the tensor
-// core overlaps them (a single accumulator makes every MMA wait for the one
-// before it, which dominates when N is small). Half 0 owns columns
+// into NACC accumulators of NTOK columns, each filled by its own MMA issuer
+// (or K step), so that several threads can issue. Half 0 owns columns
 // [0, NACC*NTOK), half 1 the next NACC*NTOK. This loads tokens [c, c+16) of
-// both halves and sums the split accumulators in f32.
+// both halves and sums, in f32, the nsets accumulators s0, s0+1, ... (mod
+// NACC) the tile used.
 template <int NTOK, int NACC>
-__device__ __forceinline__ void load_swapped(uint32_t taddr, int c, float (&fa)[16], float (&fb)[16]) {
+__device__ __forceinline__ void load_swapped(uint32_t taddr, int c, float (&fa)[16], float (&fb)[16],
+                                             int nsets = NACC, int s0 = 0) {
     uint32_t a[16], b[16];
-    tmem_ld16(taddr + c, a);
-    tmem_ld16(taddr + NACC * NTOK + c, b);
+    tmem_ld16(taddr + s0 * NTOK + c, a);
+    tmem_ld16(taddr + (NACC + s0) * NTOK + c, b);
     tmem_ld_wait();
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -306,8 +305,10 @@ __device__ __forceinline__ void load_swapped(uint32_t taddr, int c, float (&fa)[
     }
 #pragma unroll
     for (int q = 1; q < NACC; ++q) {
-        tmem_ld16(taddr + q * NTOK + c, a);
-        tmem_ld16(taddr + (NACC + q) * NTOK + c, b);
+        if (q >= nsets) break;
+        const int sq = (s0 + q) % NACC;
+        tmem_ld16(taddr + sq * NTOK + c, a);
+        tmem_ld16(taddr + (NACC + sq) * NTOK + c, b);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -713,37 +714,48 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
 // up, or two 128-column halves of the output) of NTOK columns each. Shared
 // memory then carries only the raw quantised bytes and the activations; the
 // 16-bit weights never touch it.
-constexpr int TS_STAGES = 4;   // weight stages in TMEM
+constexpr int TS_STAGES = 4;   // weight stages in TMEM (one 64-deep k block each)
 constexpr int TS_A_COL = 256;  // first TMEM column of the weight stages (64 columns each)
+constexpr int RAW2 = 18432;    // raw quantised bytes of one 128-deep stage (two k blocks)
 
 template <int MODE, int WFMT, int ACT, int NTOK>
 struct TsShape {
     static constexpr int X_STAGE = NTOK * BK * 2;
-    static constexpr int NACC = swapped_nacc(NTOK);  // split accumulators per half
-    static constexpr int ACC = 2 * NTOK * NACC;     // TMEM columns per accumulator buffer
-    static constexpr int NBUF = 2 * ACC <= TS_A_COL ? 2 : 1;
     static constexpr int OUT_COLS = MODE == MODE_GATE_UP ? 128 : 256;
-    // MMA-issuing warps. One thread issues a tcgen05.mma about every 100
-    // cycles whatever its N, so at small N the issue rate, not the tensor
-    // core, bounds a single issuer; several issuers, each owning its own
-    // accumulators (half h, split a: issuer (h * NACC + a) % NI), multiply it.
-    static constexpr int NI = 2 * NACC >= 4 ? 4 : 2;
+    // MMA issuers. One thread issues a tcgen05.mma about every 100 cycles
+    // whatever its N, so several issuing warps share the work, each with its
+    // own accumulators: NR issuers take the k blocks in turn (issuer set r
+    // owns the CTA's k blocks g = r mod NR, counted over all its tiles, and
+    // accumulator set r), and with NH = 2 each half (gate | up, or the two
+    // output halves) has its own issuer. Per 64-deep k block an issuer then
+    // issues 8 / NH MMAs and 2 commits for one k block in NR. Owning by the
+    // CTA-wide index, with stage counts that are multiples of NR, gives every
+    // ring stage a single issuer, which then sees its barrier phases in order
+    // (owning by index within a tile breaks that when KB mod NR != 0: an
+    // issuer could come back to a stage two phases ahead of its producer and
+    // take a stale phase for the current one).
+    static constexpr int NH = NTOK >= 64 ? 2 : 1;
+    static constexpr int NR = NTOK >= 128 ? 1 : (NTOK >= 64 ? 2 : 4);
+    static constexpr int NI = NH * NR;
+    static constexpr int ACC = 2 * NR * NTOK;  // TMEM columns per accumulator buffer: [half][set][token]
+    static constexpr int NBUF = 2 * ACC <= TS_A_COL ? 2 : 1;
+    // Dequantising warps: one per TMEM lane quarter and weight half.
+    static constexpr int NDQ = NUM_DQ_WARPS;
     static constexpr int EPI0 = 1 + NI;                 // first epilogue warp
     static constexpr int DQ0 = EPI0 + NUM_EPI_WARPS;    // first dequantising warp
-    static constexpr int RAWW = DQ0 + NUM_DQ_WARPS;     // raw producer warp
+    static constexpr int RAWW = DQ0 + NDQ;              // raw producer warp
     static constexpr int THREADS = 32 * (RAWW + 1);
     // epilogue staging: per epilogue warp 2 halves x 16 tokens x 32 columns
     static constexpr int STG_BYTES = NUM_EPI_WARPS * 2 * 16 * 32 * 2;
     static constexpr int AVAIL = SMEM_LIMIT - 1024 - TAIL_BYTES - STG_BYTES;
     // The activation ring is its own, deeper than the TMEM weight ring: its
-    // loads queue behind the raw weight stream, so they need as much time in
-    // flight as the raw bytes do. At least 8 raw stages are kept.
-    static constexpr int X_FIT = (AVAIL - 8 * RAW_STAGE) / X_STAGE;
-    static constexpr int XSTAGES = X_FIT < 12 ? X_FIT : 12;
-    static constexpr int RAW_FIT = (AVAIL - XSTAGES * X_STAGE) / RAW_STAGE;
+    // loads queue behind the raw weight stream. At least 4 raw stages (8 k
+    // blocks) are kept.
+    static constexpr int X_FIT = (AVAIL - 4 * RAW2) / X_STAGE;
+    static constexpr int XSTAGES = (X_FIT < 12 ? X_FIT : 12) / NR * NR;
+    static constexpr int RAW_FIT = (AVAIL - XSTAGES * X_STAGE) / RAW2;
     static constexpr int RSTAGES = RAW_FIT < MAX_RSTAGES ? RAW_FIT : MAX_RSTAGES;
-    static constexpr int SMEM = 1024 + XSTAGES * X_STAGE + RSTAGES * RAW_STAGE + STG_BYTES + TAIL_BYTES;
-    static constexpr int RAW_BYTES = WFMT == MOE_W_GPTQ_INT4 ? 8832 : 9216;
+    static constexpr int SMEM = 1024 + XSTAGES * X_STAGE + RSTAGES * RAW2 + STG_BYTES + TAIL_BYTES;
     // GPTQ gate/up writes each group of 8 k values in the order 0,4,1,5,2,6,3,7
     // (the order the int4 -> fp16 conversion produces them in); the gather
     // kernel stores the activations in the same order, so the products match
@@ -751,7 +763,8 @@ struct TsShape {
     static_assert(NBUF * ACC <= TS_A_COL, "accumulators overlap the weight stages");
     static_assert(TS_A_COL + TS_STAGES * 64 <= 512, "weight stages exceed TMEM");
     static_assert(XSTAGES >= 4 && XSTAGES <= MAX_STAGES, "activation ring size");
-    static_assert(RSTAGES >= 8, "not enough shared memory for the raw ring");
+    static_assert(XSTAGES % NR == 0 && TS_STAGES % NR == 0, "every ring stage must have one issuer");
+    static_assert(RSTAGES >= 4, "not enough shared memory for the raw ring");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory over the limit");
 };
 
@@ -862,32 +875,37 @@ __device__ __forceinline__ void nvfp4_row(const uint32_t (&w)[8], const uint32_t
     }
 }
 
-// One weight row's raw bytes for a k block, in registers: GPTQ 8 words, the
-// fp16 scale bits and the packed zero-point word; NVFP4 8 words and 4 scale
-// bytes.
+// One weight row's raw bytes for a 64-deep k block, in registers: GPTQ 8
+// words, the fp16 scale bits and the packed zero-point word; NVFP4 8 words and
+// 4 scale bytes.
 struct RawRow {
     uint32_t w[8];
     uint32_t s, z;
     uint32_t sc[4];
 };
 
+// A raw stage holds two k blocks (kp = 0, 1) of both 128-row halves:
+//   GPTQ:  codes [16 packed k rows][2 halves][128 cols] int32 at 0, scales
+//          [sg][2][128] fp16 at 16384, zeros [sg][2][16] int32 at 17408, where
+//          sg = 2 group rows for group_size 64 and 1 otherwise;
+//   NVFP4: codes [2 halves][128 rows][64 bytes] at 0, scales [8 k16 groups]
+//          [2 halves][128 rows] E4M3 at 16384.
 template <int WFMT>
-__device__ __forceinline__ void load_raw_row(const uint8_t* raw, int h, int r, RawRow& x) {
+__device__ __forceinline__ void load_raw_row(const uint8_t* raw, int h, int r, int kp, int g64, RawRow& x) {
     if (WFMT == MOE_W_GPTQ_INT4) {
-        // qweight [8 packed k rows][2 halves][128 cols] int32, scales [2][128] fp16, zeros [2][16] int32
         const uint32_t* qw = reinterpret_cast<const uint32_t*>(raw);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) x.w[i] = qw[(i * 2 + h) * 128 + r];
-        x.s = reinterpret_cast<const unsigned short*>(raw + 8192 + h * 256)[r];
-        x.z = reinterpret_cast<const uint32_t*>(raw + 8704 + h * 64)[r >> 3];
+        for (int i = 0; i < 8; ++i) x.w[i] = qw[((8 * kp + i) * 2 + h) * 128 + r];
+        const int sg = g64 ? kp : 0;
+        x.s = reinterpret_cast<const unsigned short*>(raw + 16384)[(sg * 2 + h) * 128 + r];
+        x.z = reinterpret_cast<const uint32_t*>(raw + 17408)[(sg * 2 + h) * 16 + (r >> 3)];
     } else {
-        // packed [2 halves][128 rows][32 bytes], scales [4 k16 groups][2 halves][128 rows] E4M3
-        const uint4* row = reinterpret_cast<const uint4*>(raw + h * 4096 + r * 32);
+        const uint4* row = reinterpret_cast<const uint4*>(raw + h * 8192 + r * 64 + kp * 32);
         const uint4 v0 = row[0], v1 = row[1];
         x.w[0] = v0.x; x.w[1] = v0.y; x.w[2] = v0.z; x.w[3] = v0.w;
         x.w[4] = v1.x; x.w[5] = v1.y; x.w[6] = v1.z; x.w[7] = v1.w;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) x.sc[g] = raw[8192 + g * 256 + h * 128 + r];
+        for (int g = 0; g < 4; ++g) x.sc[g] = raw[16384 + ((4 * kp + g) * 2 + h) * 128 + r];
     }
 }
 
@@ -902,34 +920,39 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
     uint8_t* smem = align1024_shared(smem_raw);
     uint8_t* sX = smem;
     uint8_t* sR = sX + XSTAGES * S::X_STAGE;
-    uint8_t* sStg = sR + RSTAGES * RAW_STAGE;
+    uint8_t* sStg = sR + RSTAGES * RAW2;
     SmemTail& s = *reinterpret_cast<SmemTail*>(sStg + S::STG_BYTES);
     volatile int* abort_flag = &s.abort_flag;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int E = p.E;
+    const int KB = (p.K + BK - 1) / BK;  // 64-deep k blocks (weight and activation stages)
+    const int KR = (KB + 1) / 2;         // 128-deep raw stages per tile
+    const int NSETS = KB < S::NR ? KB : S::NR;  // accumulator sets a tile uses
+    // GPTQ group rows per raw stage: two for group_size 64, else one
+    const int g64 = WFMT == MOE_W_GPTQ_INT4 && p.group_size == 64;
 
     const int bad = build_tile_list<XROWS>(s, p, S::OUT_COLS);
     if (tid == 0) {
         if (bad) set_err(p.err, MOE_DEV_ERR_OFFSETS);
 #pragma unroll
         for (int i = 0; i < XSTAGES; ++i) {
-            mbar_init(&s.full[i], 1);  // activation bytes
-            mbar_init(&s.empty[i], S::NI);
+            mbar_init(&s.full[i], 1);        // activation bytes
+            mbar_init(&s.empty[i], S::NH);   // the issuers of the k block (one per half with NH = 2)
         }
 #pragma unroll
         for (int i = 0; i < ASTAGES; ++i) {
             mbar_init(&s.afull[i], NUM_DQ_WARPS);  // every dequantising warp has written its rows
-            mbar_init(&s.aempty[i], S::NI);
+            mbar_init(&s.aempty[i], S::NH);
         }
 #pragma unroll
         for (int i = 0; i < RSTAGES; ++i) {
             mbar_init(&s.raw_full[i], 1);
-            mbar_init(&s.raw_empty[i], NUM_DQ_WARPS);
+            mbar_init(&s.raw_empty[i], S::NDQ);  // every dequantising warp
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&s.tfull[i], S::NI);
+            mbar_init(&s.tfull[i], S::NH * NSETS);  // every issuer that had a k block of the tile
             mbar_init(&s.tempty[i], NUM_EPI_WARPS);
         }
         mbar_init(&s.mma_done, S::NI);
@@ -948,7 +971,6 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = s.tmem_base;
-    const int KB = (p.K + BK - 1) / BK;  // a ragged last block is zero-filled
 
     if (warp == 0) {
         if (lane == 0) {
@@ -974,9 +996,11 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
     } else if (warp < S::EPI0) {
         if (lane == 0) {
             // ---------------- MMA issuers: A = weights (TMEM), B = activations ----------------
-            const int mi = warp - 1;  // this issuer's accumulators: (h * NACC + a) % NI == mi
+            const int mi = warp - 1;
+            const int hsel = S::NH == 2 ? (mi & 1) : -1;  // the half this issuer owns (-1: both)
+            const int rset = mi / S::NH;                  // its k blocks: g = rset mod NR
             constexpr uint32_t idesc = f16_idesc(ACT, 128, NTOK);
-            uint32_t stage = 0, phase = 0, astage = 0, aphase = 0;
+            int g0 = 0;  // k blocks of this CTA's earlier tiles
             int local = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
@@ -985,34 +1009,38 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
                 const int acc = S::NBUF == 2 ? (local & 1) : 0;
                 const uint32_t aph = S::NBUF == 2 ? ((local >> 1) & 1) : (local & 1);
                 ++local;
-                if (!mbar_wait(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
-                tc_fence_after();
-                const uint32_t d = tmem_base + acc * S::ACC;
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&s.full[stage], phase, abort_flag, p.err) ||
-                        !mbar_wait(&s.afull[astage], aphase, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
+                const int first = (rset - g0 % S::NR + S::NR) % S::NR;  // its first kb in this tile
+                if (first < KB) {
+                    if (!mbar_wait(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
                     tc_fence_after();
-                    const uint64_t xd = sw128_desc(smem_u32(sX + stage * S::X_STAGE));
-                    const uint32_t a0 = tmem_base + TS_A_COL + astage * 64;
+                    const uint32_t d = tmem_base + acc * S::ACC;
+                    for (int kb = first; kb < KB; kb += S::NR) {
+                        const int g = g0 + kb;
+                        const int xs = g % XSTAGES, as = g % ASTAGES;
+                        if (!mbar_wait(&s.full[xs], static_cast<uint32_t>((g / XSTAGES) & 1), abort_flag, p.err) ||
+                            !mbar_wait(&s.afull[as], static_cast<uint32_t>((g / ASTAGES) & 1), abort_flag, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t xd = sw128_desc(smem_u32(sX + xs * S::X_STAGE));
+                        const uint32_t a0 = tmem_base + TS_A_COL + as * 64;
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        const int a = k % S::NACC;
-                        const uint32_t en = kb > 0 || k >= S::NACC;
+                        for (int k = 0; k < BK / 16; ++k) {
+                            const uint32_t en = kb > first || k > 0;
 #pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            if ((h * S::NACC + a) % S::NI == mi)
-                                tc_mma_ts(d + (h * S::NACC + a) * NTOK, a0 + 32 * h + 8 * k, xd + 2 * k, idesc, en);
+                            for (int h = 0; h < 2; ++h)
+                                if (hsel < 0 || hsel == h)
+                                    tc_mma_ts(d + (h * S::NR + rset) * NTOK, a0 + 32 * h + 8 * k, xd + 2 * k, idesc,
+                                              en);
+                        }
+                        tc_commit(&s.empty[xs]);
+                        tc_commit(&s.aempty[as]);
                     }
-                    tc_commit(&s.empty[stage]);
-                    tc_commit(&s.aempty[astage]);
-                    if (++stage == XSTAGES) { stage = 0; phase ^= 1; }
-                    if (++astage == ASTAGES) { astage = 0; aphase ^= 1; }
+                    if (!ok) break;
+                    tc_commit(&s.tfull[acc]);
                 }
-                if (!ok) break;
-                tc_commit(&s.tfull[acc]);
+                g0 += KB;
             }
             tc_commit(&s.mma_done);
             mbar_drain(&s.mma_done, 0, kWaitLimitNs / 8);
@@ -1021,10 +1049,12 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
     } else if (warp < S::DQ0) {
         // ---------------- epilogue: lane = weight row of a half, columns = tokens ----------------
         const int q = warp & 3;
-        const int lrow = q * 32 + lane;
         using T = typename Act<ACT>::T;
         T* out = static_cast<T*>(p.out);
+        T* stg = reinterpret_cast<T*>(sStg) + (warp - S::EPI0) * (2 * 16 * 32);
+        constexpr int HALVES = MODE == MODE_GATE_UP ? 1 : 2;
         int local = 0;
+        int g0 = 0;  // k blocks of this CTA's earlier tiles: the tile's sets start at g0 mod NR
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
             const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
             if (tile_is_padding(p, t)) continue;
@@ -1041,16 +1071,13 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
             if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * S::ACC;
-            // Each chunk of 16 tokens goes through this warp's staging area
-            // ([half][token][32 columns]) so that it leaves as 16-byte stores
-            // of 8 columns instead of one 2-byte store per token and column.
-            T* stg = reinterpret_cast<T*>(sStg) + (warp - S::EPI0) * (2 * 16 * 32);
             const int colw = t.n0 + q * 32;  // this warp's first column (half 0)
-            constexpr int HALVES = MODE == MODE_GATE_UP ? 1 : 2;
 #pragma unroll 1
             for (int c = 0; c < NTOK && c < nvalid; c += 16) {
                 float a[16], b[16];
-                load_swapped<NTOK, S::NACC>(taddr, c, a, b);
+                load_swapped<NTOK, S::NR>(taddr, c, a, b, NSETS, g0 % S::NR);
+                // Through this warp's staging area ([half][token][32 columns]),
+                // so that the chunk leaves as 16-byte stores of 8 columns.
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     if (MODE == MODE_GATE_UP) {
@@ -1075,88 +1102,100 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.tempty[acc]);
+            g0 += KB;
         }
     } else if (warp < S::RAWW) {
         // ---------------- dequantising warps: raw shared bytes -> TMEM ----------------
-        // The raw stages arrive in order, one per k block of every non-padding
-        // tile of this CTA; the next stage's bytes are loaded into registers
-        // before the current one is converted, to hide the shared-memory latency.
+        // Item j (the CTA's j-th k block) is k block kb of its tile, in raw
+        // stage tile * KR + kb / 2 (half kb & 1 of it), weight stage j mod
+        // TS_STAGES. Each warp releases a raw stage after loading its last
+        // item. The next item's bytes are loaded into registers before the
+        // current one is converted.
         const int h = (warp - S::DQ0) >> 2;  // weight half
-        const int sp = warp & 3;                          // TMEM lane quarter this warp may access
-        const int r = sp * 32 + lane;                     // weight row within the half
+        const int sp = warp & 3;             // TMEM lane quarter this warp may access
+        const int r = sp * 32 + lane;        // weight row within the half
         const uint32_t trow = tmem_base + (static_cast<uint32_t>(sp * 32) << 16) + TS_A_COL + h * 32;
-        long items = 0;
+        int items = 0;
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x)
             if (!tile_is_padding(p, decode_tile<XROWS>(s, E, tile, S::OUT_COLS))) items += KB;
-        RawRow cur, nxt;
-        uint32_t stage = 0, phase = 0, rstage = 0, rphase = 0;
-        bool ok = items > 0 && mbar_wait(&s.raw_full[0], 0, abort_flag, p.err);
-        if (ok) {
-            load_raw_row<WFMT>(sR, h, r, cur);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s.raw_empty[0]);
-            if (++rstage == RSTAGES) { rstage = 0; rphase ^= 1; }
-        }
-        for (long it = 0; it < items && ok; ++it) {
-            if (it + 1 < items) {
-                if (!mbar_wait(&s.raw_full[rstage], rphase, abort_flag, p.err)) break;
-                load_raw_row<WFMT>(sR + rstage * RAW_STAGE, h, r, nxt);
+        int f_kb = 0, f_rs0 = 0;  // position of the next item to fetch (k block, its tile's first raw stage)
+        auto fetch = [&](RawRow& x) -> bool {
+            const int rs = f_rs0 + (f_kb >> 1);
+            const int rst = rs % RSTAGES;
+            if ((f_kb & 1) == 0 &&
+                !mbar_wait(&s.raw_full[rst], static_cast<uint32_t>((rs / RSTAGES) & 1), abort_flag, p.err))
+                return false;
+            load_raw_row<WFMT>(sR + rst * RAW2, h, r, f_kb & 1, g64, x);
+            if ((f_kb & 1) == 1 || f_kb == KB - 1) {
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&s.raw_empty[rstage]);
-                if (++rstage == RSTAGES) { rstage = 0; rphase ^= 1; }
+                if (lane == 0) mbar_arrive(&s.raw_empty[rst]);
             }
+            if (++f_kb == KB) {
+                f_kb = 0;
+                f_rs0 += KR;
+            }
+            return true;
+        };
+        RawRow cur, nxt;
+        bool ok = items > 0 && fetch(cur);
+        for (int it = 0; it < items && ok; ++it) {
+            if (it + 1 < items && !fetch(nxt)) break;
             uint32_t o[32];
             if (WFMT == MOE_W_GPTQ_INT4)
-                gptq_row<ACT, S::PERM>(cur.w, (cur.z >> (4 * (r & 7))) & 15, __ushort_as_half(static_cast<unsigned short>(cur.s)), o);
+                gptq_row<ACT, S::PERM>(cur.w, (cur.z >> (4 * (r & 7))) & 15,
+                                       __ushort_as_half(static_cast<unsigned short>(cur.s)), o);
             else
                 nvfp4_row<ACT>(cur.w, cur.sc, o);
-            if (!mbar_wait(&s.aempty[stage], phase ^ 1, abort_flag, p.err)) break;
+            const int as = it % ASTAGES;
+            if (!mbar_wait(&s.aempty[as], static_cast<uint32_t>(((it / ASTAGES) & 1) ^ 1), abort_flag, p.err)) break;
             tc_fence_after();  // the MMAs that read this TMEM stage have completed
-            tmem_st32(trow + stage * 64, o);
+            tmem_st32(trow + as * 64, o);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s.afull[stage]);
-            if (++stage == ASTAGES) { stage = 0; phase ^= 1; }
+            if (lane == 0) mbar_arrive(&s.afull[as]);
             cur = nxt;
         }
     } else {
         // ---------------- raw quantised-weight producer (last warp) ----------------
-        // A TMA copy costs its engine a roughly fixed time however small it
-        // is, so a stage is fetched with as few copies as the layouts allow:
-        // GPTQ codes + scales + zero points (3), NVFP4 codes + scales (2).
+        // A TMA copy costs its issuing thread a roughly fixed time however
+        // small it is, so a 128-deep stage (two k blocks) is fetched with as
+        // few copies as the layouts allow: GPTQ codes + scales + zero points,
+        // NVFP4 codes + scales. For an odd number of k blocks the second half
+        // of a tile's last stage is fetched but not used.
         if (lane == 0) {
+            const uint32_t bytes = WFMT == MOE_W_GPTQ_INT4 ? 16384u + (g64 ? 2u : 1u) * 640u : 18432u;
             uint32_t rstage = 0, rphase = 0;
             long issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
                 const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
                 if (tile_is_padding(p, t)) continue;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kr = 0; kr < KR; ++kr) {
                     if (!mbar_wait(&s.raw_empty[rstage], rphase ^ 1, abort_flag, p.err)) { ok = false; break; }
                     uint64_t* bar = &s.raw_full[rstage];
-                    uint8_t* rw = sR + rstage * RAW_STAGE;
-                    mbar_arrive_expect_tx(bar, S::RAW_BYTES);
+                    uint8_t* rw = sR + rstage * RAW2;
+                    mbar_arrive_expect_tx(bar, bytes);
                     if (WFMT == MOE_W_GPTQ_INT4) {
-                        const int kq = t.e * (p.K / 8) + kb * 8;
-                        const int g = t.e * (p.K / p.group_size) + (kb * BK) / p.group_size;
+                        const int kq = t.e * (p.K / 8) + kr * 16;
+                        const int g = t.e * (p.K / p.group_size) + (kr * 2 * BK) / p.group_size;
                         if (MODE == MODE_GATE_UP) {
                             tma_load_3d(rw, &tmR0, t.n0, 0, kq, bar);
-                            tma_load_3d(rw + 8192, &tmR1, t.n0, 0, g, bar);
-                            tma_load_3d(rw + 8704, &tmR2, t.n0 / 8, 0, g, bar);
+                            tma_load_3d(rw + 16384, &tmR1, t.n0, 0, g, bar);
+                            tma_load_3d(rw + 17408, &tmR2, t.n0 / 8, 0, g, bar);
                         } else {
                             tma_load_2d(rw, &tmR0, t.n0, kq, bar);
-                            tma_load_2d(rw + 8192, &tmR1, t.n0, g, bar);
-                            tma_load_2d(rw + 8704, &tmR2, t.n0 / 8, g, bar);
+                            tma_load_2d(rw + 16384, &tmR1, t.n0, g, bar);
+                            tma_load_2d(rw + 17408, &tmR2, t.n0 / 8, g, bar);
                         }
                     } else {
-                        const int sg = t.e * (p.K / 16) + kb * (BK / 16);
+                        const int sg = t.e * (p.K / 16) + kr * 8;
                         if (MODE == MODE_GATE_UP) {
-                            tma_load_3d(rw, &tmR0, kb * (BK / 2), t.n0, 2 * t.e, bar);
-                            tma_load_3d(rw + 8192, &tmR1, t.n0, 0, sg, bar);
+                            tma_load_3d(rw, &tmR0, kr * BK, t.n0, 2 * t.e, bar);
+                            tma_load_3d(rw + 16384, &tmR1, t.n0, 0, sg, bar);
                         } else {
-                            tma_load_2d(rw, &tmR0, kb * (BK / 2), t.e * p.n_w + t.n0, bar);
-                            tma_load_2d(rw + 8192, &tmR1, t.n0, sg, bar);
+                            tma_load_2d(rw, &tmR0, kr * BK, t.e * p.n_w + t.n0, bar);
+                            tma_load_2d(rw + 16384, &tmR1, t.n0, sg, bar);
                         }
                     }
                     ++issued;
@@ -1378,26 +1417,29 @@ int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Map
             MOE_REQUIRE(G >= 64 && G % 64 == 0 && K % G == 0,
                         "%s: GPTQ group_size=%d must be a multiple of 64 dividing K=%d", who, G, K);
             MOE_REQUIRE(n_out % 32 == 0, "%s: GPTQ needs %d output columns divisible by 32", who, n_out);
-            // One copy per k block fetches both 128-column halves of a tile: for
-            // gate/up a 3-D map whose middle dimension steps from the gate to the
-            // up columns (n_out apart), for down a 256-column box.
+            // One copy per 128-deep raw stage fetches both 128-column halves of a
+            // tile: for gate/up a 3-D map whose middle dimension steps from the
+            // gate to the up columns (n_out apart), for down a 256-column box.
+            // A stage spans one group row, or two for group_size 64.
             const uint64_t kq = static_cast<uint64_t>(E) * (K / 8), kg = static_cast<uint64_t>(E) * (K / G);
+            const uint32_t sg = G == 64 ? 2 : 1;
             int rc;
             if (N == 2 * n_out) {
                 const uint64_t I = n_out;
-                rc = make_tmap_3d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, I, 2, kq, I * 4, 2 * I * 4, 128, 2, 8);
+                rc = make_tmap_3d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, I, 2, kq, I * 4, 2 * I * 4, 128, 2,
+                                      16);
                 if (rc == MOE_OK)
                     rc = make_tmap_3d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, I, 2, kg, I * 2,
-                                          2 * I * 2, 128, 2, 1);
+                                          2 * I * 2, 128, 2, sg);
                 if (rc == MOE_OK)
                     rc = make_tmap_3d_raw(&m.r2, w->zeros, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, I / 8, 2, kg, I / 8 * 4,
-                                          2 * I / 8 * 4, 16, 2, 1);
+                                          2 * I / 8 * 4, 16, 2, sg);
             } else {
-                rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, kq, N, 256, 8);
+                rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, kq, N, 256, 16);
                 if (rc == MOE_OK)
-                    rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kg, N, 256, 1);
+                    rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kg, N, 256, sg);
                 if (rc == MOE_OK)
-                    rc = make_tmap_2d_raw(&m.r2, w->zeros, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, kg, N / 8, 32, 1);
+                    rc = make_tmap_2d_raw(&m.r2, w->zeros, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, kg, N / 8, 32, sg);
             }
             m.w = m.r0;
             return rc;
@@ -1406,22 +1448,22 @@ int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Map
             MOE_REQUIRE(w->w && w->scales && w->scale2, "%s: NVFP4 packed / scales / scale2 must be non-NULL", who);
             MOE_REQUIRE(K % 32 == 0, "%s: NVFP4 needs K=%d divisible by 32", who, K);
             MOE_REQUIRE(n_out % 16 == 0, "%s: NVFP4 needs %d output columns divisible by 16", who, n_out);
-            // one copy per k block for the packed codes and one for the scales
-            // (3-D maps over the gate and up halves for gate/up, 256-wide boxes
-            // for down)
+            // one copy per 128-deep raw stage for the packed codes and one for
+            // the scales (3-D maps over the gate and up halves for gate/up,
+            // 256-wide boxes for down)
             const uint64_t kg = static_cast<uint64_t>(E) * (K / 16);
             int rc;
             if (N == 2 * n_out) {
                 const uint64_t I = n_out;
                 rc = make_tmap_3d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, I,
-                                      2 * static_cast<uint64_t>(E), K / 2, I * (K / 2), 32, 128, 2);
+                                      2 * static_cast<uint64_t>(E), K / 2, I * (K / 2), 64, 128, 2);
                 if (rc == MOE_OK)
                     rc = make_tmap_3d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, I, 2, kg, I, 2 * I, 128,
-                                          2, 4);
+                                          2, 8);
             } else {
                 rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(E) * N,
-                                      K / 2, 32, 256);
-                if (rc == MOE_OK) rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kg, N, 256, 4);
+                                      K / 2, 64, 256);
+                if (rc == MOE_OK) rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kg, N, 256, 8);
             }
             m.r2 = m.r1;
             m.w = m.r0;
