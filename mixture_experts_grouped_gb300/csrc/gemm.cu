@@ -112,7 +112,12 @@ struct DecodeShape {
     static constexpr int NACC = swapped_nacc(NTOK);
     static constexpr int ACC = 2 * NTOK * NACC;
     static constexpr int TMEM_COLS = pow2_at_least(2 * ACC);
-    static constexpr int THREADS = 32 * (2 + NUM_EPI_WARPS);
+    // MMA issuers: one thread issues a tcgen05.mma about every 100 cycles
+    // whatever its N, so from 64 tokens on each weight half has its own
+    // issuing warp (with its own accumulators)
+    static constexpr int NH = NTOK >= 64 ? 2 : 1;
+    static constexpr int EPI0 = 1 + NH;  // first epilogue warp
+    static constexpr int THREADS = 32 * (EPI0 + NUM_EPI_WARPS);
     static constexpr int SMEM = 1024 + STAGES * (X_STAGE + W_STAGE) + STG_BYTES + TAIL_BYTES;
     static_assert(STAGES >= 2, "not enough shared memory for two stages");
     static_assert(TMEM_COLS <= 512, "accumulators exceed TMEM");
@@ -345,13 +350,13 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
 #pragma unroll
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&s.full[i], 1);
-            mbar_init(&s.empty[i], 1);
+            mbar_init(&s.empty[i], S::NH);  // every issuer releases the stage
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&s.tfull[i], 1);
+            mbar_init(&s.tfull[i], S::NH);
             mbar_init(&s.tempty[i], NUM_EPI_WARPS);
         }
-        mbar_init(&s.mma_done, 1);
+        mbar_init(&s.mma_done, S::NH);
         fence_mbar_init();
     }
     __syncthreads();
@@ -399,9 +404,10 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
             for (long j = first; j < issued; ++j)
                 mbar_drain(&s.full[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1), kWaitLimitNs / 8);
         }
-    } else if (warp == 1) {
+    } else if (warp < S::EPI0) {
         if (lane == 0) {
-            // ---------------- MMA issuer: A = weight halves, B = tokens ----------------
+            // ---------------- MMA issuers: A = weight halves, B = tokens ----------------
+            const int hsel = S::NH == 2 ? warp - 1 : -1;  // the half this issuer owns (-1: both)
             constexpr uint32_t idesc = f16_idesc(ACT, 128, NTOK);
             uint32_t stage = 0, phase = 0;
             int local = 0;
@@ -425,8 +431,8 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
                     for (int k = 0; k < BK / 16; ++k) {
                         const int a = k % S::NACC;
                         const uint32_t en = kb > 0 || k >= S::NACC;
-                        tc_mma(d + a * NTOK, wd + 2 * k, xd + 2 * k, idesc, en);
-                        tc_mma(d + (S::NACC + a) * NTOK, wd1 + 2 * k, xd + 2 * k, idesc, en);
+                        if (hsel != 1) tc_mma(d + a * NTOK, wd + 2 * k, xd + 2 * k, idesc, en);
+                        if (hsel != 0) tc_mma(d + (S::NACC + a) * NTOK, wd1 + 2 * k, xd + 2 * k, idesc, en);
                     }
                     tc_commit(&s.empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -443,7 +449,7 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         using T = typename Act<ACT>::T;
         T* out = static_cast<T*>(p.out);
-        T* stg = reinterpret_cast<T*>(sStg) + (warp - 2) * (2 * 16 * 32);
+        T* stg = reinterpret_cast<T*>(sStg) + (warp - S::EPI0) * (2 * 16 * 32);
         constexpr int HALVES = MODE == MODE_GATE_UP ? 1 : 2;
         int local = 0;
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
