@@ -780,21 +780,21 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t mask, uint32_t b
     return r;
 }
 
-// One GPTQ weight row for a 64-deep k block: word i holds the codes of k =
-// 8i .. 8i+7 (4 bits each, k order from the low bits), z the zero point and
-// sh the fp16 scale of the row's group. Writes (q - z) * s as 32 columns of
-// two 16-bit values. fp16: 1024 + q and 1024 + 16q come from the code bits
+// One GPTQ weight row for NW words of a k block (8 k values each): word i
+// holds the codes of k = 8i .. 8i+7 (4 bits each, k order from the low bits),
+// z the zero point and sh the fp16 scale of the row's group. Writes
+// (q - z) * s as 4 NW columns of two 16-bit values. fp16: 1024 + q and 1024 + 16q come from the code bits
 // by one mask-or each (exact), subtracting the zero point is exact, and the
 // product with s is the only rounding.
-template <int ACT, bool PERM>
-__device__ __forceinline__ void gptq_row(const uint32_t (&w)[8], int z, __half sh, uint32_t (&o)[32]) {
+template <int ACT, bool PERM, int NW = 8>
+__device__ __forceinline__ void gptq_row(const uint32_t (&w)[NW], int z, __half sh, uint32_t (&o)[4 * NW]) {
     if (ACT == MOE_ACT_F16) {
         const __half2 s2 = __half2half2(sh);
         const __half2 z1 = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400 | z)));      // 1024 + z
         const __half2 c16 = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x2C00)));         // 1/16
         const __half2 nz16 = __half2half2(__ushort_as_half(static_cast<unsigned short>(0xD400 | (z << 4))));  // -(64 + z)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < NW; ++i) {
             const uint32_t w8 = w[i] >> 8;
             uint32_t q[4] = {and_or(w[i], 0x000F000Fu, 0x64006400u),   // (k0, k4): 1024 + q
                              and_or(w[i], 0x00F000F0u, 0x64006400u),   // (k1, k5): 1024 + 16 q
@@ -825,7 +825,7 @@ __device__ __forceinline__ void gptq_row(const uint32_t (&w)[8], int z, __half s
         // an fp16 value) and rounds once to bf16
         const float s = __half2float(sh);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < NW; ++i) {
             float f[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) f[j] = static_cast<float>(static_cast<int>((w[i] >> (4 * j)) & 15u) - z) * s;
@@ -844,13 +844,14 @@ __device__ __forceinline__ void gptq_row(const uint32_t (&w)[8], int z, __half s
     }
 }
 
-// One NVFP4 weight row for a 64-deep k block: word i holds the E2M1 codes of
-// k = 8i .. 8i+7 (low nibble first), sc[g] the E4M3 scale of k = 16g ..
+// One NVFP4 weight row for NW words of a k block: word i holds the E2M1 codes
+// of k = 8i .. 8i+7 (low nibble first), sc[g] the E4M3 scale of k = 16g ..
 // 16g+15. E2M1 x E4M3 products are exact in bf16 and fp16.
-template <int ACT>
-__device__ __forceinline__ void nvfp4_row(const uint32_t (&w)[8], const uint32_t (&sc)[4], uint32_t (&o)[32]) {
+template <int ACT, int NW = 8>
+__device__ __forceinline__ void nvfp4_row(const uint32_t (&w)[NW], const uint32_t (&sc)[NW / 2],
+                                          uint32_t (&o)[4 * NW]) {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < NW / 2; ++g) {
         if (ACT == MOE_ACT_BF16) {
             const __nv_bfloat162 s2 = __float2bfloat162_rn(e4m3_to_f32(sc[g]));
 #pragma unroll
@@ -1394,7 +1395,7 @@ int dispatch(int wfmt, int act, int ntok, const Maps& m, const GemmParams& p, cu
         if (ntok == 0) return launch_pair<MODE>(m, p, st, who);
         return decode_by_ntok<MODE>(ntok, m, p, st, who);
     }
-    const int nt = ntok ? ntok : 128;
+    const int nt = ntok ? ntok : 128;  // prefill: 128-token tiles
     if (wfmt == MOE_W_GPTQ_INT4)
         return act == MOE_ACT_F16 ? ts_by_ntok<MODE, MOE_W_GPTQ_INT4, MOE_ACT_F16>(nt, m, p, st, who)
                                   : ts_by_ntok<MODE, MOE_W_GPTQ_INT4, MOE_ACT_BF16>(nt, m, p, st, who);
@@ -1405,6 +1406,8 @@ int dispatch(int wfmt, int act, int ntok, const Maps& m, const GemmParams& p, cu
 // Checks the weight descriptor and encodes its tensor maps. N = weight rows
 // per expert, K = contraction, n_out = output columns (I for gate/up).
 int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Maps& m, const char* who) {
+    // TS form: tiles of 128 gate + 128 up (or 256 down) weight rows
+    const uint32_t hc = 128, dc = 2 * hc;
     MOE_REQUIRE(w != nullptr, "%s: NULL weight descriptor", who);
     MOE_REQUIRE(act == MOE_ACT_BF16 || act == MOE_ACT_F16, "%s: unknown activation type %d", who, act);
     switch (w->format) {
@@ -1432,20 +1435,20 @@ int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Map
             int rc;
             if (N == 2 * n_out) {
                 const uint64_t I = n_out;
-                rc = make_tmap_3d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, I, 2, kq, I * 4, 2 * I * 4, 128, 2,
+                rc = make_tmap_3d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, I, 2, kq, I * 4, 2 * I * 4, hc, 2,
                                       16);
                 if (rc == MOE_OK)
                     rc = make_tmap_3d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, I, 2, kg, I * 2,
-                                          2 * I * 2, 128, 2, sg);
+                                          2 * I * 2, hc, 2, sg);
                 if (rc == MOE_OK)
                     rc = make_tmap_3d_raw(&m.r2, w->zeros, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, I / 8, 2, kg, I / 8 * 4,
-                                          2 * I / 8 * 4, 16, 2, sg);
+                                          2 * I / 8 * 4, hc / 8, 2, sg);
             } else {
-                rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, kq, N, 256, 16);
+                rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, kq, N, dc, 16);
                 if (rc == MOE_OK)
-                    rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kg, N, 256, sg);
+                    rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kg, N, dc, sg);
                 if (rc == MOE_OK)
-                    rc = make_tmap_2d_raw(&m.r2, w->zeros, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, kg, N / 8, 32, sg);
+                    rc = make_tmap_2d_raw(&m.r2, w->zeros, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, kg, N / 8, dc / 8, sg);
             }
             m.w = m.r0;
             return rc;
@@ -1462,14 +1465,14 @@ int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Map
             if (N == 2 * n_out) {
                 const uint64_t I = n_out;
                 rc = make_tmap_3d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, I,
-                                      2 * static_cast<uint64_t>(E), K / 2, I * (K / 2), 64, 128, 2);
+                                      2 * static_cast<uint64_t>(E), K / 2, I * (K / 2), 64, hc, 2);
                 if (rc == MOE_OK)
-                    rc = make_tmap_3d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, I, 2, kg, I, 2 * I, 128,
+                    rc = make_tmap_3d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, I, 2, kg, I, 2 * I, hc,
                                           2, 8);
             } else {
                 rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(E) * N,
-                                      K / 2, 64, 256);
-                if (rc == MOE_OK) rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kg, N, 256, 8);
+                                      K / 2, 64, dc);
+                if (rc == MOE_OK) rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kg, N, dc, 8);
             }
             m.r2 = m.r1;
             m.w = m.r0;
@@ -1500,6 +1503,8 @@ extern "C" int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* 
                 max_padded);
     MOE_REQUIRE(H > 0 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", who, H);
     MOE_REQUIRE(I > 0 && I % 8 == 0, "%s: I=%d must be a positive multiple of 8", who, I);
+    const long P = static_cast<long>(T) * top_k;
+    const int ntok = moe::pick_ntok(P, E, block_size);
     moe::Maps m;
     int rc = moe::weight_maps(w_gate_up, act, E, 2 * I, H, I, m, who);
     if (rc != MOE_OK) return rc;
@@ -1510,8 +1515,6 @@ extern "C" int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* 
     MOE_REQUIRE(workspace && workspace_bytes >= need && (reinterpret_cast<uintptr_t>(workspace) & 127) == 0,
                 "%s: workspace of %zu bytes (128-byte aligned) required, got %zu", who, need, workspace_bytes);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const long P = static_cast<long>(T) * top_k;
-    const int ntok = moe::pick_ntok(P, E, block_size);
 
     // 1. gather activations into sorted-row order
     {
@@ -1558,14 +1561,14 @@ extern "C" int moe_grouped_down(const void* h, int32_t act, const MoeWeight* w_d
                 max_padded);
     MOE_REQUIRE(I > 0 && I % 8 == 0, "%s: I=%d must be a positive multiple of 8", who, I);
     MOE_REQUIRE(H > 0 && H % 8 == 0, "%s: H=%d must be a positive multiple of 8", who, H);
+    const long P = static_cast<long>(T) * top_k;
+    const int ntok = moe::pick_ntok(P, E, block_size);
     moe::Maps m;
     int rc = moe::weight_maps(w_down, act, E, H, I, H, m, who);
     if (rc != MOE_OK) return rc;
     if (max_padded == 0) return MOE_OK;
     MOE_REQUIRE(h && sorted_token_ids && expert_offsets && y, "%s: NULL pointer", who);
     MOE_REQUIRE(moe::aligned16(h) && moe::aligned16(y), "%s: h / y must be 16-byte aligned", who);
-    const long P = static_cast<long>(T) * top_k;
-    const int ntok = moe::pick_ntok(P, E, block_size);
     rc = moe::make_tmap_2d(&m.x, h, max_padded, I, ntok ? ntok : 128, act);
     if (rc != MOE_OK) return rc;
     moe::GemmParams p{};

@@ -149,6 +149,12 @@ LAYER_CASES = {
     "block48_prefill": synth.MoeConfig("block48_prefill", T=500, H=256, I=256, E=4, k=2, bs=48, router="normal"),
     "block48_gptq": synth.MoeConfig("block48_gptq", T=300, H=256, I=256, E=4, k=2, bs=48, act="f16",
                                     wfmt="gptq", router="normal"),
+    # prefill form of the quantised kernels with the other activation type, an
+    # odd number of 64-deep k blocks (I=192) and a ragged last column tile (H=320)
+    "gptq_bf16_prefill": synth.MoeConfig("gptq_bf16_prefill", T=300, H=320, I=192, E=2, k=1, bs=16, act="bf16",
+                                         wfmt="gptq", router="normal", group_size=64),
+    "nvfp4_f16_prefill": synth.MoeConfig("nvfp4_f16_prefill", T=300, H=320, I=192, E=2, k=1, bs=16, act="f16",
+                                         wfmt="nvfp4", router="normal"),
 }
 
 
