@@ -64,6 +64,12 @@ extern "C" {
 
 /* ---- limits ---------------------------------------------------------------- */
 #define MOE_MAX_EXPERTS 256 /* [ferrum] moe_align_block_size: compile-time MAX_NUM_EXPERTS */
+/* Split-K area of the grouped GEMM workspaces: fp32 partial sums of up to
+ * MOE_SPLITK_CTAS CTAs (128 KB each) followed by 16 bytes of flags per CTA.
+ * It must hold zeros before its first use (allocate it zeroed); every call
+ * that finishes without a device error leaves it zeroed again. */
+#define MOE_SPLITK_CTAS 256
+#define MOE_SPLITK_BYTES ((size_t)MOE_SPLITK_CTAS * (131072 + 16))
 #define MOE_MAX_TOPK 16
 #define MOE_MAX_LORA_RANK 64
 
@@ -217,8 +223,9 @@ int moe_align_block_size_noalloc(const int32_t* topk_ids, int32_t P, int32_t E, 
 
 /* ---- a3 / a4: grouped GEMMs ----------------------------------------------- */
 
-/* Bytes of device workspace moe_grouped_gate_up needs (the gathered copy of
- * the activations in sorted-row order). */
+/* Bytes of device workspace moe_grouped_gate_up needs: the gathered copy of
+ * the activations in sorted-row order, rounded up to 256 bytes, then the
+ * split-K area (MOE_SPLITK_BYTES, zeroed before first use). */
 size_t moe_gate_up_workspace_size(int32_t max_padded, int32_t H);
 
 /*
@@ -242,7 +249,9 @@ size_t moe_gate_up_workspace_size(int32_t max_padded, int32_t H);
  *   block_size        the block_size the align step padded spans to
  *   h_out             device act [max_padded, I] out
  *   err_word          device i32 or NULL
- *   workspace         device, >= moe_gate_up_workspace_size bytes, 128-byte aligned
+ *   workspace         device, >= moe_gate_up_workspace_size bytes, 128-byte aligned;
+ *                     its split-K area zeroed before the first call, and again
+ *                     after a call that reported a device error
  * Requirements: H % 8 == 0, I % 8 == 0, E <= MOE_MAX_EXPERTS, all tensor
  * base addresses 16-byte aligned; GPTQ: group_size a multiple of 64 dividing
  * H and I % 32 == 0; NVFP4: H % 32 == 0 and I % 16 == 0. A contraction that
@@ -265,6 +274,10 @@ int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* w_gate_up,
  *   block_size        the block_size the align step padded spans to
  *   y                 device act [max_padded, H] out (padding rows and rows past
  *                     expert_offsets[E] are not guaranteed to be written)
+ *   workspace         device, >= moe_down_workspace_size() bytes, 128-byte
+ *                     aligned, zeroed before the first call (and again after a
+ *                     call that reported a device error); the decode form cuts
+ *                     tiles across CTAs (split-K) and adds partial sums there
  * Requirements: I % 8 == 0, H % 8 == 0, 16-byte aligned tensors; GPTQ:
  * group_size a multiple of 64 dividing I and H % 32 == 0; NVFP4: I % 32 == 0
  * and H % 16 == 0.
@@ -273,7 +286,10 @@ int moe_grouped_down(const void* h, int32_t act, const MoeWeight* w_down,
                      const int32_t* sorted_token_ids, const int32_t* expert_offsets,
                      int32_t T, int32_t top_k, int32_t H, int32_t I, int32_t E,
                      int32_t block_size, int32_t max_padded, void* y, int32_t* err_word,
-                     void* stream);
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace moe_grouped_down needs (the split-K area). */
+size_t moe_down_workspace_size(void);
 
 /* ---- a5: LoRA fold ----------------------------------------------------------- */
 

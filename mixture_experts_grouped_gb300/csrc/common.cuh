@@ -156,6 +156,35 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// Flags in global memory that one CTA raises for another within a launch.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait until the global flag *f is nonzero, with the same limit and abort
+// rule as mbar_wait. Every calling thread observes the flag itself (acquire),
+// so each sees the data released before it.
+__device__ __forceinline__ bool flag_wait(const int* f, volatile int* abort_flag, int32_t* err) {
+    if (ld_acquire_gpu(f)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (ld_acquire_gpu(f)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            set_err(err, MOE_DEV_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(64);
+    }
+}
+
 // Bounded wait that ignores the abort flag: used on the way out to let copies
 // already in flight land before the CTA exits.
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {

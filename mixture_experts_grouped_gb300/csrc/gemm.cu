@@ -64,6 +64,8 @@ struct GemmParams {
     int32_t* err;
     int block_size;  // align block size: spans are multiples of it, padding is a span's last < block_size rows
     int pad_free;    // the kernel's tile height is a multiple of block_size: no tile holds padding only
+    float* sk_part;  // split-K partial sums: one slice of SK_SLICE_FLOATS per CTA (decode form)
+    int* sk_flag;    // split-K flags: 4 per CTA (one per epilogue warp), zero between launches
 };
 
 struct SmemTail {
@@ -126,6 +128,112 @@ struct DecodeShape {
 
 struct TileInfo {
     int e, m0, n0, rows;
+};
+
+// ---- work partition of the decode form ----------------------------------------
+// With whole tiles per CTA, a launch of n_tiles = w * G + rem tiles on G CTAs
+// takes w + 1 tile-times however small rem is (153 tiles on 152 SMs take two).
+// So the work is split as a hybrid of data-parallel waves and stream-K:
+//   - n_tiles >= G: whole tiles are dealt round-robin (tile c + i * G), so
+//     the CTAs of a wave work on neighbouring tiles at once and share the
+//     weight rows of an expert's row blocks in L2. When the last wave is thin
+//     (rem < G / 4: far too few SMs to keep HBM busy, one SM streams at most
+//     about 1/90 of it), the last G + rem tiles are instead cut into G
+//     contiguous ranges of k-blocks of nearly equal length (with a thicker
+//     last wave, cutting measured no faster);
+//   - n_tiles <= G / 2: each tile is cut into min(G / n_tiles, KB /
+//     SK_MIN_PIECE) equal pieces.
+// A tile cut by a range boundary is finished by the CTA whose range holds its
+// k-block 0 (its owner: that piece ends the owner's range). Every other piece
+// starts a range, so a CTA holds at most one; it leaves fp32 partial sums in
+// the CTA's slice of the split-K area and raises the CTA's flags; the owner
+// waits for the flags of the CTAs after it that hold the tile's other pieces,
+// adds their slices and runs the epilogue. Waits only point to higher CTA
+// indices, and a CTA's first item never waits, so with all CTAs resident (one
+// per SM, grid <= SMs) the waits end.
+constexpr int SK_MAX_CTAS = MOE_SPLITK_CTAS;
+constexpr int SK_SLICE_FLOATS = 256 * 128;  // 2 halves x 128 weight rows x up to 128 tokens
+constexpr int SK_MIN_PIECE = 4;
+static_assert(static_cast<size_t>(SK_MAX_CTAS) * (SK_SLICE_FLOATS * 4 + 16) <= MOE_SPLITK_BYTES,
+              "split-K area too small");
+
+// One CTA's share: the whole tiles blockIdx.x + i * G below `base`, then the
+// k-block units [lo, hi) of the stream-K region, which holds the tiles from
+// `base` on (unit u = (tile - base) * KB + kb). The region holds fewer than 2 G tiles,
+// so its unit counts stay far inside 32 bits (the launcher checks
+// 2 G * KB * G < 2^31).
+struct SkPlan {
+    int base, geff;
+    uint32_t U, lo, hi;
+};
+
+__device__ __forceinline__ SkPlan sk_plan(int n_tiles, int KB, int G, int c) {
+    SkPlan pl;
+    int region;
+    if (n_tiles < G) {
+        const int split_max = KB / SK_MIN_PIECE > 1 ? KB / SK_MIN_PIECE : 1;
+        const int split = G / n_tiles < split_max ? G / n_tiles : split_max;
+        region = split > 1 ? n_tiles : 0;
+        pl.geff = split > 1 ? n_tiles * split : G;
+    } else {
+        const int w = n_tiles / G, rem = n_tiles - w * G;
+        const bool cut = rem > 0 && 4 * rem < G;
+        region = cut ? G + rem : 0;
+        pl.geff = G;
+    }
+    pl.base = n_tiles - region;
+    pl.U = static_cast<uint32_t>(region) * static_cast<uint32_t>(KB);
+    pl.lo = c < pl.geff ? pl.U * static_cast<uint32_t>(c) / static_cast<uint32_t>(pl.geff) : 0u;
+    pl.hi = c < pl.geff ? pl.U * static_cast<uint32_t>(c + 1) / static_cast<uint32_t>(pl.geff) : 0u;
+    return pl;
+}
+
+// the CTA whose range holds unit u of the stream-K region
+__device__ __forceinline__ int sk_cta_of(const SkPlan& pl, uint32_t u) {
+    return static_cast<int>(((u + 1) * static_cast<uint32_t>(pl.geff) - 1) / pl.U);
+}
+
+// One piece of a tile: k-blocks [kb0, kb1) of `tile`.
+struct SkItem {
+    int tile, kb0, kb1;
+};
+
+// Walks a CTA's share in order (the same sequence in every role): the
+// stream-K range first, then the round-robin whole tiles. A range is shorter
+// than two tiles, so the owner's piece of a cut tile comes within its first
+// three items, and the peer pieces it needs are the first items of the
+// following CTAs: they are published by the time the owner's epilogue needs
+// them, and that epilogue (which reads their slices from L2) overlaps the MMAs
+// of the whole tiles that follow instead of ending the kernel.
+struct SkWalk {
+    int tile;
+    uint32_t u;
+    __device__ __forceinline__ explicit SkWalk(const SkPlan& pl) : tile(blockIdx.x), u(pl.lo) {}
+    __device__ __forceinline__ bool next(const SkPlan& pl, int KB, SkItem& it) {
+        if (u < pl.hi) {
+            const uint32_t rt = u / static_cast<uint32_t>(KB);
+            const uint32_t t0 = rt * static_cast<uint32_t>(KB);
+            const uint32_t end = pl.hi < t0 + KB ? pl.hi : t0 + KB;
+            it.tile = pl.base + static_cast<int>(rt);
+            it.kb0 = static_cast<int>(u - t0);
+            it.kb1 = static_cast<int>(end - t0);
+            u = end;
+            return true;
+        }
+        if (tile < pl.base) {  // whole tiles of the round-robin waves
+            it.tile = tile;
+            it.kb0 = 0;
+            it.kb1 = KB;
+            tile += gridDim.x;
+            return true;
+        }
+        return false;
+    }
+    // the last CTA holding a piece of the owner's cut tile
+    __device__ __forceinline__ static int last_peer(const SkPlan& pl, int KB, const SkItem& it) {
+        if (it.kb0 > 0 || it.kb1 == KB) return blockIdx.x;
+        return sk_cta_of(pl, static_cast<uint32_t>(it.tile - pl.base) * KB + KB - 1);
+    }
 };
 
 template <int XROWS>
@@ -325,6 +433,120 @@ __device__ __forceinline__ void load_swapped(uint32_t taddr, int c, float (&fa)[
 
 // ---- bf16 decode form -------------------------------------------------------------
 
+// One 16-token chunk of a decode tile to global memory: lane = weight row of
+// each half, a / b = tokens [c, c+16) of half 0 / 1 (gate / up: one column's
+// silu(gate) * up). The chunk goes through the warp's staging area
+// ([half][token][32 columns]) so that it leaves as 16-byte stores of 8
+// columns.
+template <int MODE>
+__device__ __forceinline__ void decode_store_chunk(const float (&a)[16], const float (&b)[16], __nv_bfloat16* stg,
+                                                   __nv_bfloat16* out, int lane, int c, int nvalid, int m0,
+                                                   int colw, int n_out) {
+    using A = Act<MOE_ACT_BF16>;
+    constexpr int HALVES = MODE == MODE_GATE_UP ? 1 : 2;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        if (MODE == MODE_GATE_UP) {
+            stg[j * 32 + lane] = A::from_f(silu_mul(a[j], b[j]));
+        } else {
+            stg[j * 32 + lane] = A::from_f(a[j]);
+            stg[512 + j * 32 + lane] = A::from_f(b[j]);
+        }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 2 * HALVES; ++i) {
+        const int pc = i * 32 + lane;  // [half][16 tokens][4 pieces of 8 columns]
+        const int hh = pc >> 6, row = (pc >> 2) & 15, pq = pc & 3;
+        const int col = colw + hh * 128 + pq * 8;
+        if (c + row < nvalid && col < n_out)
+            *reinterpret_cast<uint4*>(out + static_cast<size_t>(m0 + c + row) * n_out + col) =
+                *reinterpret_cast<const uint4*>(stg + hh * 512 + row * 32 + pq * 8);
+    }
+    __syncwarp();
+}
+
+// Epilogue of one piece of a tile cut by the stream-K partition, for the
+// calling epilogue warp (TMEM lane quarter q). A later piece (to_owner)
+// leaves its fp32 sums in this CTA's slice of the split-K area and raises the
+// CTA's flag for q; the owner waits for the flags of CTAs blockIdx.x + 1 ..
+// last_peer, adds their slices to its own sums and stores the chunk. Returns
+// false when a wait gave up.
+template <int MODE, int NTOK, int NACC>
+__device__ __forceinline__ bool decode_split_epilogue(const GemmParams& p, uint64_t* tfull, uint32_t aph,
+                                                   volatile int* abort_flag, bool to_owner, int last_peer,
+                                                   uint32_t tacc, int q, int lane, int nvalid,
+                                                   __nv_bfloat16* stg, int m0, int colw) {
+    const uint32_t taddr = tacc + (static_cast<uint32_t>(q * 32) << 16);
+    // this lane's place in a slice: [quarter q][16-token chunk][half][4 floats of 16][lane], float4 units
+    const size_t lane_off = static_cast<size_t>(q) * (NTOK / 16) * 256 + lane;
+    constexpr size_t SLICE4 = SK_SLICE_FLOATS / 4;
+    if (to_owner) {
+        if (!mbar_wait(tfull, aph, abort_flag, p.err)) return false;
+        tc_fence_after();
+        float4* d = reinterpret_cast<float4*>(p.sk_part) + blockIdx.x * SLICE4 + lane_off;
+#pragma unroll 1
+        for (int c = 0; c < NTOK && c < nvalid; c += 16) {
+            float a[16], b[16];
+            load_swapped<NTOK, NACC>(taddr, c, a, b);
+            float4* dc = d + (c / 16) * 256;
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4) {
+                dc[j4 * 32] = make_float4(a[4 * j4], a[4 * j4 + 1], a[4 * j4 + 2], a[4 * j4 + 3]);
+                dc[128 + j4 * 32] = make_float4(b[4 * j4], b[4 * j4 + 1], b[4 * j4 + 2], b[4 * j4 + 3]);
+            }
+        }
+        // the slice is complete: publish it to the owner
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(p.sk_flag + blockIdx.x * 4 + q, 1);
+        return true;
+    }
+    // owner: wait for the peers, fetch the first peer's first chunk while this
+    // CTA's own MMAs may still run
+    const int first_peer = blockIdx.x + 1;
+    for (int pc = first_peer; pc <= last_peer; ++pc)
+        if (!flag_wait(p.sk_flag + pc * 4 + q, abort_flag, p.err)) return false;
+    const float4* peer0 = reinterpret_cast<const float4*>(p.sk_part) + first_peer * SLICE4 + lane_off;
+    float4 nx[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) nx[j] = __ldcg(peer0 + (j & 3) * 32 + (j >> 2) * 128);
+    if (!mbar_wait(tfull, aph, abort_flag, p.err)) return false;
+    tc_fence_after();
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 1
+    for (int c = 0; c < NTOK && c < nvalid; c += 16) {
+        float a[16], b[16];
+        load_swapped<NTOK, NACC>(taddr, c, a, b);
+#pragma unroll
+        for (int j4 = 0; j4 < 4; ++j4) {
+            const float4 x = nx[j4], y = nx[4 + j4];
+            a[4 * j4] += x.x; a[4 * j4 + 1] += x.y; a[4 * j4 + 2] += x.z; a[4 * j4 + 3] += x.w;
+            b[4 * j4] += y.x; b[4 * j4 + 1] += y.y; b[4 * j4 + 2] += y.z; b[4 * j4 + 3] += y.w;
+        }
+        if (c + 16 < NTOK && c + 16 < nvalid) {  // the first peer's next chunk
+            const float4* d = peer0 + (c / 16 + 1) * 256;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) nx[j] = __ldcg(d + (j & 3) * 32 + (j >> 2) * 128);
+        }
+        for (int pc = first_peer + 1; pc <= last_peer; ++pc) {
+            const float4* d = reinterpret_cast<const float4*>(p.sk_part) + pc * SLICE4 + lane_off + (c / 16) * 256;
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4) {
+                const float4 x = __ldcg(d + j4 * 32), y = __ldcg(d + 128 + j4 * 32);
+                a[4 * j4] += x.x; a[4 * j4 + 1] += x.y; a[4 * j4 + 2] += x.z; a[4 * j4 + 3] += x.w;
+                b[4 * j4] += y.x; b[4 * j4 + 1] += y.y; b[4 * j4 + 2] += y.z; b[4 * j4 + 3] += y.w;
+            }
+        }
+        decode_store_chunk<MODE>(a, b, stg, out, lane, c, nvalid, m0, colw, p.n_out);
+    }
+    // every lane has read the peers' slices: clear their flags for the next launch
+    __syncwarp();
+    if (lane == 0)
+        for (int pc = first_peer; pc <= last_peer; ++pc) p.sk_flag[pc * 4 + q] = 0;
+    return true;
+}
+
 template <int MODE, int NTOK>
 __global__ void __launch_bounds__(DecodeShape<MODE, NTOK>::THREADS, 1)
 grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -361,7 +583,10 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
     }
     __syncthreads();
     const int n_tiles = s.n_tiles;
-    if (static_cast<int>(blockIdx.x) >= n_tiles) return;  // block-uniform: nothing allocated yet
+    if (n_tiles == 0) return;  // block-uniform: nothing allocated yet
+    const int KB = (p.K + BK - 1) / BK;  // a ragged last block is zero-filled
+    const SkPlan plan = sk_plan(n_tiles, KB, gridDim.x, blockIdx.x);
+    if (static_cast<int>(blockIdx.x) >= plan.base && plan.lo >= plan.hi) return;
 
     if (warp == 1) {
         tmem_alloc(&s.tmem_base, S::TMEM_COLS);
@@ -375,7 +600,6 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = s.tmem_base;
-    const int KB = (p.K + BK - 1) / BK;  // a ragged last block is zero-filled
 
     if (warp == 0) {
         if (lane == 0) {
@@ -383,12 +607,13 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
             uint32_t stage = 0, phase = 0;
             long issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
+            SkItem it;
+            for (SkWalk wk(plan); ok && wk.next(plan, KB, it);) {
+                const TileInfo t = decode_tile<XROWS>(s, E, it.tile, S::OUT_COLS);
                 if (tile_is_padding(p, t)) continue;
                 int c0, c1;
                 half_bases<MODE>(p, t.n0, c0, c1);
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = it.kb0; kb < it.kb1; ++kb) {
                     if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
                     mbar_arrive_expect_tx(&s.full[stage], S::X_STAGE + W_STAGE);
                     tma_load_2d(sX + stage * S::X_STAGE, &tmX, kb * BK, t.m0, &s.full[stage]);
@@ -412,8 +637,9 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
             uint32_t stage = 0, phase = 0;
             int local = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
+            SkItem it;
+            for (SkWalk wk(plan); ok && wk.next(plan, KB, it);) {
+                const TileInfo t = decode_tile<XROWS>(s, E, it.tile, S::OUT_COLS);
                 if (tile_is_padding(p, t)) continue;
                 const int acc = local & 1;
                 const uint32_t aph = (local >> 1) & 1;
@@ -421,7 +647,7 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
                 if (!mbar_wait(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * S::ACC;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = it.kb0; kb < it.kb1; ++kb) {
                     if (!mbar_wait(&s.full[stage], phase, abort_flag, p.err)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t xd = sw128_desc(smem_u32(sX + stage * S::X_STAGE));
@@ -430,7 +656,7 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
                         const int a = k % S::NACC;
-                        const uint32_t en = kb > 0 || k >= S::NACC;
+                        const uint32_t en = kb > it.kb0 || k >= S::NACC;
                         if (hsel != 1) tc_mma(d + a * NTOK, wd + 2 * k, xd + 2 * k, idesc, en);
                         if (hsel != 0) tc_mma(d + (S::NACC + a) * NTOK, wd1 + 2 * k, xd + 2 * k, idesc, en);
                     }
@@ -450,45 +676,36 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
         using T = typename Act<ACT>::T;
         T* out = static_cast<T*>(p.out);
         T* stg = reinterpret_cast<T*>(sStg) + (warp - S::EPI0) * (2 * 16 * 32);
-        constexpr int HALVES = MODE == MODE_GATE_UP ? 1 : 2;
         int local = 0;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-            const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
+        bool ok = true;
+        SkItem it;
+        for (SkWalk wk(plan); ok && wk.next(plan, KB, it);) {
+            const TileInfo t = decode_tile<XROWS>(s, E, it.tile, S::OUT_COLS);
             if (tile_is_padding(p, t)) continue;
             const int acc = local & 1;
             const uint32_t aph = (local >> 1) & 1;
             ++local;
             const int nvalid = valid_rows(p, s, t, lane);  // its loads overlap the wait
-            if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
-            tc_fence_after();
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * S::ACC;
             const int colw = t.n0 + q * 32;  // this warp's first column (half 0)
+            const int last_peer = SkWalk::last_peer(plan, KB, it);
+            if (it.kb0 > 0 || last_peer > static_cast<int>(blockIdx.x)) {
+                // a piece of a cut tile (stream-K)
+                if (!decode_split_epilogue<MODE, NTOK, S::NACC>(p, &s.tfull[acc], aph, abort_flag, it.kb0 > 0,
+                                                                 last_peer, tmem_base + acc * S::ACC, q, lane,
+                                                                 nvalid, stg, t.m0, colw)) {
+                    ok = false;
+                    break;
+                }
+            } else {
+                if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * S::ACC;
 #pragma unroll 1
-            for (int c = 0; c < NTOK && c < nvalid; c += 16) {
-                float a[16], b[16];
-                load_swapped<NTOK, S::NACC>(taddr, c, a, b);
-                // through this warp's staging area ([half][token][32 columns]),
-                // so that the chunk leaves as 16-byte stores of 8 columns
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    if (MODE == MODE_GATE_UP) {
-                        stg[j * 32 + lane] = Act<ACT>::from_f(silu_mul(a[j], b[j]));
-                    } else {
-                        stg[j * 32 + lane] = Act<ACT>::from_f(a[j]);
-                        stg[512 + j * 32 + lane] = Act<ACT>::from_f(b[j]);
-                    }
+                for (int c = 0; c < NTOK && c < nvalid; c += 16) {
+                    float a[16], b[16];
+                    load_swapped<NTOK, S::NACC>(taddr, c, a, b);
+                    decode_store_chunk<MODE>(a, b, stg, out, lane, c, nvalid, t.m0, colw, p.n_out);
                 }
-                __syncwarp();
-#pragma unroll
-                for (int i = 0; i < 2 * HALVES; ++i) {
-                    const int pc = i * 32 + lane;  // [half][16 tokens][4 pieces of 8 columns]
-                    const int hh = pc >> 6, row = (pc >> 2) & 15, pq = pc & 3;
-                    const int col = colw + hh * 128 + pq * 8;
-                    if (c + row < nvalid && col < p.n_out)
-                        *reinterpret_cast<uint4*>(out + static_cast<size_t>(t.m0 + c + row) * p.n_out + col) =
-                            *reinterpret_cast<const uint4*>(stg + hh * 512 + row * 32 + pq * 8);
-                }
-                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();
@@ -1286,12 +1503,18 @@ int launch_decode(const Maps& m, const GemmParams& p, cudaStream_t st, const cha
         if (rc != MOE_OK) return rc;
         configured_for = dev;
     }
+    // tiles at most, times the pieces a tile may be cut into when tiles are fewer than SMs
+    const int KB = (p.K + BK - 1) / BK;
     const long bound = static_cast<long>((p.max_padded + NTOK - 1) / NTOK + p.E) *
-                       ((p.n_out + S::OUT_COLS - 1) / S::OUT_COLS);
-    const int sms = sm_count();
+                       ((p.n_out + S::OUT_COLS - 1) / S::OUT_COLS) * (KB / SK_MIN_PIECE > 1 ? KB / SK_MIN_PIECE : 1);
+    int sms = sm_count();
     if (sms <= 0) return fail(MOE_ERR_CUDA, "%s: cannot query the SM count", who);
+    if (sms > SK_MAX_CTAS) sms = SK_MAX_CTAS;  // one split-K slice per CTA
     const int grid = static_cast<int>(bound < sms ? bound : sms);
     if (grid <= 0) return MOE_OK;
+    if (!p.sk_part || !p.sk_flag) return fail(MOE_ERR_INVALID, "%s: no split-K area", who);
+    // the stream-K unit arithmetic is 32-bit: region (< 2 grid tiles) x KB x grid
+    if (2L * grid * KB * grid >= (1L << 31)) return fail(MOE_ERR_UNSUPPORTED, "%s: contraction too long", who);
     GemmParams q = p;
     q.pad_free = NTOK % p.block_size == 0;
     kernel<<<grid, S::THREADS, S::SMEM, st>>>(m.x, m.w, q);
@@ -1486,10 +1709,25 @@ int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Map
 }  // namespace
 }  // namespace moe
 
+namespace moe {
+namespace {
+// the gathered activations, then the split-K area
+size_t gather_bytes(int32_t max_padded, int32_t H) {
+    return (static_cast<size_t>(max_padded) * H * 2 + 255) / 256 * 256;
+}
+void set_splitk(GemmParams& p, void* area) {
+    p.sk_part = static_cast<float*>(area);
+    p.sk_flag = reinterpret_cast<int*>(static_cast<uint8_t*>(area) + static_cast<size_t>(SK_MAX_CTAS) * SK_SLICE_FLOATS * 4);
+}
+}  // namespace
+}  // namespace moe
+
 extern "C" size_t moe_gate_up_workspace_size(int32_t max_padded, int32_t H) {
     if (max_padded < 0 || H < 0) return 0;
-    return static_cast<size_t>(max_padded) * H * 2;
+    return moe::gather_bytes(max_padded, H) + MOE_SPLITK_BYTES;
 }
+
+extern "C" size_t moe_down_workspace_size(void) { return MOE_SPLITK_BYTES; }
 
 extern "C" int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* w_gate_up,
                                    const int32_t* sorted_token_ids, const int32_t* expert_offsets, int32_t T,
@@ -1547,13 +1785,14 @@ extern "C" int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* 
     p.group_size = w_gate_up->group_size;
     p.err = err_word;
     p.block_size = block_size;
+    moe::set_splitk(p, static_cast<uint8_t*>(workspace) + moe::gather_bytes(max_padded, H));
     return moe::dispatch<moe::MODE_GATE_UP>(w_gate_up->format, act, ntok, m, p, st, who);
 }
 
 extern "C" int moe_grouped_down(const void* h, int32_t act, const MoeWeight* w_down, const int32_t* sorted_token_ids,
                                 const int32_t* expert_offsets, int32_t T, int32_t top_k, int32_t H, int32_t I,
                                 int32_t E, int32_t block_size, int32_t max_padded, void* y, int32_t* err_word,
-                                void* stream) {
+                                void* workspace, size_t workspace_bytes, void* stream) {
     const char* who = "moe_grouped_down";
     MOE_REQUIRE(E >= 1 && E <= MOE_MAX_EXPERTS, "%s: E=%d outside [1, %d]", who, E, MOE_MAX_EXPERTS);
     MOE_REQUIRE(block_size >= 1, "%s: block_size=%d must be positive", who, block_size);
@@ -1569,6 +1808,9 @@ extern "C" int moe_grouped_down(const void* h, int32_t act, const MoeWeight* w_d
     if (max_padded == 0) return MOE_OK;
     MOE_REQUIRE(h && sorted_token_ids && expert_offsets && y, "%s: NULL pointer", who);
     MOE_REQUIRE(moe::aligned16(h) && moe::aligned16(y), "%s: h / y must be 16-byte aligned", who);
+    MOE_REQUIRE(workspace && workspace_bytes >= MOE_SPLITK_BYTES && (reinterpret_cast<uintptr_t>(workspace) & 127) == 0,
+                "%s: workspace of %zu bytes (128-byte aligned) required, got %zu", who,
+                static_cast<size_t>(MOE_SPLITK_BYTES), workspace_bytes);
     rc = moe::make_tmap_2d(&m.x, h, max_padded, I, ntok ? ntok : 128, act);
     if (rc != MOE_OK) return rc;
     moe::GemmParams p{};
@@ -1585,5 +1827,6 @@ extern "C" int moe_grouped_down(const void* h, int32_t act, const MoeWeight* w_d
     p.group_size = w_down->group_size;
     p.err = err_word;
     p.block_size = block_size;
+    moe::set_splitk(p, workspace);
     return moe::dispatch<moe::MODE_DOWN>(w_down->format, act, ntok, m, p, static_cast<cudaStream_t>(stream), who);
 }

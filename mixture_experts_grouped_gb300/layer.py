@@ -117,7 +117,10 @@ class MoeLayer:
         self.align_ws_bytes = M.moe_align_workspace_size(self.P, E)
         self.align_ws = torch.empty(self.align_ws_bytes, dtype=torch.uint8, device=device)
         self.gate_up_ws_bytes = M.moe_gate_up_workspace_size(self.max_padded, H)
-        self.gate_up_ws = torch.empty(max(1, self.gate_up_ws_bytes), dtype=torch.uint8, device=device)
+        # zeroed: both GEMM workspaces end in a split-K area that must start at zero
+        self.gate_up_ws = torch.zeros(max(1, self.gate_up_ws_bytes), dtype=torch.uint8, device=device)
+        self.down_ws_bytes = M.moe_down_workspace_size()
+        self.down_ws = torch.zeros(self.down_ws_bytes, dtype=torch.uint8, device=device)
         self.h = torch.empty((self.max_padded, I), dtype=dt, device=device)
         self.y = torch.empty((self.max_padded, H), dtype=dt, device=device)
         self.out = torch.empty((T, H), dtype=dt, device=device)
@@ -142,7 +145,7 @@ class MoeLayer:
     def down(self, stream=None):
         M.moe_grouped_down(self.h, self.act_code, self.w_down.desc, self.sorted_token_ids, self.expert_offsets,
                            self.T, self.k, self.H, self.I, self.E, self.bs, self.max_padded, self.y, self.err,
-                           stream)
+                           self.down_ws, self.down_ws_bytes, stream)
 
     def lora_fold(self, stream=None, row_offset=0, row_end=None):
         if self.lora is None:

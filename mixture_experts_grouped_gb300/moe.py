@@ -59,7 +59,9 @@ _SIGNATURES = {
                                       c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
                                       c_size_t, c_void_p]),
     "moe_grouped_down": (c_int32, [c_void_p, c_int32, POINTER(MoeWeight), c_void_p, c_void_p, c_int32, c_int32,
-                                   c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
+                                   c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                   c_size_t, c_void_p]),
+    "moe_down_workspace_size": (c_size_t, []),
     "moe_lora_grouped_down": (c_int32, [POINTER(MoeExpertRoute), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                         c_void_p, c_uint32, c_uint32, c_uint32, c_int32, c_int32, c_void_p]),
     "moe_combine": (c_int32, [c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
@@ -171,11 +173,15 @@ def moe_grouped_gate_up(x, act, w_gate_up: MoeWeight, sorted_token_ids, expert_o
         block_size, max_padded, _ptr(h_out), _ptr(err_word), _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
+def moe_down_workspace_size() -> int:
+    return int(lib().moe_down_workspace_size())
+
+
 def moe_grouped_down(h, act, w_down: MoeWeight, sorted_token_ids, expert_offsets, T, top_k, H, I, E, block_size,
-                     max_padded, y, err_word, stream=None):
+                     max_padded, y, err_word, workspace, workspace_bytes, stream=None):
     _check("moe_grouped_down", lib().moe_grouped_down(
         _ptr(h), act, ctypes.byref(w_down), _ptr(sorted_token_ids), _ptr(expert_offsets), T, top_k, H, I, E,
-        block_size, max_padded, _ptr(y), _ptr(err_word), _stream(stream)))
+        block_size, max_padded, _ptr(y), _ptr(err_word), _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def moe_lora_grouped_down(route: MoeExpertRoute, x, base_out, expert_offsets, sorted_token_ids, row_adapter, xa,

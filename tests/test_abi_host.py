@@ -67,7 +67,12 @@ def test_capacity_matches_the_bound(moe):
 
 
 def test_workspace_sizes(moe):
-    assert moe.moe_gate_up_workspace_size(8704, 4096) == 8704 * 4096 * 2
+    # the gathered rows (rounded up to 256 bytes), then the split-K area: 128 KB of
+    # partial sums and 16 bytes of flags for each of 256 CTAs
+    splitk = 256 * (128 * 1024 + 16)
+    assert moe.moe_down_workspace_size() == splitk
+    assert moe.moe_gate_up_workspace_size(8704, 4096) == 8704 * 4096 * 2 + splitk
+    assert moe.moe_gate_up_workspace_size(3, 8) == 256 + splitk
     small = moe.moe_align_workspace_size(32, 8)
     big = moe.moe_align_workspace_size(131072, 128)
     assert small > 0 and big >= 131072 * 4 + 64 * 128 * 4
@@ -92,11 +97,11 @@ def test_workspace_sizes(moe):
     lambda m: m.moe_grouped_gate_up(16, 0, m.MoeWeight(7, 0, 16, None, None, None), 16, 16, 4, 2, 128, 64, 8,
                                     16, 64, 16, 0, 16, 1 << 30, 0),             # unknown format
     lambda m: m.moe_grouped_down(16, 0, m.MoeWeight(0, 0, 16, None, None, None), 16, 16, 4, 2, 128, 100, 8, 16, 64,
-                                 16, 0, 0),                                     # I % 8
+                                 16, 0, 16, 1 << 30, 0),                         # I % 8
     lambda m: m.moe_grouped_down(16, 0, m.MoeWeight(2, 0, 16, 16, None, 16), 16, 16, 4, 2, 128, 72, 8, 16, 64, 16,
-                                 0, 0),                                         # NVFP4 K % 32
+                                 0, 16, 1 << 30, 0),                             # NVFP4 K % 32
     lambda m: m.moe_grouped_down(16, 1, m.MoeWeight(1, 64, 16, 16, 16, None), 16, 16, 4, 2, 200, 64, 8, 16, 64, 16,
-                                 0, 0),                                         # GPTQ H % 32
+                                 0, 16, 1 << 30, 0),                             # GPTQ H % 32
     lambda m: m.moe_combine(16, 0, 16, 16, 16, 4, 100, 2, 64, 0, 0),             # H % 8
     lambda m: m.moe_lora_grouped_down(m.MoeExpertRoute(16, 16, 16, 4, 64, 128, 65), 16, 16, 16, 16, None, 16,
                                       0, 64, 0, 8, 2, 0),                       # rank > MAX

@@ -155,6 +155,10 @@ LAYER_CASES = {
                                          wfmt="gptq", router="normal", group_size=64),
     "nvfp4_f16_prefill": synth.MoeConfig("nvfp4_f16_prefill", T=300, H=320, I=192, E=2, k=1, bs=16, act="f16",
                                          wfmt="nvfp4", router="normal"),
+    # decode form with fewer tiles than SMs: tiles cut into k pieces summed by
+    # their owner CTA, with ragged contractions (H=1000, I=520: last k blocks of
+    # 40 and 8) and ragged last column tiles
+    "splitk_ragged_k": synth.MoeConfig("splitk_ragged_k", T=6, H=1000, I=520, E=4, k=2, bs=16, router="normal"),
 }
 
 
@@ -170,6 +174,8 @@ def test_layer_steps_match_oracle(dev, name):
     al = orc.align_block_size(ref_ids.reshape(-1), cfg.E, cfg.bs, lay.max_padded)
     check_route_align_exact(g, ref_ids, ref_w, al)
     assert g["err"] == 0, f"device error word {g['err']:#x}"
+    # the split-K flags (the last 4 KB of each GEMM workspace) are left zero
+    assert not lay.gate_up_ws[-4096:].any() and not lay.down_ws[-4096:].any()
     P = cfg.P
     rows = valid_rows(al.sorted_token_ids, al.total_tokens_post_pad, P)
     # gate/up (+ silu*up) from the same x
@@ -199,6 +205,25 @@ def test_layer_steps_match_oracle(dev, name):
         ex = np.searchsorted(al.expert_offsets, rows, side="right") - 1
         odd = rows[ex % 2 == 1]
         assert np.array_equal(L.act_numpy(lay.y, cfg.act)[odd], g["y_bits"][odd])
+
+
+@pytest.mark.parametrize("name", ["fine_grained@T1", "fine_grained@T64", "splitk_ragged_k"])
+def test_split_k_repeatable(dev, name):
+    """Decode launches that cut tiles across CTAs: each run leaves the split-K
+    flags zero, so back-to-back runs give the same bits (the owner adds the
+    partial sums in a fixed order)."""
+    import torch
+    cfg = LAYER_CASES[name]
+    inp = synth.make_inputs(cfg)
+    lay, x, logits = gpu_layer(cfg, inp, dev)
+    first = [t.clone() for t in (lay.h, lay.y, lay.out)]
+    for _ in range(3):
+        lay.forward(x, logits)
+    torch.cuda.synchronize()
+    assert int(lay.err.item()) == 0
+    for a, b in zip(first, (lay.h, lay.y, lay.out)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert not lay.gate_up_ws[-4096:].any() and not lay.down_ws[-4096:].any()
 
 
 @pytest.mark.parametrize("name", ["tiny", "fine_grained@T64", "gptq@T16", "nvfp4_lora@T2048", "skewed"])
@@ -278,7 +303,7 @@ def test_gemm_rejects_bad_offsets_on_device(dev, name):
     lay.err.zero_()
     y_before = lay.y.clone()
     moe.moe_grouped_down(lay.h, lay.act_code, lay.w_down.desc, lay.sorted_token_ids, bad, cfg.T, cfg.k, cfg.H, cfg.I,
-                         cfg.E, cfg.bs, lay.max_padded, lay.y, lay.err)
+                         cfg.E, cfg.bs, lay.max_padded, lay.y, lay.err, lay.down_ws, lay.down_ws_bytes)
     torch.cuda.synchronize()
     assert int(lay.err.item()) & moe.MOE_DEV_ERR_OFFSETS
     assert torch.equal(lay.y.view(torch.int16), y_before.view(torch.int16))
