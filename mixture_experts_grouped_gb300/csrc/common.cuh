@@ -45,6 +45,11 @@ int make_tmap_2d_raw(CUtensorMap* map, const void* base, CUtensorMapDataType dt,
 // byte strides s1 (between d1 steps) and s2 (between d2 steps), box
 // b0 x b1 x b2. Used to fetch two separated halves of a weight tile with one
 // copy.
+// Encode a 5-D bf16/fp16 tensor map with the 128-byte swizzle: dims d[0]
+// (contiguous; a box of 64 elements = 128 bytes) to d[4], byte strides st of
+// dims 1..4, box b.
+int make_tmap_5d(CUtensorMap* map, const void* base, int act, const uint64_t (&d)[5], const uint64_t (&st)[4],
+                 const uint32_t (&b)[5]);
 int make_tmap_3d_raw(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t d0,
                      uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2);
 
@@ -232,6 +237,14 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_5d_pair(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                                 int32_t c2, int32_t c3, int32_t c4, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar_cluster)
         : "memory");
 }
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2,

@@ -729,16 +729,77 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
 // MMAs; both CTAs' TMA loads complete on the leader's full barrier; the
 // leader's commits arrive on both CTAs' barriers; the follower's epilogue
 // warps release the accumulator through the leader's barrier.
+//
+// The last row tile of an expert's span holds span mod 256 rows. When it
+// holds 128 rows or fewer, the tile runs with the operands swapped: the 256
+// weight rows are the M=256 operand (128 per CTA) and the tile's rows the N
+// operand (N = rows rounded up to 16, N/2 per CTA), so the tensor cores do
+// not spend a 256-row MMA on a 64-row tail (about 1/7 of all rows processed
+// on a Mixtral-shaped batch). For gate/up each CTA then takes 64 gate and the
+// 64 up rows of the same output columns, interleaved in groups of 8 by one
+// 5-D TMA copy, so the SiLU pairs TMEM lane j with lane j + 8.
+// Epilogue of a swapped pair tile for the calling warp: TMEM lanes 32q..32q+31
+// of this CTA are weight rows, columns 0..N-1 the tile's rows (tokens).
+//   gate/up: lane j holds, for output column n0 + 64 rank + 16 q + 8 (j >> 4) +
+//   (j & 7), the gate sums if (j & 8) == 0 and the up sums otherwise;
+//   down: lane j is output column n0 + 128 rank + 32 q + j.
+// Each 16-row chunk goes through the warp's staging area and leaves as 16-byte
+// stores of 8 columns.
+template <int MODE>
+__device__ __forceinline__ void pair_swapped_epilogue(const GemmParams& p, uint32_t ta, __nv_bfloat16* stg,
+                                                      const TileInfo& t, int nvalid, int rank, int q, int lane) {
+    using A = Act<MOE_ACT_BF16>;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 1
+    for (int c = 0; c < nvalid; c += 16) {
+        uint32_t u[16];
+        tmem_ld16(ta + c, u);
+        tmem_ld_wait();
+        if (MODE == MODE_GATE_UP) {
+            const bool gate = (lane & 8) == 0;
+            const int cl = 8 * (lane >> 4) + (lane & 7);  // column within the warp's 16
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float g = __uint_as_float(u[j]);
+                const float up = __shfl_down_sync(0xffffffffu, g, 8);
+                if (gate) stg[j * 16 + cl] = A::from_f(silu_mul(g, up));
+            }
+            __syncwarp();
+            // [16 rows][16 columns]: 32 pieces of 8 columns, one per lane
+            const int r = lane >> 1, pq = lane & 1;
+            const int col = t.n0 + 64 * rank + 16 * q + 8 * pq;
+            if (c + r < nvalid && col < p.n_out)
+                *reinterpret_cast<uint4*>(out + static_cast<size_t>(t.m0 + c + r) * p.n_out + col) =
+                    *reinterpret_cast<const uint4*>(stg + r * 16 + pq * 8);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) stg[j * 32 + lane] = A::from_f(__uint_as_float(u[j]));
+            __syncwarp();
+            // [16 rows][32 columns]: 64 pieces of 8 columns, two per lane
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int pc = i * 32 + lane, r = pc >> 2, pq = pc & 3;
+                const int col = t.n0 + 128 * rank + 32 * q + 8 * pq;
+                if (c + r < nvalid && col < p.n_out)
+                    *reinterpret_cast<uint4*>(out + static_cast<size_t>(t.m0 + c + r) * p.n_out + col) =
+                        *reinterpret_cast<const uint4*>(stg + r * 32 + pq * 8);
+            }
+        }
+        __syncwarp();
+    }
+}
+
 constexpr int PAIR_STAGES = 6;
 constexpr int PAIR_A = 128 * BK * 2;  // this CTA's 128 activation rows
 constexpr int PAIR_B = 128 * BK * 2;  // this CTA's half of the weight tile
-constexpr int PAIR_SMEM = 1024 + PAIR_STAGES * (PAIR_A + PAIR_B) + TAIL_BYTES;
+constexpr int PAIR_STG = NUM_EPI_WARPS * 16 * 32 * 2;  // swapped epilogue: per warp 16 rows x 32 columns
+constexpr int PAIR_SMEM = 1024 + PAIR_STAGES * (PAIR_A + PAIR_B) + PAIR_STG + TAIL_BYTES;
 static_assert(PAIR_SMEM <= SMEM_LIMIT, "pair kernel shared memory over the limit");
 
 template <int MODE>
 __global__ void __launch_bounds__(192, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                         const GemmParams p) {
+                         const __grid_constant__ CUtensorMap tmW5, const GemmParams p) {
     constexpr int ACT = MOE_ACT_BF16;
     constexpr int XROWS = 256;
     constexpr int OUT_COLS = MODE == MODE_GATE_UP ? 128 : 256;
@@ -746,7 +807,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
     uint8_t* smem = align1024_shared(smem_raw);
     uint8_t* sA = smem;
     uint8_t* sB = smem + PAIR_STAGES * PAIR_A;
-    SmemTail& s = *reinterpret_cast<SmemTail*>(sB + PAIR_STAGES * PAIR_B);
+    uint8_t* sStg = sB + PAIR_STAGES * PAIR_B;
+    SmemTail& s = *reinterpret_cast<SmemTail*>(sStg + PAIR_STG);
     volatile int* abort_flag = &s.abort_flag;
 
     const int tid = threadIdx.x;
@@ -780,6 +842,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmX);
         tma_prefetch_desc(&tmW);
+        if (MODE == MODE_GATE_UP) tma_prefetch_desc(&tmW5);
     }
     tc_fence_before();
     cluster_sync_all();  // both CTAs' barriers initialised and TMEM allocated
@@ -801,13 +864,21 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
                 int c0, c1;
                 half_bases<MODE>(p, t.n0, c0, c1);
                 const int wrow = t.e * p.n_w + (rank == 0 ? c0 : c1);
-                const int arow = t.m0 + static_cast<int>(rank) * 128;
+                // swapped tail: this CTA holds rows [m0 + rank * N/2, +N/2) (the 128-row box
+                // over-fetches; the MMA reads N/2 of them)
+                const bool swapped = t.rows <= 128;
+                const int arow = t.m0 + static_cast<int>(rank) * (swapped ? ((t.rows + 15) & ~15) / 2 : 128);
+                // gate/up swapped: 8-row groups of gate and up rows for output columns
+                // [n0 + 64 * rank, +64): group coordinate (n0 + 64 * rank) / 8
+                const bool w5 = MODE == MODE_GATE_UP && swapped;
+                const int g5 = t.n0 / 8 + 8 * static_cast<int>(rank);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
                     if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2 * (PAIR_A + PAIR_B));
                     const uint32_t bar = leader_full0 + stage * 8;
                     tma_load_2d_pair(sA + stage * PAIR_A, &tmX, kb * BK, arow, bar);
-                    tma_load_2d_pair(sB + stage * PAIR_B, &tmW, kb * BK, wrow, bar);
+                    if (w5) tma_load_5d_pair(sB + stage * PAIR_B, &tmW5, kb * BK, 0, 0, g5, t.e, bar);
+                    else tma_load_2d_pair(sB + stage * PAIR_B, &tmW, kb * BK, wrow, bar);
                     ++issued;
                     if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -835,13 +906,22 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
                 if (!mbar_wait(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * 256;
+                const bool swapped = t.rows <= 128;
+                const uint32_t idesc_sw = f16_idesc(ACT, 256, (t.rows + 15) & ~15);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&s.full[stage], phase, abort_flag, p.err)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t ad = sw128_desc(smem_u32(sA + stage * PAIR_A));
                     const uint64_t bd = sw128_desc(smem_u32(sB + stage * PAIR_B));
+                    if (swapped) {  // D = weight rows x tile rows
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) tc_mma_pair(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                        for (int k = 0; k < BK / 16; ++k)
+                            tc_mma_pair(d, bd + 2 * k, ad + 2 * k, idesc_sw, (kb | k) != 0);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k)
+                            tc_mma_pair(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                    }
                     tc_commit_pair(&s.empty[stage], 0x3);
                     if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -856,6 +936,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
         // ---------------- epilogue (both CTAs, each its own 128 rows) ----------------
         const int q = warp & 3;
         const int lrow = q * 32 + lane;
+        __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(sStg) + (warp - 2) * (16 * 32);
         int local = 0;
         for (int tile = pair; tile < n_tiles; tile += npairs) {
             const TileInfo t = decode_tile<XROWS>(s, E, tile, OUT_COLS);
@@ -870,7 +951,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
             const bool row_ok = row < nvalid;
             const size_t orow = static_cast<size_t>(t.m0 + row) * p.n_out;
             const uint32_t ta = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 256;
-            if (MODE == MODE_GATE_UP) {
+            if (t.rows <= 128) {
+                // swapped tail: lane = weight row, TMEM columns = the tile's rows
+                pair_swapped_epilogue<MODE>(p, ta, stg, t, nvalid, static_cast<int>(rank), q, lane);
+            } else if (MODE == MODE_GATE_UP) {
 #pragma unroll 1
                 for (int c = 0; c < 128; c += 32) {
                     uint32_t g[32], u[32];
@@ -1474,7 +1558,7 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sort
 // ---- host side -------------------------------------------------------------------
 
 struct Maps {
-    CUtensorMap x, w, r0, r1, r2;
+    CUtensorMap x, w, w5, r0, r1, r2;  // w5: gate/up rows interleaved by 8 (bf16 pair form)
 };
 
 // Activation rows per tile. 0 selects the prefill form (128 rows as the MMA's
@@ -1606,7 +1690,7 @@ int launch_pair(const Maps& m, const GemmParams& p, cudaStream_t st, const char*
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
     GemmParams q = p;
     q.pad_free = 256 % p.block_size == 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, m.x, m.w, q);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, m.x, m.w, m.w5, q);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
     count_launch();
     return check_launch(who);
@@ -1640,6 +1724,17 @@ int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Map
             MOE_REQUIRE(w->w != nullptr, "%s: NULL bf16 weight", who);
             int rc = make_tmap_2d(&m.w, w->w, static_cast<uint64_t>(E) * N, K, 128, act);
             if (rc != MOE_OK) return rc;
+            m.w5 = m.w;
+            if (N == 2 * n_out) {
+                // gate/up rows as (k, 8 rows, gate | up, 8-row group, expert): one copy
+                // brings 64 gate rows and the 64 up rows of the same columns, by 8
+                const uint64_t I = static_cast<uint64_t>(n_out), row = static_cast<uint64_t>(K) * 2;
+                const uint64_t d[5] = {static_cast<uint64_t>(K), 8, 2, I / 8, static_cast<uint64_t>(E)};
+                const uint64_t st[4] = {row, I * row, 8 * row, 2 * I * row};
+                const uint32_t b[5] = {64, 8, 2, 8, 1};
+                rc = make_tmap_5d(&m.w5, w->w, act, d, st, b);
+                if (rc != MOE_OK) return rc;
+            }
             m.r0 = m.r1 = m.r2 = m.w;
             return MOE_OK;
         }

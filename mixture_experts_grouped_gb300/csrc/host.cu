@@ -111,6 +111,25 @@ int make_tmap_2d_raw(CUtensorMap* map, const void* base, CUtensorMapDataType dt,
     return MOE_OK;
 }
 
+int make_tmap_5d(CUtensorMap* map, const void* base, int act, const uint64_t (&d)[5], const uint64_t (&st)[4],
+                 const uint32_t (&b)[5]) {
+    auto fn = encode_fn();
+    if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    if (!aligned16(base)) return fail(MOE_ERR_INVALID, "tensor base address %p is not 16-byte aligned", base);
+    for (int i = 0; i < 4; ++i)
+        if (st[i] % 16 != 0)
+            return fail(MOE_ERR_INVALID, "tensor stride %llu is not a 16-byte multiple", (unsigned long long)st[i]);
+    cuuint64_t dims[5] = {d[0], d[1], d[2], d[3], d[4]};
+    cuuint64_t strides[4] = {st[0], st[1], st[2], st[3]};
+    cuuint32_t box[5] = {b[0], b[1], b[2], b[3], b[4]};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(map, act == MOE_ACT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MOE_ERR_INVALID, "cuTensorMapEncodeTiled failed (%d) for a 5-D map", (int)r);
+    return MOE_OK;
+}
+
 int make_tmap_3d_raw(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t d0,
                      uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
     auto fn = encode_fn();
