@@ -36,6 +36,7 @@ inline int n_chunks(int P) { return (P + kChunk - 1) / kChunk; }
 __global__ void __launch_bounds__(32 * kWarps)
 align_count_rank_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ chunk_counts,
                         int32_t* __restrict__ rank_in_chunk, int32_t* err) {
+    pdl_wait();
     __shared__ int cnt[kWarps][MOE_MAX_EXPERTS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < kWarps * MOE_MAX_EXPERTS; i += blockDim.x) (&cnt[0][0])[i] = 0;
@@ -89,6 +90,7 @@ __global__ void __launch_bounds__(MOE_MAX_EXPERTS)
 align_scan_kernel(int P, int E, int bs, int max_padded, int nchunks, int32_t* __restrict__ chunk_counts,
                   int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
                   int32_t* __restrict__ offsets, int32_t* __restrict__ total_post_pad, int32_t* err) {
+    pdl_wait();
     __shared__ int s_span[MOE_MAX_EXPERTS];
     __shared__ int s_total;
     const int e = threadIdx.x;
@@ -136,6 +138,7 @@ align_scan_kernel(int P, int E, int bs, int max_padded, int nchunks, int32_t* __
 __global__ void align_scatter_kernel(const int32_t* __restrict__ ids, int P, int E,
                                      const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ rank_in_chunk,
                                      int32_t* __restrict__ sorted_ids, int32_t* __restrict__ pair_to_row) {
+    pdl_wait();
     const int p = blockIdx.x * blockDim.x + threadIdx.x;
     if (p >= P) return;
     const int id = ids[p];
@@ -155,6 +158,7 @@ align_single_block_kernel(const int32_t* __restrict__ ids, int P, int E, int bs,
                           int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
                           int32_t* __restrict__ offsets, int32_t* __restrict__ total_post_pad,
                           int32_t* __restrict__ pair_to_row, int32_t* err) {
+    pdl_wait();
     __shared__ int cnt[kWarps][MOE_MAX_EXPERTS];
     __shared__ int s_span[MOE_MAX_EXPERTS];
     __shared__ int s_off[MOE_MAX_EXPERTS];
@@ -282,17 +286,17 @@ extern "C" int moe_align_block_size(const int32_t* topk_ids, int32_t P, int32_t 
         static_cast<char*>(workspace) + (static_cast<size_t>(nchunks) * E * sizeof(int32_t) + 255) / 256 * 256);
     int launches = 0;
     if (nchunks <= 1) {
-        moe::align_single_block_kernel<<<1, 32 * moe::kWarps, 0, st>>>(topk_ids, P, E, block_size, max_padded,
+        moe::launch_pdl(moe::align_single_block_kernel, 1, 32 * moe::kWarps, 0, st, topk_ids, P, E, block_size, max_padded,
                                                                       sorted_token_ids, expert_ids, expert_offsets,
                                                                       total_tokens_post_pad, pair_to_row, err_word);
         ++launches;
     } else {
-        moe::align_count_rank_kernel<<<nchunks, 32 * moe::kWarps, 0, st>>>(topk_ids, P, E, chunk_counts,
+        moe::launch_pdl(moe::align_count_rank_kernel, nchunks, 32 * moe::kWarps, 0, st, topk_ids, P, E, chunk_counts,
                                                                           rank_in_chunk, err_word);
-        moe::align_scan_kernel<<<1, MOE_MAX_EXPERTS, 0, st>>>(P, E, block_size, max_padded, nchunks, chunk_counts,
+        moe::launch_pdl(moe::align_scan_kernel, 1, MOE_MAX_EXPERTS, 0, st, P, E, block_size, max_padded, nchunks, chunk_counts,
                                                              sorted_token_ids, expert_ids, expert_offsets,
                                                              total_tokens_post_pad, err_word);
-        moe::align_scatter_kernel<<<(P + 255) / 256, 256, 0, st>>>(topk_ids, P, E, chunk_counts, rank_in_chunk,
+        moe::launch_pdl(moe::align_scatter_kernel, (P + 255) / 256, 256, 0, st, topk_ids, P, E, chunk_counts, rank_in_chunk,
                                                                   sorted_token_ids, pair_to_row);
         launches += 3;
     }

@@ -16,6 +16,7 @@ template <int ACT>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ pair_to_row, const float* __restrict__ w,
                uint4* __restrict__ out, int H, int top_k, int max_padded, int32_t* err) {
+    pdl_wait();
     const int t = blockIdx.y;
     const int v = blockIdx.x * kThreads + threadIdx.x;  // 16-byte vector index in the row
     const int vpr = H / 8;
@@ -75,10 +76,10 @@ extern "C" int moe_combine(const void* y, int32_t act, const int32_t* pair_to_ro
         const int32_t* pr = pair_to_row + static_cast<size_t>(t0) * top_k;
         const float* wt = topk_weights + static_cast<size_t>(t0) * top_k;
         if (act == MOE_ACT_BF16)
-            moe::combine_kernel<MOE_ACT_BF16><<<grid, moe::kThreads, 0, st>>>(yv, pr, wt, ov, H, top_k, max_padded,
+            moe::launch_pdl(moe::combine_kernel<MOE_ACT_BF16>, grid, moe::kThreads, 0, st, yv, pr, wt, ov, H, top_k, max_padded,
                                                                              err_word);
         else
-            moe::combine_kernel<MOE_ACT_F16><<<grid, moe::kThreads, 0, st>>>(yv, pr, wt, ov, H, top_k, max_padded,
+            moe::launch_pdl(moe::combine_kernel<MOE_ACT_F16>, grid, moe::kThreads, 0, st, yv, pr, wt, ov, H, top_k, max_padded,
                                                                             err_word);
         ++launches;
     }

@@ -551,6 +551,7 @@ template <int MODE, int NTOK>
 __global__ void __launch_bounds__(DecodeShape<MODE, NTOK>::THREADS, 1)
 grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                            const GemmParams p) {
+    pdl_wait();
     using S = DecodeShape<MODE, NTOK>;
     constexpr int ACT = MOE_ACT_BF16;
     constexpr int XROWS = NTOK, STAGES = S::STAGES;
@@ -800,6 +801,7 @@ template <int MODE>
 __global__ void __launch_bounds__(192, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                          const __grid_constant__ CUtensorMap tmW5, const GemmParams p) {
+    pdl_wait();
     constexpr int ACT = MOE_ACT_BF16;
     constexpr int XROWS = 256;
     constexpr int OUT_COLS = MODE == MODE_GATE_UP ? 128 : 256;
@@ -1222,6 +1224,7 @@ __global__ void __launch_bounds__(TsShape<MODE, WFMT, ACT, NTOK>::THREADS, 1)
 grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmR0,
                        const __grid_constant__ CUtensorMap tmR1, const __grid_constant__ CUtensorMap tmR2,
                        const GemmParams p) {
+    pdl_wait();
     using S = TsShape<MODE, WFMT, ACT, NTOK>;
     constexpr int XROWS = NTOK, XSTAGES = S::XSTAGES, ASTAGES = TS_STAGES, RSTAGES = S::RSTAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -1538,6 +1541,8 @@ __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_ids,
                    const int32_t* __restrict__ offsets, int E, int T, int top_k, int vec_per_row, int max_padded,
                    int perm, uint4* __restrict__ xs, int32_t* err) {
+    pdl_wait();
+    pdl_launch_next();
     const int total = min(__ldg(offsets + E), max_padded);
     const int P = T * top_k;
     for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < total; r += gridDim.x * 8) {
@@ -1601,7 +1606,7 @@ int launch_decode(const Maps& m, const GemmParams& p, cudaStream_t st, const cha
     if (2L * grid * KB * grid >= (1L << 31)) return fail(MOE_ERR_UNSUPPORTED, "%s: contraction too long", who);
     GemmParams q = p;
     q.pad_free = NTOK % p.block_size == 0;
-    kernel<<<grid, S::THREADS, S::SMEM, st>>>(m.x, m.w, q);
+    moe::launch_pdl(kernel, grid, S::THREADS, S::SMEM, st, m.x, m.w, q);
     count_launch();
     return check_launch(who);
 }
@@ -1637,7 +1642,7 @@ int launch_ts(const Maps& m, const GemmParams& p, cudaStream_t st, const char* w
     if (grid <= 0) return MOE_OK;
     GemmParams q = p;
     q.pad_free = NTOK % p.block_size == 0;
-    kernel<<<grid, S::THREADS, S::SMEM, st>>>(m.x, m.r0, m.r1, m.r2, q);
+    moe::launch_pdl(kernel, grid, S::THREADS, S::SMEM, st, m.x, m.r0, m.r1, m.r2, q);
     count_launch();
     return check_launch(who);
 }
@@ -1661,7 +1666,7 @@ int launch_pair(const Maps& m, const GemmParams& p, cudaStream_t st, const char*
     int dev = 0;
     cudaGetDevice(&dev);
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
@@ -1688,6 +1693,10 @@ int launch_pair(const Maps& m, const GemmParams& p, cudaStream_t st, const char*
     const long pairs = bound < max_pairs ? bound : max_pairs;
     if (pairs <= 0) return MOE_OK;
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    // programmatic dependent launch, as for every kernel of the library (launch_pdl)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     GemmParams q = p;
     q.pad_free = 256 % p.block_size == 0;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, m.x, m.w, m.w5, q);
@@ -1855,7 +1864,7 @@ extern "C" int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* 
         int blocks = (max_padded + 7) / 8;
         const int cap = sms > 0 ? sms * 8 : 1024;
         if (blocks > cap) blocks = cap;
-        moe::gather_rows_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(x), sorted_token_ids,
+        moe::launch_pdl(moe::gather_rows_kernel, blocks, 256, 0, st, static_cast<const uint4*>(x), sorted_token_ids,
                                                         expert_offsets, E, T, top_k, H / 8, max_padded,
                                                         w_gate_up->format == MOE_W_GPTQ_INT4 ? 1 : 0,
                                                         static_cast<uint4*>(workspace), err_word);

@@ -100,6 +100,7 @@ lora_shrink_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restric
                    const uint64_t* __restrict__ a_table, __nv_bfloat16* __restrict__ xa, int n_experts, int max_rank,
                    int k_in, uint32_t x_gather, uint32_t row_offset, uint32_t row_end, int P, int top_k,
                    int32_t* err) {
+    pdl_wait();
     extern __shared__ __align__(16) uint8_t smem[];
     LoraTiles& s = *reinterpret_cast<LoraTiles*>(smem);
     __nv_bfloat16* sA = reinterpret_cast<__nv_bfloat16*>(smem + ((sizeof(LoraTiles) + 15) / 16) * 16);
@@ -172,6 +173,7 @@ lora_expand_fold_kernel(const __nv_bfloat16* __restrict__ xa, const int32_t* __r
                         const uint64_t* __restrict__ b_table, const float* __restrict__ scale_table,
                         __nv_bfloat16* __restrict__ base, int n_experts, int n_out, int max_rank, uint32_t row_offset,
                         uint32_t row_end, int P, int top_k, const uint64_t* __restrict__ a_table) {
+    pdl_wait();
     constexpr int CPC = 64 / RCAP;
     __shared__ LoraTiles s;
     __shared__ int s_src[kRowTile];
@@ -264,7 +266,7 @@ extern "C" int moe_lora_grouped_down(const MoeExpertRoute* route, const void* x,
         if (rc != MOE_OK) return rc;
         configured_for = dev;
     }
-    moe::lora_shrink_kernel<<<grid, 32 * moe::kShrinkWarps, shrink_smem, st>>>(
+    moe::launch_pdl(moe::lora_shrink_kernel, grid, 32 * moe::kShrinkWarps, shrink_smem, st,
         static_cast<const __nv_bfloat16*>(x), expert_offsets, sorted_token_ids, row_adapter, route->a_table,
         static_cast<__nv_bfloat16*>(xa), route->n_experts, route->max_rank, route->k_in, x_gather, row_offset,
         row_end, P, top_k, nullptr);
@@ -274,15 +276,15 @@ extern "C" int moe_lora_grouped_down(const MoeExpertRoute* route, const void* x,
     const auto* xa_p = static_cast<const __nv_bfloat16*>(xa);
     auto* base_p = static_cast<__nv_bfloat16*>(base_out);
     if (route->max_rank <= 16)
-        moe::lora_expand_fold_kernel<16><<<grid, moe::kExpandThreads, 0, st>>>(
+        moe::launch_pdl(moe::lora_expand_fold_kernel<16>, grid, moe::kExpandThreads, 0, st,
             xa_p, expert_offsets, sorted_token_ids, row_adapter, route->b_table, route->scale_table, base_p,
             route->n_experts, route->n_out, route->max_rank, row_offset, row_end, P, top_k, route->a_table);
     else if (route->max_rank <= 32)
-        moe::lora_expand_fold_kernel<32><<<grid, moe::kExpandThreads, 0, st>>>(
+        moe::launch_pdl(moe::lora_expand_fold_kernel<32>, grid, moe::kExpandThreads, 0, st,
             xa_p, expert_offsets, sorted_token_ids, row_adapter, route->b_table, route->scale_table, base_p,
             route->n_experts, route->n_out, route->max_rank, row_offset, row_end, P, top_k, route->a_table);
     else
-        moe::lora_expand_fold_kernel<64><<<grid, moe::kExpandThreads, 0, st>>>(
+        moe::launch_pdl(moe::lora_expand_fold_kernel<64>, grid, moe::kExpandThreads, 0, st,
             xa_p, expert_offsets, sorted_token_ids, row_adapter, route->b_table, route->scale_table, base_p,
             route->n_experts, route->n_out, route->max_rank, row_offset, row_end, P, top_k, route->a_table);
     moe::count_launch();

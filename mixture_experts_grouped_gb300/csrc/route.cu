@@ -23,6 +23,7 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
 __global__ void __launch_bounds__(32 * kRowsPerBlock)
 route_topk_softmax_kernel(const float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ w, int T,
                           int E, int k, int renorm) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
     if (row >= T) return;
@@ -120,7 +121,7 @@ extern "C" int moe_route_topk_softmax(const float* logits, int32_t* topk_ids, fl
     if (T == 0) return MOE_OK;
     MOE_REQUIRE(logits && topk_ids && topk_weights, "moe_route_topk_softmax: NULL pointer");
     const int blocks = (T + moe::kRowsPerBlock - 1) / moe::kRowsPerBlock;
-    moe::route_topk_softmax_kernel<<<blocks, 32 * moe::kRowsPerBlock, 0, static_cast<cudaStream_t>(stream)>>>(
+    moe::launch_pdl(moe::route_topk_softmax_kernel, blocks, 32 * moe::kRowsPerBlock, 0, static_cast<cudaStream_t>(stream),
         logits, topk_ids, topk_weights, T, E, top_k, renormalize ? 1 : 0);
     moe::count_launch();
     return moe::check_launch("moe_route_topk_softmax");
