@@ -40,7 +40,7 @@ __all__ = [
     "align_block_size", "AlignResult", "ensure_group_arrays", "GroupArrayError",
     "e2m1_value", "e4m3_value", "dequant_bf16", "dequant_gptq", "dequant_nvfp4",
     "expert_weight", "prepare_f64", "grouped_gate_up", "grouped_down", "lora_grouped_down",
-    "combine", "moe_layer", "LayerResult",
+    "lora_gather_bgmv", "gather_bgmv_grids", "combine", "moe_layer", "LayerResult",
 ]
 
 # ----------------------------------------------------------------------------
@@ -529,6 +529,64 @@ def lora_grouped_down(x: np.ndarray, base_out: np.ndarray, lora_a: dict, lora_b:
             acc = (bf16_bits_to_f64(base[r]).astype(np.float32) + prod).astype(np.float32)
             base[r] = f64_to_bf16_bits(acc.astype(np.float64))
     return base, xa_out
+
+
+def lora_gather_bgmv(x: np.ndarray, base_out: np.ndarray, lora_a: dict, lora_b: dict,
+                     scale: np.ndarray, n_experts: int, indices: np.ndarray, top_k: int,
+                     row_adapter: Optional[np.ndarray], x_gather: int = 0,
+                     xa: Optional[np.ndarray] = None):
+    """Decode-path LoRA fold on slot-major rows ([lora] ``moe_lora_gather_bgmv``
+    doc and launcher, ``gather_row_token``).
+
+    The rows are the flat ``(token, slot)`` pairs ``s = t * top_k + j``, in that
+    order, ``n_slots = indices.shape[0]`` of them (no expert sort, no padding).
+    Row s takes its expert from ``indices[s]`` and its adapt decision from
+    ``row_adapter[s // top_k]`` (``< 0``: the row is left alone; ``None``: every
+    row folds). A row whose expert is ``>= n_experts`` or has no adapter is left
+    alone too. The input row is ``x[s]`` (``x_gather = 0``: slot-major
+    ``[n_slots, k_in]``, the down fold) or ``x[s // top_k]`` (``x_gather = 1``:
+    token-major, the gate/up fold). Per folded row the arithmetic is that of
+    :func:`lora_grouped_down`:
+
+    * ``xa[s, j] = bf16(sum_i x_row[i] * A_e[j, i])``;
+    * ``delta[n] = bf16(sum_j xa[s, j] * B_e[n, j])``;
+    * ``base[s, n] = bf16(fp32(base[s, n]) + fp32(scale_e * fp32(delta[n])))``.
+
+    Returns ``(new_base_bits, xa_bits)``; ``xa`` rows of rows left alone keep
+    their input value (zeros if ``xa`` is None).
+    """
+    base = np.array(base_out, dtype=np.uint16, copy=True)
+    xs = bf16_bits_to_f64(x)
+    idx = np.asarray(indices).astype(np.int64)
+    rank = next(iter(lora_a.values())).shape[0] if lora_a else 0
+    xa_out = (np.zeros((idx.shape[0], rank), dtype=np.uint16) if xa is None
+              else np.array(xa, dtype=np.uint16, copy=True))
+    for s in range(idx.shape[0]):
+        e = int(idx[s])
+        if e >= n_experts or e not in lora_a:
+            continue
+        tok = s // top_k
+        if row_adapter is not None and int(row_adapter[tok]) < 0:
+            continue
+        A = bf16_bits_to_f64(lora_a[e])                      # [rank, k_in]
+        B = bf16_bits_to_f64(lora_b[e])                      # [n_out, rank]
+        xr = xs[s] if x_gather == 0 else xs[tok]
+        xa_row = round_to_bf16(A @ xr)
+        xa_out[s] = f64_to_bf16_bits(xa_row)
+        delta = round_to_bf16(B @ xa_row)
+        prod = (np.float32(scale[e]) * delta.astype(np.float32)).astype(np.float32)
+        acc = (bf16_bits_to_f64(base[s]).astype(np.float32) + prod).astype(np.float32)
+        base[s] = f64_to_bf16_bits(acc.astype(np.float64))
+    return base, xa_out
+
+
+def gather_bgmv_grids(max_rank: int, n_out: int, n_slots: int):
+    """The page's exact launch grids of the decode fold ([lora]
+    ``gather_bgmv_grids``): ``([ceil(max_rank/4), n_slots, 1], [ceil(n_out/4),
+    n_slots, 1])`` for the shrink and the expand, four outputs per 256-thread
+    block. Kept as the record of the page's shape; the CUDA kernels size their
+    own grids."""
+    return ([-(-max_rank // 4), n_slots, 1], [-(-n_out // 4), n_slots, 1])
 
 
 # ----------------------------------------------------------------------------

@@ -156,3 +156,91 @@ def test_fold_step_rounds_in_f32_without_fma():
     out, _ = orc.lora_grouped_down(x, base, A, B, np.array([3.0], np.float32), 1, off, sorted_ids, 1, 1,
                                    None, 0, 1)
     assert orc.bf16_bits_to_f64(out)[0, 0] == 1.0078125
+
+
+# ---------------------------------------------------------------------------
+# decode gather fold (slot-major rows)
+# ---------------------------------------------------------------------------
+
+def _slot_setup(seed=5):
+    cfg, inp, res, al, h, y, rows = _setup(seed=seed)
+    rng = np.random.default_rng(seed)
+    n_slots = cfg.P
+    k_in = cfg.I
+    indices = res.ids.reshape(-1).astype(np.uint32)              # expert of slot s = t*k + j
+    p2r = al.pair_to_row
+    base_slot = orc.f64_to_bf16_bits(rng.standard_normal((n_slots, cfg.H)))
+    x_slot = orc.f64_to_bf16_bits(rng.standard_normal((n_slots, k_in)))
+    x_tok = orc.f64_to_bf16_bits(rng.standard_normal((cfg.T, k_in)))
+    return cfg, inp, al, indices, p2r, base_slot, x_slot, x_tok
+
+
+def _sorted_copy(al, slot_rows, n_rows):
+    out = np.zeros((n_rows,) + slot_rows.shape[1:], slot_rows.dtype)
+    out[al.pair_to_row] = slot_rows
+    return out
+
+
+@pytest.mark.parametrize("x_gather", [0, 1])
+def test_gather_fold_equals_sorted_fold_on_the_same_pairs(x_gather):
+    # the slot-major fold of row s is the sorted fold of the row holding pair s
+    cfg, inp, al, indices, p2r, base_slot, x_slot, x_tok = _slot_setup()
+    lora = inp["lora"]
+    n_rows = al.sorted_token_ids.shape[0]
+    base_sorted = _sorted_copy(al, base_slot, n_rows)
+    x = x_slot if x_gather == 0 else x_tok
+    xs = _sorted_copy(al, x_slot, n_rows) if x_gather == 0 else x_tok
+    got, xa = orc.lora_gather_bgmv(x, base_slot, lora["a"], lora["b"], lora["scale"], lora["n_experts"],
+                                   indices, cfg.k, None, x_gather)
+    want, xa_want = orc.lora_grouped_down(xs, base_sorted, lora["a"], lora["b"], lora["scale"], lora["n_experts"],
+                                          al.expert_offsets, al.sorted_token_ids, cfg.P, cfg.k, None, 0,
+                                          al.total_tokens_post_pad, x_gather)
+    np.testing.assert_array_equal(got, want[p2r])
+    np.testing.assert_array_equal(xa, xa_want[p2r])
+    # adapted experts (even) changed their rows, the others did not
+    even = indices % 2 == 0
+    assert np.all(np.any(got[even] != base_slot[even], axis=1))
+    np.testing.assert_array_equal(got[~even], base_slot[~even])
+
+
+def test_gather_fold_row_adapter_is_per_token():
+    cfg, inp, al, indices, p2r, base_slot, x_slot, x_tok = _slot_setup(seed=6)
+    lora = inp["lora"]
+    ra = np.zeros(cfg.T, np.int32)
+    ra[1::2] = -1                                              # odd tokens keep their base rows
+    got, _ = orc.lora_gather_bgmv(x_slot, base_slot, lora["a"], lora["b"], lora["scale"], lora["n_experts"],
+                                  indices, cfg.k, ra, 0)
+    full, _ = orc.lora_gather_bgmv(x_slot, base_slot, lora["a"], lora["b"], lora["scale"], lora["n_experts"],
+                                   indices, cfg.k, None, 0)
+    tok = np.arange(cfg.P) // cfg.k
+    np.testing.assert_array_equal(got[tok % 2 == 1], base_slot[tok % 2 == 1])
+    np.testing.assert_array_equal(got[tok % 2 == 0], full[tok % 2 == 0])
+
+
+def test_gather_fold_skips_experts_past_the_table():
+    cfg, inp, al, indices, p2r, base_slot, x_slot, x_tok = _slot_setup(seed=7)
+    lora = inp["lora"]
+    got, xa = orc.lora_gather_bgmv(x_slot, base_slot, lora["a"], lora["b"], lora["scale"], 2,
+                                   indices, cfg.k, None, 0)
+    keep = indices != 0                                        # only expert 0 is adapted and < 2
+    np.testing.assert_array_equal(got[keep], base_slot[keep])
+    assert not xa[keep].any()
+    assert np.all(np.any(got[~keep] != base_slot[~keep], axis=1))
+
+
+def test_gather_fold_single_row_by_hand():
+    # one slot, rank 1, k_in 2, n_out 2, all values exact in bf16:
+    # xa = 1*2 + 3*(-1) = -1; delta = [-1 * 4, -1 * 0.5] = [-4, -0.5];
+    # base' = base + 2 * delta = [10 - 8, 1 - 1] = [2, 0]
+    b = orc.f64_to_bf16_bits
+    got, xa = orc.lora_gather_bgmv(b(np.array([[1.0, 3.0]])), b(np.array([[10.0, 1.0]])),
+                                   {0: b(np.array([[2.0, -1.0]]))}, {0: b(np.array([[4.0], [0.5]]))},
+                                   np.array([2.0], np.float32), 1, np.array([0], np.uint32), 1, None, 0)
+    np.testing.assert_array_equal(orc.bf16_bits_to_f64(got), [[2.0, 0.0]])
+    np.testing.assert_array_equal(orc.bf16_bits_to_f64(xa), [[-1.0]])
+
+
+def test_gather_bgmv_grids_of_the_page():
+    # four outputs per block along x, one slot per block along y
+    assert orc.gather_bgmv_grids(16, 2048, 64) == ([4, 64, 1], [512, 64, 1])
+    assert orc.gather_bgmv_grids(17, 2050, 1) == ([5, 1, 1], [513, 1, 1])
