@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline time budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fold-only", action="store_true",
+                    help="time the decode LoRA fold (moe_lora_gather_bgmv) alone on the workload's slot-major rows")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -432,6 +434,75 @@ def run_ours(args, cfg, rank, world, local_rank):
     return line
 
 
+def run_fold(args, cfg):
+    """The decode LoRA fold alone: moe_lora_gather_bgmv on the T * top_k
+    slot-major rows of the workload (x = post-SiLU rows [P, I], base = down
+    outputs [P, H]), expert ids from the library's own routing of the
+    workload's logits. Reports algorithmic bytes per launch over the
+    CUDA-event time against the HBM peak."""
+    import numpy as np
+    import torch
+
+    from mixture_experts_grouped_gb300 import build as B
+    from mixture_experts_grouped_gb300 import layer as L
+    from mixture_experts_grouped_gb300 import moe as M
+    from mixture_experts_grouped_gb300 import synth
+
+    if not os.path.exists(M.LIB_PATH):
+        B.build()
+    assert cfg.lora_rank > 0, "--fold-only needs a workload with a LoRA rank"
+    dev = torch.device("cuda", 0)
+    inp = synth.make_inputs(cfg)
+    lora = inp["lora"]
+    dl = L.upload_lora(lora, cfg.I, cfg.H, dev)
+    P = cfg.P
+    logits = torch.from_numpy(inp["logits"]).to(dev)
+    ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+    w = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
+    M.moe_route_topk_softmax(logits, ids, w, cfg.T, cfg.E, cfg.k, cfg.renormalize)
+    g = torch.Generator(device="cpu").manual_seed(0)
+    x = torch.randn((P, cfg.I), generator=g).to(torch.bfloat16).to(dev)
+    base = torch.randn((P, cfg.H), generator=g).to(torch.bfloat16).to(dev)
+    xa = torch.zeros((P, dl.route.max_rank), dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+    e_host = ids.reshape(-1).cpu().numpy()
+    adapted = np.array([e < lora["n_experts"] and e in lora["a"] for e in e_host])
+    F = int(adapted.sum())
+    U = len(set(e_host[adapted].tolist()))
+    r = dl.route.max_rank
+    bytes_per = (F * cfg.I * 2 + U * (r * cfg.I * 2 + cfg.H * r * 2) + F * r * 2 * 2 + F * cfg.H * 2 * 2 + P * 4)
+
+    def launch():
+        M.moe_lora_gather_bgmv(dl.route, x, base, ids, None, xa, P, cfg.k, 0)
+
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    n0 = M.moe_launch_count()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(args.steps):
+        launch()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    launches = M.moe_launch_count() - n0
+    pk, src = peaks()
+    gbs = bytes_per / (ms * 1e-3) / 1e9
+    return {
+        "metric": "decode LoRA fold (moe_lora_gather_bgmv) algorithmic GB/s", "value": round(gbs, 2),
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: n_slots={P} k_in={cfg.I} n_out={cfg.H} rank={r} "
+                               f"folded_rows={F} adapted_experts_touched={U}",
+                   "l2": "back-to-back launches; the fold's working set fits in L2"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gbs / pk["hbm_gbs"], 4), "peak_source": src, "bytes_per_launch": bytes_per},
+        "gpu_launches": launches,
+    }
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -443,7 +514,9 @@ def main():
         kv = dict(item.split("=") for item in args.override.split(","))
         cfg = replace(cfg, name=f"{cfg.name}[{args.override}]",
                       **{k: type(getattr(cfg, k))(v) for k, v in kv.items()})
-    if args.impl == "reference":
+    if args.fold_only:
+        line = run_fold(args, cfg) if rank == 0 else None
+    elif args.impl == "reference":
         line = run_reference(args, cfg, rank, world)
     else:
         if world > 1:

@@ -11,6 +11,7 @@
  *   moe_grouped_gate_up      grouped gate/up GEMM with the SiLU-mul fused
  *   moe_grouped_down         grouped down GEMM
  *   moe_lora_grouped_down    optional per-expert LoRA shrink/expand fold
+ *   moe_lora_gather_bgmv     the same fold on unsorted slot-major rows (decode)
  *   moe_combine              weighted top-k combine
  *
  * Sources the semantics are restated from (cited per call below):
@@ -325,6 +326,30 @@ int moe_lora_grouped_down(const MoeExpertRoute* route, const void* x, void* base
                           const int32_t* row_adapter, void* xa, uint32_t row_offset,
                           uint32_t row_end, uint32_t x_gather, int32_t num_tokens,
                           int32_t top_k, void* stream);
+
+/*
+ * Decode-path LoRA fold on slot-major rows ([lora] moe_lora_gather_bgmv;
+ * argument order kept). The rows are the flat (token, slot) pairs
+ * s = t * top_k + j, s < n_slots, in that order (no expert sort). Row s folds
+ * with expert e = indices[s] when e < route->n_experts, a_table[e] != 0 and
+ * (row_adapter == NULL or row_adapter[s / top_k] >= 0):
+ *     xa[s, j] = bf16( sum_i xrow[i] * A_e[j, i] )
+ *     base_out[s, n] = bf16( f32(base_out[s, n]) + f32(scale_e * f32(bf16( sum_j xa[s, j] * B_e[n, j] ))) )
+ * with xrow = x[s] (x_gather 0: slot-major rows, the down fold) or
+ * x[s / top_k] (x_gather 1: token-major rows, the gate/up fold); the sums
+ * accumulate in f32. Other rows of base_out and xa are left untouched.
+ *   route        host pointer; its tables are device arrays
+ *   x            device bf16 [n_slots, k_in] (x_gather 0) or [n_slots / top_k, k_in]
+ *   base_out     device bf16 [n_slots, n_out], folded in place
+ *   indices      device u32 [n_slots]: expert of each row
+ *   row_adapter  device i32 [n_slots / top_k] or NULL
+ *   xa           device bf16 [n_slots, max_rank] scratch
+ * Requirements: k_in % 8 == 0, n_out % 4 == 0, 1 <= max_rank <=
+ * MOE_MAX_LORA_RANK, top_k >= 1, x 16-byte aligned.
+ */
+int moe_lora_gather_bgmv(const MoeExpertRoute* route, const void* x, void* base_out,
+                         const uint32_t* indices, const int32_t* row_adapter, void* xa,
+                         uint32_t n_slots, uint32_t top_k, uint32_t x_gather, void* stream);
 
 /* ---- a6: combine ------------------------------------------------------------- */
 

@@ -221,6 +221,106 @@ lora_expand_fold_kernel(const __nv_bfloat16* __restrict__ xa, const int32_t* __r
     }
 }
 
+// ---- decode gather fold: slot-major rows --------------------------------------
+//
+// Restates [lora] moe_lora_gather_bgmv: row s = t * top_k + j of the flat
+// (token, slot) rows takes its expert from indices[s] and its adapt decision
+// from row_adapter[s / top_k]; no expert sort. Decode batches have few rows,
+// so a block serves one row: the shrink's eight warps split the rank, the
+// expand's threads split the output columns.
+
+// the expert row s folds with, or -1 when it folds nothing
+__device__ __forceinline__ int gather_row_expert(uint32_t s, const uint32_t* indices, const int32_t* row_adapter,
+                                                 const uint64_t* a_table, uint32_t n_experts, uint32_t top_k) {
+    const uint32_t e = indices[s];
+    if (e >= n_experts || a_table[e] == 0) return -1;
+    if (row_adapter && row_adapter[s / top_k] < 0) return -1;
+    return static_cast<int>(e);
+}
+
+// xa[s, j] = bf16(x_row . A_e[j]) for j < max_rank; warp w takes j = w, w + 8, ...
+__global__ void __launch_bounds__(32 * kShrinkWarps)
+lora_gather_shrink_kernel(const __nv_bfloat16* __restrict__ x, const uint32_t* __restrict__ indices,
+                          const int32_t* __restrict__ row_adapter, const uint64_t* __restrict__ a_table,
+                          __nv_bfloat16* __restrict__ xa, uint32_t n_experts, int max_rank, int k_in,
+                          uint32_t top_k, uint32_t x_gather) {
+    pdl_wait();
+    const uint32_t s = blockIdx.x;
+    const int e = gather_row_expert(s, indices, row_adapter, a_table, n_experts, top_k);
+    if (e < 0) return;  // block-uniform
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int chunks = k_in / 8;
+    const size_t src = x_gather ? s / top_k : s;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + src * k_in);
+    const uint4* A = reinterpret_cast<const uint4*>(a_table[e]);
+    constexpr int JW = MOE_MAX_LORA_RANK / kShrinkWarps;  // outputs per warp at most
+    float acc[JW];
+#pragma unroll
+    for (int i = 0; i < JW; ++i) acc[i] = 0.0f;
+    for (int c = lane; c < chunks; c += 32) {
+        const uint4 xv = __ldg(xr + c);
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int i = 0; i < JW; ++i) {
+            const int j = warp + i * kShrinkWarps;
+            if (j < max_rank) {
+                const uint4 av = __ldg(A + static_cast<size_t>(j) * chunks + c);
+                const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 a2 = Act<MOE_ACT_BF16>::unpack2(aw[q]);
+                    const float2 x2 = Act<MOE_ACT_BF16>::unpack2(xw[q]);
+                    acc[i] = fmaf(x2.x, a2.x, acc[i]);
+                    acc[i] = fmaf(x2.y, a2.y, acc[i]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < JW; ++i) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
+        const int j = warp + i * kShrinkWarps;
+        if (lane == 0 && j < max_rank) xa[static_cast<size_t>(s) * max_rank + j] = __float2bfloat16_rn(acc[i]);
+    }
+}
+
+// base[s, n] = bf16(f32(base[s, n]) + f32(scale_e * bf16(xa[s] . B_e[n]))) for
+// the CPC = 64 / RCAP consecutive columns of each thread (RCAP: rank capacity)
+template <int RCAP>
+__global__ void __launch_bounds__(kExpandThreads)
+lora_gather_expand_fold_kernel(const __nv_bfloat16* __restrict__ xa, const uint32_t* __restrict__ indices,
+                               const int32_t* __restrict__ row_adapter, const uint64_t* __restrict__ a_table,
+                               const uint64_t* __restrict__ b_table, const float* __restrict__ scale_table,
+                               __nv_bfloat16* __restrict__ base, uint32_t n_experts, int n_out, int max_rank,
+                               uint32_t top_k) {
+    pdl_wait();
+    constexpr int CPC = 64 / RCAP;
+    __shared__ float s_xa[RCAP];
+    const uint32_t s = blockIdx.x;
+    const int e = gather_row_expert(s, indices, row_adapter, a_table, n_experts, top_k);
+    if (e < 0) return;  // block-uniform
+    if (threadIdx.x < RCAP)
+        s_xa[threadIdx.x] =
+            threadIdx.x < max_rank ? __bfloat162float(xa[static_cast<size_t>(s) * max_rank + threadIdx.x]) : 0.0f;
+    __syncthreads();
+    const int n0 = (blockIdx.y * kExpandThreads + threadIdx.x) * CPC;
+    if (n0 >= n_out) return;  // n_out % 4 == 0 and CPC divides 4: a thread's columns are all in range
+    const __nv_bfloat16* B = reinterpret_cast<const __nv_bfloat16*>(b_table[e]);
+    const float sc = scale_table[e];
+    __nv_bfloat16* yrow = base + static_cast<size_t>(s) * n_out + n0;
+#pragma unroll
+    for (int i = 0; i < CPC; ++i) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < RCAP; ++j)
+            if (j < max_rank) acc = fmaf(s_xa[j], __bfloat162float(B[static_cast<size_t>(n0 + i) * max_rank + j]), acc);
+        const float d = __bfloat162float(__float2bfloat16_rn(acc));  // bf16 delta
+        const float y = __bfloat162float(yrow[i]);
+        yrow[i] = __float2bfloat16_rn(__fadd_rn(y, __fmul_rn(sc, d)));
+    }
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -289,4 +389,52 @@ extern "C" int moe_lora_grouped_down(const MoeExpertRoute* route, const void* x,
             route->n_experts, route->n_out, route->max_rank, row_offset, row_end, P, top_k, route->a_table);
     moe::count_launch();
     return moe::check_launch("moe_lora_grouped_down (expand)");
+}
+
+extern "C" int moe_lora_gather_bgmv(const MoeExpertRoute* route, const void* x, void* base_out,
+                                    const uint32_t* indices, const int32_t* row_adapter, void* xa, uint32_t n_slots,
+                                    uint32_t top_k, uint32_t x_gather, void* stream) {
+    const char* who = "moe_lora_gather_bgmv";
+    MOE_REQUIRE(route != nullptr, "%s: NULL route", who);
+    MOE_REQUIRE(route->n_experts >= 1 && route->n_experts <= MOE_MAX_EXPERTS, "%s: n_experts=%u outside [1, %d]",
+                who, route->n_experts, MOE_MAX_EXPERTS);
+    MOE_REQUIRE(route->max_rank >= 1 && route->max_rank <= MOE_MAX_LORA_RANK, "%s: max_rank=%u outside [1, %d]",
+                who, route->max_rank, MOE_MAX_LORA_RANK);
+    MOE_REQUIRE(route->k_in > 0 && route->k_in % 8 == 0, "%s: k_in=%u must be a positive multiple of 8", who,
+                route->k_in);
+    MOE_REQUIRE(route->n_out > 0 && route->n_out % 4 == 0, "%s: n_out=%u must be a positive multiple of 4", who,
+                route->n_out);
+    MOE_REQUIRE(x_gather <= 1, "%s: x_gather=%u must be 0 or 1", who, x_gather);
+    MOE_REQUIRE(top_k >= 1, "%s: top_k must be positive", who);
+    MOE_REQUIRE(n_slots <= 0x7fffffffu, "%s: n_slots=%u too large", who, n_slots);
+    if (n_slots == 0) return MOE_OK;
+    MOE_REQUIRE(route->a_table && route->b_table && route->scale_table && x && base_out && indices && xa,
+                "%s: NULL pointer", who);
+    MOE_REQUIRE(moe::aligned16(x), "%s: x must be 16-byte aligned", who);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    moe::launch_pdl(moe::lora_gather_shrink_kernel, dim3(n_slots), 32 * moe::kShrinkWarps, 0, st,
+                    static_cast<const __nv_bfloat16*>(x), indices, row_adapter, route->a_table,
+                    static_cast<__nv_bfloat16*>(xa), route->n_experts, static_cast<int>(route->max_rank),
+                    static_cast<int>(route->k_in), top_k, x_gather);
+    moe::count_launch();
+    int rc = moe::check_launch("moe_lora_gather_bgmv (shrink)");
+    if (rc != MOE_OK) return rc;
+    const auto* xa_p = static_cast<const __nv_bfloat16*>(xa);
+    auto* base_p = static_cast<__nv_bfloat16*>(base_out);
+    const int n_out = static_cast<int>(route->n_out), rank = static_cast<int>(route->max_rank);
+    auto cols = [&](int cpc) { return dim3(n_slots, (n_out + moe::kExpandThreads * cpc - 1) / (moe::kExpandThreads * cpc)); };
+    if (rank <= 16)
+        moe::launch_pdl(moe::lora_gather_expand_fold_kernel<16>, cols(4), moe::kExpandThreads, 0, st, xa_p, indices,
+                        row_adapter, route->a_table, route->b_table, route->scale_table, base_p, route->n_experts,
+                        n_out, rank, top_k);
+    else if (rank <= 32)
+        moe::launch_pdl(moe::lora_gather_expand_fold_kernel<32>, cols(2), moe::kExpandThreads, 0, st, xa_p, indices,
+                        row_adapter, route->a_table, route->b_table, route->scale_table, base_p, route->n_experts,
+                        n_out, rank, top_k);
+    else
+        moe::launch_pdl(moe::lora_gather_expand_fold_kernel<64>, cols(1), moe::kExpandThreads, 0, st, xa_p, indices,
+                        row_adapter, route->a_table, route->b_table, route->scale_table, base_p, route->n_experts,
+                        n_out, rank, top_k);
+    moe::count_launch();
+    return moe::check_launch("moe_lora_gather_bgmv (expand)");
 }

@@ -64,6 +64,8 @@ _SIGNATURES = {
     "moe_down_workspace_size": (c_size_t, []),
     "moe_lora_grouped_down": (c_int32, [POINTER(MoeExpertRoute), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                         c_void_p, c_uint32, c_uint32, c_uint32, c_int32, c_int32, c_void_p]),
+    "moe_lora_gather_bgmv": (c_int32, [POINTER(MoeExpertRoute), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                       c_uint32, c_uint32, c_uint32, c_void_p]),
     "moe_combine": (c_int32, [c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
                               c_void_p, c_void_p]),
     "moe_validate_group_arrays": (c_int32, [c_char_p, c_int32, POINTER(c_int32), c_int32, POINTER(c_char_p),
@@ -182,6 +184,13 @@ def moe_grouped_down(h, act, w_down: MoeWeight, sorted_token_ids, expert_offsets
     _check("moe_grouped_down", lib().moe_grouped_down(
         _ptr(h), act, ctypes.byref(w_down), _ptr(sorted_token_ids), _ptr(expert_offsets), T, top_k, H, I, E,
         block_size, max_padded, _ptr(y), _ptr(err_word), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def moe_lora_gather_bgmv(route: MoeExpertRoute, x, base_out, indices, row_adapter, xa, n_slots, top_k, x_gather,
+                         stream=None):
+    _check("moe_lora_gather_bgmv", lib().moe_lora_gather_bgmv(
+        ctypes.byref(route), _ptr(x), _ptr(base_out), _ptr(indices), _ptr(row_adapter), _ptr(xa), n_slots, top_k,
+        x_gather, _stream(stream)))
 
 
 def moe_lora_grouped_down(route: MoeExpertRoute, x, base_out, expert_offsets, sorted_token_ids, row_adapter, xa,

@@ -107,6 +107,13 @@ def test_workspace_sizes(moe):
                                       0, 64, 0, 8, 2, 0),                       # rank > MAX
     lambda m: m.moe_lora_grouped_down(m.MoeExpertRoute(16, 16, 16, 4, 64, 128, 16), 16, 16, 16, 16, None, 16,
                                       10, 5, 0, 8, 2, 0),                       # window reversed
+    lambda m: m.moe_lora_gather_bgmv(m.MoeExpertRoute(16, 16, 16, 4, 64, 128, 65), 16, 16, 16, None, 16, 8, 2, 0, 0),
+    lambda m: m.moe_lora_gather_bgmv(m.MoeExpertRoute(16, 16, 16, 4, 60, 128, 16), 16, 16, 16, None, 16, 8, 2, 0, 0),
+    lambda m: m.moe_lora_gather_bgmv(m.MoeExpertRoute(16, 16, 16, 4, 64, 126, 16), 16, 16, 16, None, 16, 8, 2, 0, 0),
+    lambda m: m.moe_lora_gather_bgmv(m.MoeExpertRoute(16, 16, 16, 4, 64, 128, 16), 16, 16, 16, None, 16, 8, 2, 2, 0),
+    lambda m: m.moe_lora_gather_bgmv(m.MoeExpertRoute(16, 16, 16, 4, 64, 128, 16), 16, 16, 16, None, 16, 8, 0, 0, 0),
+    lambda m: m.moe_lora_gather_bgmv(m.MoeExpertRoute(16, 16, 16, 4, 64, 128, 16), 16, 16, None, None, 16, 8, 2, 0, 0),
+    lambda m: m.moe_lora_gather_bgmv(m.MoeExpertRoute(16, 16, 16, 4, 64, 128, 16), 24, 16, 16, None, 16, 8, 2, 0, 0),
 ])
 def test_host_detected_misuse_returns_invalid_before_any_launch(moe, call):
     n0 = moe.moe_launch_count()

@@ -241,6 +241,46 @@ def test_layer_end_to_end(dev, name):
     ffn_close(g["out"], ref.out, f"{name}: layer output")
 
 
+@pytest.mark.parametrize("x_gather,adapter,rank", [(0, False, 16), (1, True, 16), (0, True, 40), (1, False, 64)])
+def test_lora_gather_bgmv_matches_oracle(dev, x_gather, adapter, rank):
+    """Decode gather fold on slot-major rows: folded rows within tolerance of the
+    oracle, every other row of base and xa untouched bit for bit. Expert ids
+    come from real routing; the last adapted expert lies past n_experts."""
+    import torch
+    from mixture_experts_grouped_gb300 import layer as L, moe
+    cfg = synth.MoeConfig("gather_fold", T=37, H=520, I=264, E=16, k=4, bs=16, router="normal",
+                          lora_rank=rank, lora_scale=2.0, seed=3)
+    inp = synth.make_inputs(cfg)
+    lora = dict(inp["lora"])
+    lora["n_experts"] = 14                                  # adapted expert 14 folds nothing
+    ids, _ = orc.route_topk_softmax(inp["logits"], cfg.k, cfg.renormalize)
+    indices = ids.reshape(-1).astype(np.uint32)
+    rng = np.random.default_rng(11)
+    n = cfg.P
+    x = orc.f64_to_bf16_bits(rng.standard_normal((n if x_gather == 0 else cfg.T, cfg.I)))
+    base = orc.f64_to_bf16_bits(rng.standard_normal((n, cfg.H)))
+    ra = np.where(rng.random(cfg.T) < 0.3, -1, 0).astype(np.int32) if adapter else None
+    want, xa_want = orc.lora_gather_bgmv(x, base, lora["a"], lora["b"], lora["scale"], lora["n_experts"],
+                                         indices, cfg.k, ra, x_gather)
+    dl = L.upload_lora(lora, cfg.I, cfg.H, dev)
+    dl.route.n_experts = lora["n_experts"]                   # the table stops before adapted expert 14
+    xd = L.act_tensor(x, "bf16", dev)
+    bd = L.act_tensor(base, "bf16", dev)
+    idx = torch.from_numpy(indices.view(np.int32)).to(dev)
+    rad = torch.from_numpy(ra).to(dev) if adapter else None
+    xad = torch.zeros((n, dl.route.max_rank), dtype=torch.bfloat16, device=dev)
+    moe.moe_lora_gather_bgmv(dl.route, xd, bd, idx, rad, xad, n, cfg.k, x_gather)
+    torch.cuda.synchronize()
+    got = L.act_numpy(bd, "bf16")
+    xa = L.act_numpy(xad, "bf16")
+    folded = np.any(want != base, axis=1) | np.any(xa_want != 0, axis=1)
+    assert folded.sum() > n // 4 and (~folded).sum() > 0
+    np.testing.assert_array_equal(got[~folded], base[~folded])
+    assert not xa[~folded].any()
+    ffn_close(orc.bf16_bits_to_f64(got[folded]), orc.bf16_bits_to_f64(want[folded]), "gather fold: base")
+    ffn_close(orc.bf16_bits_to_f64(xa[folded]), orc.bf16_bits_to_f64(xa_want[folded]), "gather fold: xa")
+
+
 def test_lora_windows_bit_identical_to_one_window(dev):
     import torch
     from mixture_experts_grouped_gb300 import layer as L
