@@ -118,7 +118,7 @@ typedef struct MoeWeight {
  * Per-expert LoRA tables of the down-projection fold ([lora] MoeExpertRoute).
  * a_table / b_table hold one device address per expert (0 = expert
  * unadapted): A_e is bf16 [max_rank, k_in], B_e is bf16 [n_out, max_rank]
- * (max_rank is B_e's row stride). scale_table holds scale_e (0 where
+ * (max_rank is B_e's row stride), both 16-byte aligned. scale_table holds scale_e (0 where
  * unadapted). n_experts is the table length = largest adapted id + 1; experts
  * at or past it fold nothing.
  */

@@ -226,8 +226,8 @@ lora_expand_fold_kernel(const __nv_bfloat16* __restrict__ xa, const int32_t* __r
 // Restates [lora] moe_lora_gather_bgmv: row s = t * top_k + j of the flat
 // (token, slot) rows takes its expert from indices[s] and its adapt decision
 // from row_adapter[s / top_k]; no expert sort. Decode batches have few rows,
-// so a block serves one row: the shrink's eight warps split the rank, the
-// expand's threads split the output columns.
+// so a block serves one row: its eight warps split the rank for the shrink,
+// then its threads split the output columns for the expand.
 
 // the expert row s folds with, or -1 when it folds nothing
 __device__ __forceinline__ int gather_row_expert(uint32_t s, const uint32_t* indices, const int32_t* row_adapter,
@@ -238,86 +238,106 @@ __device__ __forceinline__ int gather_row_expert(uint32_t s, const uint32_t* ind
     return static_cast<int>(e);
 }
 
-// xa[s, j] = bf16(x_row . A_e[j]) for j < max_rank; warp w takes j = w, w + 8, ...
-__global__ void __launch_bounds__(32 * kShrinkWarps)
-lora_gather_shrink_kernel(const __nv_bfloat16* __restrict__ x, const uint32_t* __restrict__ indices,
-                          const int32_t* __restrict__ row_adapter, const uint64_t* __restrict__ a_table,
-                          __nv_bfloat16* __restrict__ xa, uint32_t n_experts, int max_rank, int k_in,
-                          uint32_t top_k, uint32_t x_gather) {
-    pdl_wait();
-    const uint32_t s = blockIdx.x;
-    const int e = gather_row_expert(s, indices, row_adapter, a_table, n_experts, top_k);
-    if (e < 0) return;  // block-uniform
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int chunks = k_in / 8;
-    const size_t src = x_gather ? s / top_k : s;
-    const uint4* xr = reinterpret_cast<const uint4*>(x + src * k_in);
-    const uint4* A = reinterpret_cast<const uint4*>(a_table[e]);
-    constexpr int JW = MOE_MAX_LORA_RANK / kShrinkWarps;  // outputs per warp at most
-    float acc[JW];
-#pragma unroll
-    for (int i = 0; i < JW; ++i) acc[i] = 0.0f;
-    for (int c = lane; c < chunks; c += 32) {
-        const uint4 xv = __ldg(xr + c);
-        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-        for (int i = 0; i < JW; ++i) {
-            const int j = warp + i * kShrinkWarps;
-            if (j < max_rank) {
-                const uint4 av = __ldg(A + static_cast<size_t>(j) * chunks + c);
-                const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float2 a2 = Act<MOE_ACT_BF16>::unpack2(aw[q]);
-                    const float2 x2 = Act<MOE_ACT_BF16>::unpack2(xw[q]);
-                    acc[i] = fmaf(x2.x, a2.x, acc[i]);
-                    acc[i] = fmaf(x2.y, a2.y, acc[i]);
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < JW; ++i) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
-        const int j = warp + i * kShrinkWarps;
-        if (lane == 0 && j < max_rank) xa[static_cast<size_t>(s) * max_rank + j] = __float2bfloat16_rn(acc[i]);
-    }
-}
-
-// base[s, n] = bf16(f32(base[s, n]) + f32(scale_e * bf16(xa[s] . B_e[n]))) for
-// the CPC = 64 / RCAP consecutive columns of each thread (RCAP: rank capacity)
+// One block per row s, shrink and expand in one launch (the page uses two):
+//   xa[s, j] = bf16(x_row . A_e[j]), warp w taking j = w, w + 8, ...;
+//   base[s, n] = bf16(f32(base[s, n]) + f32(scale_e * bf16(xa[s] . B_e[n]))),
+//   each thread taking CPC = 64 / RCAP consecutive columns per pass
+//   (RCAP: rank capacity of the instantiation).
+// The shrink's sums meet in shared memory, so the expand needs no second
+// launch and no global round trip of xa.
 template <int RCAP>
-__global__ void __launch_bounds__(kExpandThreads)
-lora_gather_expand_fold_kernel(const __nv_bfloat16* __restrict__ xa, const uint32_t* __restrict__ indices,
-                               const int32_t* __restrict__ row_adapter, const uint64_t* __restrict__ a_table,
-                               const uint64_t* __restrict__ b_table, const float* __restrict__ scale_table,
-                               __nv_bfloat16* __restrict__ base, uint32_t n_experts, int n_out, int max_rank,
-                               uint32_t top_k) {
+__global__ void __launch_bounds__(32 * kShrinkWarps)
+lora_gather_fold_kernel(const __nv_bfloat16* __restrict__ x, const uint32_t* __restrict__ indices,
+                        const int32_t* __restrict__ row_adapter, const uint64_t* __restrict__ a_table,
+                        const uint64_t* __restrict__ b_table, const float* __restrict__ scale_table,
+                        __nv_bfloat16* __restrict__ xa, __nv_bfloat16* __restrict__ base, uint32_t n_experts,
+                        int k_in, int n_out, int max_rank, uint32_t top_k, uint32_t x_gather) {
     pdl_wait();
     constexpr int CPC = 64 / RCAP;
     __shared__ float s_xa[RCAP];
     const uint32_t s = blockIdx.x;
     const int e = gather_row_expert(s, indices, row_adapter, a_table, n_experts, top_k);
     if (e < 0) return;  // block-uniform
-    if (threadIdx.x < RCAP)
-        s_xa[threadIdx.x] =
-            threadIdx.x < max_rank ? __bfloat162float(xa[static_cast<size_t>(s) * max_rank + threadIdx.x]) : 0.0f;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x < RCAP) s_xa[threadIdx.x] = 0.0f;  // ranks past max_rank stay 0
     __syncthreads();
-    const int n0 = (blockIdx.y * kExpandThreads + threadIdx.x) * CPC;
-    if (n0 >= n_out) return;  // n_out % 4 == 0 and CPC divides 4: a thread's columns are all in range
-    const __nv_bfloat16* B = reinterpret_cast<const __nv_bfloat16*>(b_table[e]);
+    {
+        const int chunks = k_in / 8;
+        const size_t src = x_gather ? s / top_k : s;
+        const uint4* xr = reinterpret_cast<const uint4*>(x + src * k_in);
+        const uint4* A = reinterpret_cast<const uint4*>(a_table[e]);
+        constexpr int JW = (RCAP + kShrinkWarps - 1) / kShrinkWarps;  // outputs per warp at most
+        float acc[JW];
+#pragma unroll
+        for (int i = 0; i < JW; ++i) acc[i] = 0.0f;
+        for (int c = lane; c < chunks; c += 32) {
+            const uint4 xv = __ldg(xr + c);
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int i = 0; i < JW; ++i) {
+                const int j = warp + i * kShrinkWarps;
+                if (j < max_rank) {
+                    const uint4 av = __ldg(A + static_cast<size_t>(j) * chunks + c);
+                    const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 a2 = Act<MOE_ACT_BF16>::unpack2(aw[q]);
+                        const float2 x2 = Act<MOE_ACT_BF16>::unpack2(xw[q]);
+                        acc[i] = fmaf(x2.x, a2.x, acc[i]);
+                        acc[i] = fmaf(x2.y, a2.y, acc[i]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < JW; ++i) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
+            const int j = warp + i * kShrinkWarps;
+            if (lane == 0 && j < max_rank) {
+                const __nv_bfloat16 v = __float2bfloat16_rn(acc[i]);  // bf16 xa
+                xa[static_cast<size_t>(s) * max_rank + j] = v;
+                s_xa[j] = __bfloat162float(v);
+            }
+        }
+    }
+    __syncthreads();
+    const __nv_bfloat16* Bbase = reinterpret_cast<const __nv_bfloat16*>(b_table[e]);
     const float sc = scale_table[e];
-    __nv_bfloat16* yrow = base + static_cast<size_t>(s) * n_out + n0;
+    for (int n0 = threadIdx.x * CPC; n0 < n_out; n0 += blockDim.x * CPC) {
+        // this thread's CPC rows of B_e: CPC * max_rank consecutive values
+        const __nv_bfloat16* B = Bbase + static_cast<size_t>(n0) * max_rank;
+        float bw[CPC][RCAP];
+        if (max_rank == RCAP) {  // 64 values = 128 aligned bytes: eight 16-byte loads
 #pragma unroll
-    for (int i = 0; i < CPC; ++i) {
-        float acc = 0.0f;
+            for (int v = 0; v < CPC * RCAP / 8; ++v) {
+                const uint4 q = __ldg(reinterpret_cast<const uint4*>(B) + v);
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int j = 0; j < RCAP; ++j)
-            if (j < max_rank) acc = fmaf(s_xa[j], __bfloat162float(B[static_cast<size_t>(n0 + i) * max_rank + j]), acc);
-        const float d = __bfloat162float(__float2bfloat16_rn(acc));  // bf16 delta
-        const float y = __bfloat162float(yrow[i]);
-        yrow[i] = __float2bfloat16_rn(__fadd_rn(y, __fmul_rn(sc, d)));
+                for (int h = 0; h < 4; ++h) {
+                    const float2 f = Act<MOE_ACT_BF16>::unpack2(w[h]);
+                    const int k0 = v * 8 + 2 * h;
+                    bw[k0 / RCAP][k0 % RCAP] = f.x;
+                    bw[(k0 + 1) / RCAP][(k0 + 1) % RCAP] = f.y;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < CPC; ++i)
+#pragma unroll
+                for (int j = 0; j < RCAP; ++j)
+                    bw[i][j] = j < max_rank ? __bfloat162float(B[i * max_rank + j]) : 0.0f;
+        }
+        __nv_bfloat16* yrow = base + static_cast<size_t>(s) * n_out + n0;
+#pragma unroll
+        for (int i = 0; i < CPC; ++i) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int j = 0; j < RCAP; ++j) acc = fmaf(s_xa[j], bw[i][j], acc);
+            const float d = __bfloat162float(__float2bfloat16_rn(acc));  // bf16 delta
+            const float y = __bfloat162float(yrow[i]);
+            yrow[i] = __float2bfloat16_rn(__fadd_rn(y, __fmul_rn(sc, d)));
+        }
     }
 }
 
@@ -412,29 +432,24 @@ extern "C" int moe_lora_gather_bgmv(const MoeExpertRoute* route, const void* x, 
                 "%s: NULL pointer", who);
     MOE_REQUIRE(moe::aligned16(x), "%s: x must be 16-byte aligned", who);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    moe::launch_pdl(moe::lora_gather_shrink_kernel, dim3(n_slots), 32 * moe::kShrinkWarps, 0, st,
-                    static_cast<const __nv_bfloat16*>(x), indices, row_adapter, route->a_table,
-                    static_cast<__nv_bfloat16*>(xa), route->n_experts, static_cast<int>(route->max_rank),
-                    static_cast<int>(route->k_in), top_k, x_gather);
-    moe::count_launch();
-    int rc = moe::check_launch("moe_lora_gather_bgmv (shrink)");
-    if (rc != MOE_OK) return rc;
-    const auto* xa_p = static_cast<const __nv_bfloat16*>(xa);
+    const auto* xp = static_cast<const __nv_bfloat16*>(x);
+    auto* xa_p = static_cast<__nv_bfloat16*>(xa);
     auto* base_p = static_cast<__nv_bfloat16*>(base_out);
-    const int n_out = static_cast<int>(route->n_out), rank = static_cast<int>(route->max_rank);
-    auto cols = [&](int cpc) { return dim3(n_slots, (n_out + moe::kExpandThreads * cpc - 1) / (moe::kExpandThreads * cpc)); };
+    const int k_in = static_cast<int>(route->k_in), n_out = static_cast<int>(route->n_out),
+              rank = static_cast<int>(route->max_rank);
+    const dim3 grid(n_slots), block(32 * moe::kShrinkWarps);
     if (rank <= 16)
-        moe::launch_pdl(moe::lora_gather_expand_fold_kernel<16>, cols(4), moe::kExpandThreads, 0, st, xa_p, indices,
-                        row_adapter, route->a_table, route->b_table, route->scale_table, base_p, route->n_experts,
-                        n_out, rank, top_k);
+        moe::launch_pdl(moe::lora_gather_fold_kernel<16>, grid, block, 0, st, xp, indices, row_adapter,
+                        route->a_table, route->b_table, route->scale_table, xa_p, base_p, route->n_experts, k_in,
+                        n_out, rank, top_k, x_gather);
     else if (rank <= 32)
-        moe::launch_pdl(moe::lora_gather_expand_fold_kernel<32>, cols(2), moe::kExpandThreads, 0, st, xa_p, indices,
-                        row_adapter, route->a_table, route->b_table, route->scale_table, base_p, route->n_experts,
-                        n_out, rank, top_k);
+        moe::launch_pdl(moe::lora_gather_fold_kernel<32>, grid, block, 0, st, xp, indices, row_adapter,
+                        route->a_table, route->b_table, route->scale_table, xa_p, base_p, route->n_experts, k_in,
+                        n_out, rank, top_k, x_gather);
     else
-        moe::launch_pdl(moe::lora_gather_expand_fold_kernel<64>, cols(1), moe::kExpandThreads, 0, st, xa_p, indices,
-                        row_adapter, route->a_table, route->b_table, route->scale_table, base_p, route->n_experts,
-                        n_out, rank, top_k);
+        moe::launch_pdl(moe::lora_gather_fold_kernel<64>, grid, block, 0, st, xp, indices, row_adapter,
+                        route->a_table, route->b_table, route->scale_table, xa_p, base_p, route->n_experts, k_in,
+                        n_out, rank, top_k, x_gather);
     moe::count_launch();
-    return moe::check_launch("moe_lora_gather_bgmv (expand)");
+    return moe::check_launch("moe_lora_gather_bgmv");
 }
