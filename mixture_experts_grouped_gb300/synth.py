@@ -16,6 +16,8 @@ Workloads (names used across the tests and the benchmark):
 * ``fine_grained``    H=2048, I=768, E=128, k=8, bs=64, bf16, Zipf-biased router
 * ``gptq``            H=2048, I=1408, E=64, k=6, bs=16, fp16 activations, GPTQ int4
 * ``nvfp4_lora``      T=2048, H=2048, I=768, E=128, k=8, bs=64, NVFP4 + rank-16 LoRA
+* ``fp8``             T=2048, H=2048, I=768, E=128, k=8, bs=64, FP8 (E4M3) weights with
+                      per-row fp32 scales, bf16 activations
 """
 
 from __future__ import annotations
@@ -41,7 +43,7 @@ class MoeConfig:
     k: int
     bs: int
     act: str = "bf16"          # activation dtype: "bf16" | "f16"
-    wfmt: str = "bf16"         # weight format: "bf16" | "gptq" | "nvfp4"
+    wfmt: str = "bf16"         # weight format: "bf16" | "gptq" | "nvfp4" | "fp8"
     router: str = "gemm"       # "gemm": logits = x @ Wr; "normal": N(0,1); "zipf": N(0,1) + bias
     router_std: float = 0.02   # std of Wr for router="gemm"
     weight_std: float = 0.02
@@ -69,6 +71,7 @@ CONFIGS = {
                       wfmt="gptq", router="normal"),
     "nvfp4_lora": MoeConfig("nvfp4_lora", T=2048, H=2048, I=768, E=128, k=8, bs=64,
                             wfmt="nvfp4", router="normal", lora_rank=16),
+    "fp8": MoeConfig("fp8", T=2048, H=2048, I=768, E=128, k=8, bs=64, wfmt="fp8", router="normal"),
 }
 
 FINE_GRAINED_T = (1, 8, 64, 512, 4096, 16384)
@@ -160,6 +163,29 @@ def _nvfp4_weight(seed, tensor, E, N, K, n_scale2):
             "scale2": s2}
 
 
+# E4M3 exponent-field probabilities (fields 0..10; 0 = zero and subnormals),
+# so that most codes are 0.125 .. 7.5 and some are subnormal
+_E4M3_EXP_P = np.array([0.03, 0.02, 0.03, 0.05, 0.09, 0.14, 0.18, 0.18, 0.14, 0.09, 0.05])
+
+
+def _fp8_weight(seed, tensor, E, N, K):
+    """FP8 (E4M3) codes drawn directly (random sign, exponent field from
+    ``_E4M3_EXP_P``, any mantissa: never NaN) with one fp32 scale per output
+    row U(0.5, 1.5) * 0.0075, so that the decoded weights have RMS close to
+    0.02, the scale of the bf16 workloads."""
+    def codes(e):
+        r = _rng(seed, tensor, e)
+        ex = r.choice(len(_E4M3_EXP_P), size=(N, K), p=_E4M3_EXP_P).astype(np.uint8)
+        man = r.integers(0, 8, size=(N, K), dtype=np.uint8)
+        sign = r.integers(0, 2, size=(N, K), dtype=np.uint8) << 7
+        return (sign | (ex << 3) | man).astype(np.uint8)
+
+    def scales(e):
+        return (_rng(seed, tensor + 100, e).uniform(0.5, 1.5, size=N) * 0.0075).astype(np.float32)
+
+    return {"format": "fp8", "codes": _per_expert(codes, E), "scales": _per_expert(scales, E)}
+
+
 def make_weights(cfg: MoeConfig) -> dict:
     """Expert weights: gate/up stacked ``[E, 2I, H]`` (rows ``[0, I)`` gate,
     ``[I, 2I)`` up) and down ``[E, H, I]`` in the config's format."""
@@ -173,6 +199,9 @@ def make_weights(cfg: MoeConfig) -> dict:
     elif cfg.wfmt == "nvfp4":
         gu = _nvfp4_weight(s, _GU, E, 2 * I, H, 2)
         dn = _nvfp4_weight(s, _DOWN, E, H, I, 1)
+    elif cfg.wfmt == "fp8":
+        gu = _fp8_weight(s, _GU, E, 2 * I, H)
+        dn = _fp8_weight(s, _DOWN, E, H, I)
     else:
         raise ValueError(cfg.wfmt)
     return {"w_gate_up": gu, "w_down": dn}

@@ -38,7 +38,7 @@ __all__ = [
     "round_act", "act_to_f64", "f64_to_act",
     "align_capacity", "route_topk_softmax", "warp_order_sum_f32",
     "align_block_size", "AlignResult", "ensure_group_arrays", "GroupArrayError",
-    "e2m1_value", "e4m3_value", "dequant_bf16", "dequant_gptq", "dequant_nvfp4",
+    "e2m1_value", "e4m3_value", "dequant_bf16", "dequant_gptq", "dequant_nvfp4", "dequant_fp8",
     "expert_weight", "prepare_f64", "grouped_gate_up", "grouped_down", "lora_grouped_down",
     "lora_gather_bgmv", "gather_bgmv_grids", "combine", "moe_layer", "LayerResult",
 ]
@@ -359,6 +359,20 @@ def dequant_nvfp4(packed: np.ndarray, scales: np.ndarray, scale2) -> np.ndarray:
     return w * s2.reshape(-1, 1)
 
 
+def dequant_fp8(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """FP8 (E4M3) weight of one expert -> fp64 ``W[n, kappa]``.
+
+    The pages name FP8 grouped prefill weights beside NVFP4 and bf16 ([lora]
+    module doc: the same fold serves the nvfp4, bf16 and fp8 grouped prefill
+    paths) but print no layout. Reading, the plainest W8A16 one: E4M3 codes
+    ``[N, K]`` (OCP FP8, bias 7, no infinities, 0x7F / 0xFF NaN), one fp32
+    scale per output row, ``w[n, kappa] = e4m3(codes[n, kappa]) * scales[n]``.
+    """
+    v = e4m3_value(np.asarray(codes, dtype=np.uint8))                 # [N, K]
+    s = np.asarray(scales, dtype=np.float32).astype(np.float64)
+    return v * s.reshape(-1, 1)
+
+
 def expert_weight(spec: dict, e: int) -> np.ndarray:
     """Dequantised fp64 ``W[n, kappa]`` of expert e for a weight spec.
 
@@ -373,6 +387,7 @@ def expert_weight(spec: dict, e: int) -> np.ndarray:
       "scale2": f32 [S, E]}`` where ``S = 2`` for a gate/up weight (rows
       ``[0, N/2)`` take ``scale2[0, e]``, rows ``[N/2, N)`` take ``scale2[1, e]``)
       and ``S = 1`` otherwise.
+    * ``{"format": "fp8", "codes": uint8 [E, N, K], "scales": f32 [E, N]}``
     """
     fmt = spec["format"]
     if fmt == "f64":
@@ -390,13 +405,15 @@ def expert_weight(spec: dict, e: int) -> np.ndarray:
         else:
             row_s2 = np.full(N, s2[0, e], dtype=np.float32)
         return dequant_nvfp4(spec["packed"][e], spec["scales"][e], row_s2)
+    if fmt == "fp8":
+        return dequant_fp8(spec["codes"][e], spec["scales"][e])
     raise ValueError(f"unknown weight format {fmt!r}")
 
 
 def prepare_f64(spec: dict) -> dict:
-    """Expand every expert of a weight spec to fp64 once (exact for all three
-    formats), so repeated layer calls skip the per-call dequantisation."""
-    E = next(v for k, v in spec.items() if k in ("w", "qweight", "packed")).__len__()
+    """Expand every expert of a weight spec to fp64 once (exact for every
+    format), so repeated layer calls skip the per-call dequantisation."""
+    E = next(v for k, v in spec.items() if k in ("w", "qweight", "packed", "codes")).__len__()
     return {"format": "f64", "w": [expert_weight(spec, e) for e in range(E)]}
 
 

@@ -153,10 +153,41 @@ def test_expert_weight_nvfp4_gate_up_scale2_split():
 
 def test_prepared_f64_weights_are_the_dequantised_values():
     from mixture_experts_grouped_gb300 import synth
-    for wfmt, act in (("bf16", "bf16"), ("gptq", "f16"), ("nvfp4", "bf16")):
+    for wfmt, act in (("bf16", "bf16"), ("gptq", "f16"), ("nvfp4", "bf16"), ("fp8", "bf16")):
         cfg = synth.MoeConfig("p", T=4, H=64, I=64, E=3, k=1, bs=4, wfmt=wfmt, act=act, router="normal",
                               group_size=64)
         w = synth.make_weights(cfg)["w_gate_up"]
         pre = orc.prepare_f64(w)
         for e in range(3):
             np.testing.assert_array_equal(orc.expert_weight(pre, e), orc.expert_weight(w, e))
+
+
+def test_fp8_dequant_hand_built_codes():
+    # 0x38 = 1.0, 0xB8 = -1.0, 0x01 = 2^-9 (smallest subnormal), 0x7E = 448 (largest finite),
+    # 0x00 / 0x80 = +0 / -0; row scales 2 and 0.5
+    codes = np.array([[0x38, 0xB8, 0x00], [0x01, 0x7E, 0x80]], np.uint8)
+    w = orc.dequant_fp8(codes, np.array([2.0, 0.5], np.float32))
+    np.testing.assert_array_equal(w, [[2.0, -2.0, 0.0], [2.0 ** -10, 224.0, -0.0]])
+    assert np.signbit(w[1, 2])
+
+
+def test_fp8_dequant_matches_torch_float8():
+    # torch's float8_e4m3fn is the OCP E4M3 format: every finite code decodes alike
+    codes = np.arange(256, dtype=np.uint8).reshape(16, 16)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = orc.dequant_fp8(codes, np.ones(16, np.float32))
+    fin = np.isfinite(want)
+    np.testing.assert_array_equal(got[fin], want[fin])
+    assert np.all(np.isnan(got[~fin]))
+
+
+def test_expert_weight_fp8_row_scales():
+    from mixture_experts_grouped_gb300 import synth
+    cfg = synth.MoeConfig("p", T=4, H=64, I=32, E=3, k=1, bs=4, wfmt="fp8", router="normal")
+    w = synth.make_weights(cfg)["w_gate_up"]
+    for e in range(3):
+        W = orc.expert_weight(w, e)
+        assert W.shape == (64, 64)
+        np.testing.assert_array_equal(W, orc.e4m3_value(w["codes"][e]) * w["scales"][e].astype(np.float64)[:, None])
+        rms = np.sqrt(np.mean(W ** 2))
+        assert 0.01 < rms < 0.04 and np.all(np.isfinite(W))
