@@ -86,6 +86,8 @@ def algorithmic(cfg, ids):
     elif cfg.wfmt == "gptq":
         G = cfg.group_size
         per_expert = sum(K * N // 2 + (K // G) * N * 2 + (K // G) * (N // 8) * 4 for K, N in ((H, 2 * I), (I, H)))
+    elif cfg.wfmt == "fp8":
+        per_expert = sum(K * N + N * 4 for K, N in ((H, 2 * I), (I, H)))
     else:
         per_expert = sum(K * N // 2 + (K // 16) * N + 4 for K, N in ((H, 2 * I), (I, H)))
     act = 2
@@ -99,6 +101,8 @@ def algorithmic(cfg, ids):
     elif cfg.wfmt == "gptq":
         G = cfg.group_size
         gu_weight = H * 2 * I // 2 + (H // G) * 2 * I * 2 + (H // G) * (2 * I // 8) * 4
+    elif cfg.wfmt == "fp8":
+        gu_weight = H * 2 * I + 2 * I * 4
     else:
         gu_weight = H * 2 * I // 2 + (H // 16) * 2 * I + 8
     # the gate/up call: gather (x read, rows written), GEMM (rows read, weights, h written)

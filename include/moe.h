@@ -81,6 +81,7 @@ extern "C" {
 #define MOE_W_BF16 0      /* dense weight in the activation type */
 #define MOE_W_GPTQ_INT4 1 /* raw GPTQ 4-bit: qweight / scales / qzeros ([triton]) */
 #define MOE_W_NVFP4 2     /* E2M1 + E4M3 per-16 scales + fp32 scale2 ([cutlass]) */
+#define MOE_W_FP8_E4M3 3  /* E4M3 codes + one fp32 scale per output row ([lora]: fp8 grouped weights) */
 
 /*
  * A stacked expert weight of E experts, each of logical shape [N, K]
@@ -104,6 +105,11 @@ extern "C" {
  *                scale2 = fp32 [S, E]: S = 2 for a gate/up weight (gate's E
  *                         values, then up's), S = 1 for a down weight
  *                w(n, k) = e2m1 * e4m3(scales[k/16][n]) * scale2
+ *   MOE_W_FP8_E4M3 (the pages name fp8 grouped weights but print no layout;
+ *                this is the plain W8A16 reading):
+ *                w      = E4M3 uint8 [E, N, K] (OCP FP8: bias 7, no inf)
+ *                scales = fp32 [E, N], one per output row
+ *                w(n, k) = e4m3(w[n][k]) * scales[n]
  */
 typedef struct MoeWeight {
     int32_t format;     /* MOE_W_* */
@@ -255,8 +261,8 @@ size_t moe_gate_up_workspace_size(int32_t max_padded, int32_t H);
  *                     after a call that reported a device error
  * Requirements: H % 8 == 0, I % 8 == 0, E <= MOE_MAX_EXPERTS, all tensor
  * base addresses 16-byte aligned; GPTQ: group_size a multiple of 64 dividing
- * H and I % 32 == 0; NVFP4: H % 32 == 0 and I % 16 == 0. A contraction that
- * is not a multiple of 64 is zero-padded on chip.
+ * H and I % 32 == 0; NVFP4: H % 32 == 0 and I % 16 == 0; FP8: H % 16 == 0.
+ * A contraction that is not a multiple of 64 is zero-padded on chip.
  */
 int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* w_gate_up,
                         const int32_t* sorted_token_ids, const int32_t* expert_offsets,
@@ -281,7 +287,7 @@ int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* w_gate_up,
  *                     tiles across CTAs (split-K) and adds partial sums there
  * Requirements: I % 8 == 0, H % 8 == 0, 16-byte aligned tensors; GPTQ:
  * group_size a multiple of 64 dividing I and H % 32 == 0; NVFP4: I % 32 == 0
- * and H % 16 == 0.
+ * and H % 16 == 0; FP8: I % 16 == 0.
  */
 int moe_grouped_down(const void* h, int32_t act, const MoeWeight* w_down,
                      const int32_t* sorted_token_ids, const int32_t* expert_offsets,

@@ -64,6 +64,7 @@ struct GemmParams {
     int32_t* err;
     int block_size;  // align block size: spans are multiples of it, padding is a span's last < block_size rows
     int pad_free;    // the kernel's tile height is a multiple of block_size: no tile holds padding only
+    const float* row_scale;  // FP8: fp32 scale per weight row [E, n_w]
     float* sk_part;  // split-K partial sums: one slice of SK_SLICE_FLOATS per CTA (decode form)
     int* sk_flag;    // split-K flags: 4 per CTA (one per epilogue warp), zero between launches
 };
@@ -1185,11 +1186,36 @@ __device__ __forceinline__ void nvfp4_row(const uint32_t (&w)[NW], const uint32_
     }
 }
 
+// One FP8 weight row for a k block: word i holds the E4M3 codes of k = 4i ..
+// 4i+3 (lowest byte first). Writes the codes' values unscaled (the row scale
+// multiplies the f32 accumulator in the epilogue) as 32 columns of two 16-bit
+// values: E4M3 -> f16 is one exact conversion per pair, and every E4M3 value
+// is also exact in bf16 (4 significant bits, exponents 2^-9 .. 2^8).
+template <int ACT>
+__device__ __forceinline__ void fp8_row(const uint32_t (&w)[16], uint32_t (&o)[32]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        uint32_t lo, hi;  // (k 4i, 4i+1), (k 4i+2, 4i+3) as f16x2
+        asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+            : "=r"(lo), "=r"(hi) : "r"(w[i]));
+        if (ACT == MOE_ACT_F16) {
+            o[2 * i] = lo;
+            o[2 * i + 1] = hi;
+        } else {
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+            o[2 * i] = Act<ACT>::pack2(a.x, a.y);
+            o[2 * i + 1] = Act<ACT>::pack2(b.x, b.y);
+        }
+    }
+}
+
 // One weight row's raw bytes for a 64-deep k block, in registers: GPTQ 8
 // words, the fp16 scale bits and the packed zero-point word; NVFP4 8 words and
 // 4 scale bytes.
 struct RawRow {
-    uint32_t w[8];
+    uint32_t w[16];  // GPTQ / NVFP4: 8 words; FP8: 16 (one code byte per k)
     uint32_t s, z;
     uint32_t sc[4];
 };
@@ -1200,9 +1226,17 @@ struct RawRow {
 //          sg = 2 group rows for group_size 64 and 1 otherwise;
 //   NVFP4: codes [2 halves][128 rows][64 bytes] at 0, scales [8 k16 groups]
 //          [2 halves][128 rows] E4M3 at 16384.
+// An FP8 raw stage holds one k block: codes [2 halves][128 rows][64 bytes].
 template <int WFMT>
 __device__ __forceinline__ void load_raw_row(const uint8_t* raw, int h, int r, int kp, int g64, RawRow& x) {
-    if (WFMT == MOE_W_GPTQ_INT4) {
+    if (WFMT == MOE_W_FP8_E4M3) {
+        const uint4* row = reinterpret_cast<const uint4*>(raw + h * 8192 + r * 64);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = row[i];
+            x.w[4 * i] = v.x; x.w[4 * i + 1] = v.y; x.w[4 * i + 2] = v.z; x.w[4 * i + 3] = v.w;
+        }
+    } else if (WFMT == MOE_W_GPTQ_INT4) {
         const uint32_t* qw = reinterpret_cast<const uint32_t*>(raw);
 #pragma unroll
         for (int i = 0; i < 8; ++i) x.w[i] = qw[((8 * kp + i) * 2 + h) * 128 + r];
@@ -1239,7 +1273,8 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
     const int warp = tid >> 5, lane = tid & 31;
     const int E = p.E;
     const int KB = (p.K + BK - 1) / BK;  // 64-deep k blocks (weight and activation stages)
-    const int KR = (KB + 1) / 2;         // 128-deep raw stages per tile
+    constexpr int KPR = WFMT == MOE_W_FP8_E4M3 ? 1 : 2;  // k blocks per raw stage
+    const int KR = (KB + KPR - 1) / KPR;                   // raw stages per tile
     const int NSETS = KB < S::NR ? KB : S::NR;  // accumulator sets a tile uses
     // GPTQ group rows per raw stage: two for group_size 64, else one
     const int g64 = WFMT == MOE_W_GPTQ_INT4 && p.group_size == 64;
@@ -1378,6 +1413,14 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
             if (WFMT == MOE_W_NVFP4) {
                 s2a = __ldg(p.scale2 + t.e);
                 s2b = (MODE == MODE_GATE_UP) ? __ldg(p.scale2 + p.E + t.e) : s2a;
+            } else if (WFMT == MOE_W_FP8_E4M3) {
+                // this lane's weight rows: half 0 row n, half 1 the up row I + n (gate/up)
+                // or n + 128 (down); rows past the output are never stored
+                const int n = t.n0 + q * 32 + lane;
+                const float* rs = p.row_scale + static_cast<size_t>(t.e) * p.n_w;
+                if (n < p.n_out) s2a = __ldg(rs + n);
+                const int n1 = MODE == MODE_GATE_UP ? p.n_out + n : n + 128;
+                if ((MODE == MODE_GATE_UP ? n : n + 128) < p.n_out) s2b = __ldg(rs + n1);
             }
             if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
             tc_fence_after();
@@ -1395,7 +1438,7 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
                         stg[j * 32 + lane] = Act<ACT>::from_f(silu_mul(a[j] * s2a, b[j] * s2b));
                     } else {
                         stg[j * 32 + lane] = Act<ACT>::from_f(a[j] * s2a);
-                        stg[512 + j * 32 + lane] = Act<ACT>::from_f(b[j] * s2a);
+                        stg[512 + j * 32 + lane] = Act<ACT>::from_f(b[j] * s2b);
                     }
                 }
                 __syncwarp();
@@ -1431,13 +1474,18 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
             if (!tile_is_padding(p, decode_tile<XROWS>(s, E, tile, S::OUT_COLS))) items += KB;
         int f_kb = 0, f_rs0 = 0;  // position of the next item to fetch (k block, its tile's first raw stage)
         auto fetch = [&](RawRow& x) -> bool {
-            const int rs = f_rs0 + (f_kb >> 1);
+            const int rs = f_rs0 + f_kb / KPR;
             const int rst = rs % RSTAGES;
-            if ((f_kb & 1) == 0 &&
+            if (f_kb % KPR == 0 &&
                 !mbar_wait(&s.raw_full[rst], static_cast<uint32_t>((rs / RSTAGES) & 1), abort_flag, p.err))
                 return false;
-            load_raw_row<WFMT>(sR + rst * RAW2, h, r, f_kb & 1, g64, x);
-            if ((f_kb & 1) == 1 || f_kb == KB - 1) {
+            load_raw_row<WFMT>(sR + rst * RAW2, h, r, f_kb % KPR, g64, x);
+            if (f_kb % KPR == KPR - 1 || f_kb == KB - 1) {
+                // the stage was read through the generic proxy and is refilled by
+                // TMA (the async proxy): order the reads before the release, or
+                // the next copy may land under them (seen as stale rows for a
+                // few tiles once the dequantisation is fast)
+                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s.raw_empty[rst]);
             }
@@ -1452,11 +1500,20 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
         for (int it = 0; it < items && ok; ++it) {
             if (it + 1 < items && !fetch(nxt)) break;
             uint32_t o[32];
-            if (WFMT == MOE_W_GPTQ_INT4)
-                gptq_row<ACT, S::PERM>(cur.w, (cur.z >> (4 * (r & 7))) & 15,
+            if (WFMT == MOE_W_GPTQ_INT4) {
+                uint32_t w8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w8[i] = cur.w[i];
+                gptq_row<ACT, S::PERM>(w8, (cur.z >> (4 * (r & 7))) & 15,
                                        __ushort_as_half(static_cast<unsigned short>(cur.s)), o);
-            else
-                nvfp4_row<ACT>(cur.w, cur.sc, o);
+            } else if (WFMT == MOE_W_NVFP4) {
+                uint32_t w8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w8[i] = cur.w[i];
+                nvfp4_row<ACT>(w8, cur.sc, o);
+            } else {
+                fp8_row<ACT>(cur.w, o);
+            }
             const int as = it % ASTAGES;
             if (!mbar_wait(&s.aempty[as], static_cast<uint32_t>(((it / ASTAGES) & 1) ^ 1), abort_flag, p.err)) break;
             tc_fence_after();  // the MMAs that read this TMEM stage have completed
@@ -1475,7 +1532,9 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
         // NVFP4 codes + scales. For an odd number of k blocks the second half
         // of a tile's last stage is fetched but not used.
         if (lane == 0) {
-            const uint32_t bytes = WFMT == MOE_W_GPTQ_INT4 ? 16384u + (g64 ? 2u : 1u) * 640u : 18432u;
+            const uint32_t bytes = WFMT == MOE_W_GPTQ_INT4 ? 16384u + (g64 ? 2u : 1u) * 640u
+                                   : WFMT == MOE_W_NVFP4   ? 18432u
+                                                           : 16384u;
             uint32_t rstage = 0, rphase = 0;
             long issued = 0;
             bool ok = true;
@@ -1499,6 +1558,12 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
                             tma_load_2d(rw + 16384, &tmR1, t.n0, g, bar);
                             tma_load_2d(rw + 17408, &tmR2, t.n0 / 8, g, bar);
                         }
+                    } else if (WFMT == MOE_W_FP8_E4M3) {
+                        // one 64-deep k block of both halves: [2][128 rows][64 bytes]
+                        if (MODE == MODE_GATE_UP)
+                            tma_load_3d(rw, &tmR0, kr * BK, t.n0, 2 * t.e, bar);
+                        else
+                            tma_load_2d(rw, &tmR0, kr * BK, t.e * p.n_w + t.n0, bar);
                     } else {
                         const int sg = t.e * (p.K / 16) + kr * 8;
                         if (MODE == MODE_GATE_UP) {
@@ -1715,8 +1780,11 @@ int dispatch(int wfmt, int act, int ntok, const Maps& m, const GemmParams& p, cu
     if (wfmt == MOE_W_GPTQ_INT4)
         return act == MOE_ACT_F16 ? ts_by_ntok<MODE, MOE_W_GPTQ_INT4, MOE_ACT_F16>(nt, m, p, st, who)
                                   : ts_by_ntok<MODE, MOE_W_GPTQ_INT4, MOE_ACT_BF16>(nt, m, p, st, who);
-    return act == MOE_ACT_F16 ? ts_by_ntok<MODE, MOE_W_NVFP4, MOE_ACT_F16>(nt, m, p, st, who)
-                              : ts_by_ntok<MODE, MOE_W_NVFP4, MOE_ACT_BF16>(nt, m, p, st, who);
+    if (wfmt == MOE_W_NVFP4)
+        return act == MOE_ACT_F16 ? ts_by_ntok<MODE, MOE_W_NVFP4, MOE_ACT_F16>(nt, m, p, st, who)
+                                  : ts_by_ntok<MODE, MOE_W_NVFP4, MOE_ACT_BF16>(nt, m, p, st, who);
+    return act == MOE_ACT_F16 ? ts_by_ntok<MODE, MOE_W_FP8_E4M3, MOE_ACT_F16>(nt, m, p, st, who)
+                              : ts_by_ntok<MODE, MOE_W_FP8_E4M3, MOE_ACT_BF16>(nt, m, p, st, who);
 }
 
 // Checks the weight descriptor and encodes its tensor maps. N = weight rows
@@ -1805,6 +1873,24 @@ int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Map
             m.w = m.r0;
             return rc;
         }
+        case MOE_W_FP8_E4M3: {
+            MOE_REQUIRE(w->w && w->scales, "%s: FP8 codes / scales must be non-NULL", who);
+            MOE_REQUIRE(K % 16 == 0, "%s: FP8 needs K=%d divisible by 16", who, K);
+            // one copy per 64-deep raw stage: a 3-D map over the gate and up
+            // halves for gate/up, a 256-row box for down
+            int rc;
+            if (N == 2 * n_out) {
+                const uint64_t I = n_out;
+                rc = make_tmap_3d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, I, 2 * static_cast<uint64_t>(E),
+                                      K, I * K, 64, hc, 2);
+            } else {
+                rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(E) * N, K,
+                                      64, dc);
+            }
+            m.r1 = m.r2 = m.r0;
+            m.w = m.r0;
+            return rc;
+        }
         default:
             return fail(MOE_ERR_INVALID, "%s: unknown weight format %d", who, w->format);
     }
@@ -1886,6 +1972,7 @@ extern "C" int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* 
     p.max_padded = max_padded;
     p.out = h_out;
     p.scale2 = w_gate_up->scale2;
+    p.row_scale = static_cast<const float*>(w_gate_up->scales);
     p.group_size = w_gate_up->group_size;
     p.err = err_word;
     p.block_size = block_size;
@@ -1928,6 +2015,7 @@ extern "C" int moe_grouped_down(const void* h, int32_t act, const MoeWeight* w_d
     p.max_padded = max_padded;
     p.out = y;
     p.scale2 = w_down->scale2;
+    p.row_scale = static_cast<const float*>(w_down->scales);
     p.group_size = w_down->group_size;
     p.err = err_word;
     p.block_size = block_size;

@@ -65,6 +65,10 @@ def upload_weight(spec: dict, act: str, device) -> DeviceWeight:
         s2 = torch.from_numpy(np.ascontiguousarray(spec["scale2"], dtype=np.float32)).to(device)
         return DeviceWeight(M.MoeWeight(M.MOE_W_NVFP4, 0, pk.data_ptr(), sc.data_ptr(), None, s2.data_ptr()),
                             [pk, sc, s2])
+    if fmt == "fp8":
+        cd = torch.from_numpy(np.ascontiguousarray(spec["codes"])).to(device)
+        sc = torch.from_numpy(np.ascontiguousarray(spec["scales"], dtype=np.float32)).to(device)
+        return DeviceWeight(M.MoeWeight(M.MOE_W_FP8_E4M3, 0, cd.data_ptr(), sc.data_ptr(), None, None), [cd, sc])
     raise ValueError(f"unknown weight format {fmt!r}")
 
 

@@ -20,10 +20,10 @@ MOE_DEV_ERR_EXPERT_ID, MOE_DEV_ERR_CAPACITY, MOE_DEV_ERR_OFFSETS, MOE_DEV_ERR_PA
     0x1, 0x2, 0x4, 0x8, 0x10)
 MOE_MAX_EXPERTS, MOE_MAX_TOPK, MOE_MAX_LORA_RANK = 256, 16, 64
 MOE_ACT_BF16, MOE_ACT_F16 = 0, 1
-MOE_W_BF16, MOE_W_GPTQ_INT4, MOE_W_NVFP4 = 0, 1, 2
+MOE_W_BF16, MOE_W_GPTQ_INT4, MOE_W_NVFP4, MOE_W_FP8_E4M3 = 0, 1, 2, 3
 
 ACT_CODES = {"bf16": MOE_ACT_BF16, "f16": MOE_ACT_F16}
-WFMT_CODES = {"bf16": MOE_W_BF16, "gptq": MOE_W_GPTQ_INT4, "nvfp4": MOE_W_NVFP4}
+WFMT_CODES = {"bf16": MOE_W_BF16, "gptq": MOE_W_GPTQ_INT4, "nvfp4": MOE_W_NVFP4, "fp8": MOE_W_FP8_E4M3}
 
 
 class MoeError(RuntimeError):

@@ -159,6 +159,13 @@ LAYER_CASES = {
     # their owner CTA, with ragged contractions (H=1000, I=520: last k blocks of
     # 40 and 8) and ragged last column tiles
     "splitk_ragged_k": synth.MoeConfig("splitk_ragged_k", T=6, H=1000, I=520, E=4, k=2, bs=16, router="normal"),
+    # FP8 (E4M3) weights with row scales: decode (16-token tiles, four issuers), prefill
+    # (128-token tiles) with the other activation type, and a ragged I / K
+    "fp8@T64": _cfg("fp8@T64"),
+    "fp8_f16_prefill": synth.MoeConfig("fp8_f16_prefill", T=300, H=320, I=208, E=2, k=1, bs=16, act="f16",
+                                       wfmt="fp8", router="normal"),
+    "fp8_decode_ragged": synth.MoeConfig("fp8_decode_ragged", T=24, H=272, I=144, E=8, k=2, bs=16,
+                                         wfmt="fp8", router="normal"),
     # CTA-pair form with short last row tiles (a few to ~100 rows past a multiple of 256)
     # run with swapped operands; I=192 leaves the second gate/up column tile half empty
     "pair_tails": synth.MoeConfig("pair_tails", T=600, H=256, I=192, E=2, k=1, bs=16, router="normal"),
