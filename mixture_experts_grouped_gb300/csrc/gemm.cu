@@ -24,9 +24,10 @@
 //       - bf16 decode: grouped_gemm_decode_kernel, operands swapped: each
 //         weight half is an M=128 operand and NTOK tokens (16..128, one align
 //         block) the N operand;
-//       - GPTQ / NVFP4, any size: grouped_gemm_ts_kernel, weights dequantised
-//         by eight warps into TMEM and used as the M=128 A operand, NTOK tokens
-//         (128 for prefill) the N operand from shared memory.
+//       - GPTQ / NVFP4 / FP8, any size: grouped_gemm_ts_kernel, weights
+//         dequantised by eight or sixteen warps into TMEM and used as the
+//         M=128 A operand, NTOK tokens (128 for prefill) the N operand from
+//         shared memory.
 //   * Roles: TMA producer warps feed multi-stage rings; MMA issues go to
 //     double-buffered TMEM accumulators where TMEM allows; four epilogue warps
 //     drain them (tcgen05.ld -> activation -> global).
@@ -1016,17 +1017,17 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
 
 // ---- TS form: quantised weights dequantised into TMEM ----------------------------
 //
-// For GPTQ and NVFP4 weights the weight tile is the MMA's A operand and lives
-// in TMEM: eight dequantising warps each own 32 weight rows (TMEM lanes) of
-// one 128-row half and write a row's 64 k values of a k block as 32 columns
-// with tcgen05.st. The activations (NTOK token rows) are the B operand in
+// For GPTQ, NVFP4 and FP8 weights the weight tile is the MMA's A operand and
+// lives in TMEM: each set of eight dequantising warps owns 32 weight rows
+// (TMEM lanes) of one 128-row half per warp and writes a row's 64 k values of
+// a k block as 32 columns with tcgen05.st. The activations (NTOK token rows) are the B operand in
 // shared memory, fed by TMA. D is (weight row x token), two halves (gate |
 // up, or two 128-column halves of the output) of NTOK columns each. Shared
 // memory then carries only the raw quantised bytes and the activations; the
 // 16-bit weights never touch it.
 constexpr int TS_STAGES = 4;   // weight stages in TMEM (one 64-deep k block each)
 constexpr int TS_A_COL = 256;  // first TMEM column of the weight stages (64 columns each)
-constexpr int RAW2 = 18432;    // raw quantised bytes of one 128-deep stage (two k blocks)
+constexpr int RAW2 = 18432;    // bytes of one raw stage: two k blocks (GPTQ, NVFP4) or one (FP8)
 
 template <int MODE, int WFMT, int ACT, int NTOK>
 struct TsShape {
@@ -1556,10 +1557,11 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
     } else {
         // ---------------- raw quantised-weight producer (last warp) ----------------
         // A TMA copy costs its issuing thread a roughly fixed time however
-        // small it is, so a 128-deep stage (two k blocks) is fetched with as
-        // few copies as the layouts allow: GPTQ codes + scales + zero points,
-        // NVFP4 codes + scales. For an odd number of k blocks the second half
-        // of a tile's last stage is fetched but not used.
+        // small it is, so a stage is fetched with as few copies as the layouts
+        // allow: GPTQ codes + scales + zero points and NVFP4 codes + scales
+        // for a 128-deep stage (two k blocks; for an odd number of k blocks
+        // the second half of a tile's last stage is fetched but not used),
+        // FP8 codes for a 64-deep one.
         if (lane == 0) {
             const uint32_t bytes = WFMT == MOE_W_GPTQ_INT4 ? 16384u + (g64 ? 2u : 1u) * 640u
                                    : WFMT == MOE_W_NVFP4   ? 18432u
