@@ -272,6 +272,24 @@ def run_reference(args, cfg, rank, world):
     return base
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest value over the ranks (the slowest replica's time), through
+    an all-reduce on the default process group; the value itself on one rank."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, units_per_rank: float, ms: float) -> float:
+    """Units per second processed by all replicas together in ms milliseconds
+    (weak scaling: every rank processes units_per_rank)."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def config_dict(cfg, world):
     return {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top_k={cfg.k} block_size={cfg.bs} "
                         f"act={cfg.act} weights={cfg.wfmt}" + (f" lora_rank={cfg.lora_rank}" if cfg.lora_rank else ""),
@@ -356,12 +374,9 @@ def run_ours(args, cfg, rank, world, local_rank):
     clk = clocks.stop()
     gu_ms = sum(a.elapsed_time(b) for a, b in ev_gu) / args.steps
     split_ms = s0.elapsed_time(s1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     ms_per_step = ms / args.steps
-    tokens_per_s = world * cfg.T * args.steps / (ms / 1e3)
+    tokens_per_s = whole_job_rate(world, cfg.T * args.steps, ms)
 
     # ---- end to end through the public API: pinned host in, host out ----
     x_host = x.cpu().pin_memory()
@@ -385,12 +400,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         out_host.copy_(lay.out, non_blocking=True)
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * cfg.T * n_e2e / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = whole_job_rate(world, cfg.T * n_e2e, e2e_ms)
     if int(lay.err.item()) != 0:
         raise RuntimeError(f"device error word {int(lay.err.item()):#x}")
     if rank != 0:
