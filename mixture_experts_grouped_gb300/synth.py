@@ -226,9 +226,9 @@ def make_lora(cfg: MoeConfig) -> Optional[dict]:
 def make_activations(cfg: MoeConfig) -> dict:
     """Token activations ``x [T, H]`` and router logits ``[T, E]`` (f32).
 
-    * ``gemm``: ``Wr [H, E]`` f32 N(0, router_std) and ``logits = f32(x @ Wr)``
-      with the product taken in fp64 (the router GEMM itself sits before the
-      layer and is part of the input recipe);
+    * ``gemm``: ``Wr [H, E]`` f32 N(0, router_std) (returned as ``w_router``)
+      and ``logits = f32(x @ Wr)`` with the product taken in fp64 (the router
+      GEMM sits before the layer; its logits are part of the input recipe);
     * ``normal``: logits N(0, 1);
     * ``zipf``: logits N(0, 1) plus ``-1.1 * ln(e + 1)``, the log-probability of
       a Zipf(s=1.1) popularity with rank e + 1.
@@ -243,6 +243,7 @@ def make_activations(cfg: MoeConfig) -> dict:
         else:
             xf = x.astype(np.float64)
         logits = (xf @ wr.astype(np.float64)).astype(np.float32)
+        return {"x": x, "logits": logits, "w_router": wr}
     elif cfg.router == "normal":
         logits = r.standard_normal((T, E), dtype=np.float32)
     elif cfg.router == "zipf":

@@ -36,7 +36,7 @@ import numpy as np
 __all__ = [
     "bf16_bits_to_f64", "round_to_bf16", "f64_to_bf16_bits", "round_to_f16",
     "round_act", "act_to_f64", "f64_to_act",
-    "align_capacity", "route_topk_softmax", "warp_order_sum_f32",
+    "align_capacity", "router_logits", "route_topk_softmax", "warp_order_sum_f32",
     "align_block_size", "AlignResult", "ensure_group_arrays", "GroupArrayError",
     "e2m1_value", "e4m3_value", "dequant_bf16", "dequant_gptq", "dequant_nvfp4", "dequant_fp8",
     "expert_weight", "prepare_f64", "grouped_gate_up", "grouped_down", "lora_grouped_down",
@@ -132,6 +132,19 @@ def warp_order_sum_f32(v: np.ndarray) -> np.float32:
     for off in (16, 8, 4, 2, 1):
         part = [np.float32(part[l] + part[l ^ off]) for l in range(32)]
     return part[0]
+
+
+def router_logits(x: np.ndarray, act: str, w_router: np.ndarray) -> np.ndarray:
+    """Router GEMM before step a1: ``logits[t, e] = f32(sum_h x[t, h] *
+    Wr[h, e])`` with the sum taken in fp64 and rounded once to f32.
+
+    The pages route from given logits and print no router; the workloads
+    define one (a router weight ``Wr [H, E]`` f32 and logits computed once on
+    the host from the activations). ``x`` holds bf16 bits or fp16 values
+    (``act``); every product is exact in fp64.
+    """
+    xf = act_to_f64(np.asarray(x), act)
+    return (xf @ np.asarray(w_router, dtype=np.float32).astype(np.float64)).astype(np.float32)
 
 
 def route_topk_softmax(logits: np.ndarray, top_k: int, renormalize: bool = True):

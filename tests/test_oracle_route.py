@@ -122,3 +122,35 @@ def test_invalid_k_rejected():
         orc.route_topk_softmax(np.zeros((2, 4), np.float32), 5, True)
     with pytest.raises(ValueError):
         orc.route_topk_softmax(np.zeros((2, 4), np.float32), 0, True)
+
+
+def test_router_logits_match_exactly_rounded_sums():
+    # every product of a bf16 / fp16 value and an f32 weight is exact in fp64;
+    # math.fsum gives the exactly rounded sum, which rounds once to f32
+    import math
+    from mixture_experts_grouped_gb300 import synth
+    for act in ("bf16", "f16"):
+        cfg = synth.MoeConfig("r", T=7, H=96, I=8, E=5, k=2, bs=4, act=act, router="gemm", router_std=0.3)
+        a = synth.make_activations(cfg)
+        got = orc.router_logits(a["x"], act, a["w_router"])
+        xf = orc.act_to_f64(a["x"], act)
+        wf = a["w_router"].astype(np.float64)
+        for t in range(cfg.T):
+            for e in range(cfg.E):
+                want = np.float32(math.fsum(float(xf[t, h]) * float(wf[h, e]) for h in range(cfg.H)))
+                assert got[t, e] == want, (act, t, e, got[t, e], want)
+        # the workload's own logits are the same router product
+        np.testing.assert_array_equal(got, a["logits"])
+
+
+def test_router_logits_linear_in_the_weight():
+    from mixture_experts_grouped_gb300 import synth
+    cfg = synth.MoeConfig("r", T=5, H=64, I=8, E=4, k=1, bs=4, router="gemm", router_std=0.2)
+    a = synth.make_activations(cfg)
+    w = a["w_router"]
+    # a one-hot weight column picks one activation feature exactly
+    one = np.zeros_like(w)
+    one[17, 2] = 1.0
+    got = orc.router_logits(a["x"], "bf16", one)
+    np.testing.assert_array_equal(got[:, 2], orc.act_to_f64(a["x"], "bf16")[:, 17].astype(np.float32))
+    assert not got[:, [0, 1, 3]].any()
