@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline time budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--router-only", action="store_true",
+                    help="time the router GEMM + routing (moe_router_topk_softmax) alone on the workload's tokens")
     ap.add_argument("--fold-only", action="store_true",
                     help="time the decode LoRA fold (moe_lora_gather_bgmv) alone on the workload's slot-major rows")
     a = ap.parse_args()
@@ -533,6 +535,78 @@ def run_fold(args, cfg):
     }
 
 
+# FP32 fused multiply-add peak of the CUDA cores: 152 SMs x 128 lanes x 2 FLOP
+# x 2.07 GHz (maximum SM clock), the bound of the router GEMM
+ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def run_router(args, cfg):
+    """The router GEMM and routing alone (moe_router_topk_softmax): logits =
+    x . Wr with the workload's router weight (a router="gemm" workload), then
+    the top-k softmax. Replayed from CUDA graphs of 20 calls."""
+    import torch
+
+    from mixture_experts_grouped_gb300 import build as B
+    from mixture_experts_grouped_gb300 import layer as L
+    from mixture_experts_grouped_gb300 import moe as M
+    from mixture_experts_grouped_gb300 import synth
+
+    if not os.path.exists(M.LIB_PATH):
+        B.build()
+    assert cfg.router == "gemm", "--router-only needs a workload with a router weight (router=gemm)"
+    dev = torch.device("cuda", 0)
+    a = synth.make_activations(cfg)
+    x = L.act_tensor(a["x"], cfg.act, dev)
+    wr = torch.from_numpy(a["w_router"]).to(dev)
+    logits = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device=dev)
+    ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+    w = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
+
+    def launch():
+        M.moe_router_topk_softmax(x, M.ACT_CODES[cfg.act], wr, cfg.T, cfg.H, cfg.E, cfg.k, cfg.renormalize, logits,
+                                  ids, w)
+
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    R = 20
+    reps = max(1, args.steps // R)
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        launch()
+    torch.cuda.current_stream().wait_stream(side)
+    n_cap = M.moe_launch_count()
+    with torch.cuda.graph(graph):
+        for _ in range(R):
+            launch()
+    per_graph = M.moe_launch_count() - n_cap
+    graph.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        graph.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * R)
+    flops = 2.0 * cfg.T * cfg.H * cfg.E
+    tf = flops / (ms * 1e-3) / 1e12
+    return {
+        "metric": "router GEMM + top-k softmax (moe_router_topk_softmax) TFLOP/s", "value": round(tf, 3),
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": reps * R, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "f32 (bf16/fp16 activations)", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} E={cfg.E} top_k={cfg.k} act={cfg.act}",
+                   "l2": "back-to-back calls from a CUDA graph"},
+        "roofline": {"bound": "alu", "achieved": round(tf, 3), "peak": round(ALU_FP32_TFLOPS, 1), "unit": "TFLOP/s",
+                     "frac": round(tf / ALU_FP32_TFLOPS, 4),
+                     "peak_source": "152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz", "flops_per_call": flops},
+        "gpu_launches": per_graph * reps,
+    }
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -544,7 +618,9 @@ def main():
         kv = dict(item.split("=") for item in args.override.split(","))
         cfg = replace(cfg, name=f"{cfg.name}[{args.override}]",
                       **{k: type(getattr(cfg, k))(v) for k, v in kv.items()})
-    if args.fold_only:
+    if args.router_only:
+        line = run_router(args, cfg) if rank == 0 else None
+    elif args.fold_only:
         line = run_fold(args, cfg) if rank == 0 else None
     elif args.impl == "reference":
         line = run_reference(args, cfg, rank, world)

@@ -7,6 +7,7 @@
  * router and the combine, so the whole layer can be captured in a CUDA graph):
  *
  *   moe_route_topk_softmax   top-k softmax routing
+ *   moe_router_topk_softmax  the router GEMM (x . Wr) in front of it
  *   moe_align_block_size     sort (token, expert) pairs into block-padded spans
  *   moe_grouped_gate_up      grouped gate/up GEMM with the SiLU-mul fused
  *   moe_grouped_down         grouped down GEMM
@@ -167,6 +168,25 @@ uint64_t moe_launch_count(void);
 int moe_route_topk_softmax(const float* logits, int32_t* topk_ids, float* topk_weights,
                            int32_t T, int32_t E, int32_t top_k, int32_t renormalize,
                            void* stream);
+
+/*
+ * Router GEMM, then routing (SURVEY next row 4; the pages route from given
+ * logits and print no router, the workloads define one):
+ *     logits[t, e] = f32( sum_h x[t, h] * w_router[h, e] )
+ * accumulated in f32 by fused multiply-adds in ascending h, then
+ * moe_route_topk_softmax on those logits (same outputs and rules).
+ *   x             device act [T, H], 16-byte aligned
+ *   act           MOE_ACT_BF16 | MOE_ACT_F16
+ *   w_router      device f32 [H, E]
+ *   logits        device f32 [T, E] out (also the routing input)
+ *   topk_ids / topk_weights   as moe_route_topk_softmax
+ * Requirements: H % 8 == 0, 1 <= E <= MOE_MAX_EXPERTS, 1 <= top_k <= min(E,
+ * MOE_MAX_TOPK).
+ */
+int moe_router_topk_softmax(const void* x, int32_t act, const float* w_router, int32_t T,
+                            int32_t H, int32_t E, int32_t top_k, int32_t renormalize,
+                            float* logits, int32_t* topk_ids, float* topk_weights, void* stream);
+
 
 /* ---- a2: align ------------------------------------------------------------- */
 

@@ -48,6 +48,8 @@ _SIGNATURES = {
     "moe_launch_count": (c_uint64, []),
     "moe_route_topk_softmax": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
                                          c_void_p]),
+    "moe_router_topk_softmax": (c_int32, [c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32, c_int32,
+                                          c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
     "moe_align_capacity": (c_int64, [c_int64, c_int32, c_int32]),
     "moe_align_workspace_size": (c_size_t, [c_int32, c_int32]),
     "moe_align_block_size": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
@@ -133,6 +135,13 @@ def moe_launch_count() -> int:
 def moe_route_topk_softmax(logits, topk_ids, topk_weights, T, E, top_k, renormalize=True, stream=None):
     _check("moe_route_topk_softmax", lib().moe_route_topk_softmax(
         _ptr(logits), _ptr(topk_ids), _ptr(topk_weights), T, E, top_k, 1 if renormalize else 0, _stream(stream)))
+
+
+def moe_router_topk_softmax(x, act, w_router, T, H, E, top_k, renormalize, logits, topk_ids, topk_weights,
+                            stream=None):
+    _check("moe_router_topk_softmax", lib().moe_router_topk_softmax(
+        _ptr(x), act, _ptr(w_router), T, H, E, top_k, 1 if renormalize else 0, _ptr(logits), _ptr(topk_ids),
+        _ptr(topk_weights), _stream(stream)))
 
 
 def moe_align_capacity(P, E, block_size) -> int:

@@ -82,6 +82,10 @@ def test_workspace_sizes(moe):
     lambda m: m.moe_route_topk_softmax(0, 0, 0, 4, 300, 2, True, 0),            # E > MAX
     lambda m: m.moe_route_topk_softmax(0, 0, 0, 4, 8, 9, True, 0),              # top_k > E
     lambda m: m.moe_route_topk_softmax(0, 0, 0, 4, 64, 17, True, 0),            # top_k > MAX_TOPK
+    lambda m: m.moe_router_topk_softmax(16, 0, 16, 4, 100, 8, 2, True, 16, 16, 16, 0),   # H % 8
+    lambda m: m.moe_router_topk_softmax(16, 2, 16, 4, 128, 8, 2, True, 16, 16, 16, 0),   # act
+    lambda m: m.moe_router_topk_softmax(16, 0, 16, 4, 128, 300, 2, True, 16, 16, 16, 0), # E > MAX
+    lambda m: m.moe_router_topk_softmax(16, 0, None, 4, 128, 8, 2, True, 16, 16, 16, 0), # NULL weight
     lambda m: m.moe_route_topk_softmax(0, 0, 0, 4, 8, 2, True, 0),              # NULL pointers
     lambda m: m.moe_align_block_size(0, 32, 257, 16, 1024, 8, 8, 8, 8, 8, 0, 8, 1 << 20, 0),   # E > 256
     lambda m: m.moe_align_block_size(0, 32, 8, 0, 1024, 8, 8, 8, 8, 8, 0, 8, 1 << 20, 0),     # bs = 0

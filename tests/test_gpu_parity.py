@@ -248,6 +248,32 @@ def test_layer_end_to_end(dev, name):
     ffn_close(g["out"], ref.out, f"{name}: layer output")
 
 
+@pytest.mark.parametrize("T,H,E,k,act", [(16, 128, 8, 2, "bf16"), (64, 4096, 8, 2, "bf16"), (100, 2048, 128, 8, "bf16"),
+                                         (45, 200, 60, 6, "f16"), (33, 1024, 256, 8, "f16")])
+def test_router_gemm_then_routing(dev, T, H, E, k, act):
+    """Router GEMM on the GPU: logits within the f32 accumulation bound of the
+    oracle's exactly rounded product, and the routing of those logits
+    bit-exact (selection, order and weights)."""
+    import torch
+    from mixture_experts_grouped_gb300 import layer as L, moe
+    cfg = synth.MoeConfig("router", T=T, H=H, I=8, E=E, k=k, bs=16, act=act, router="gemm", router_std=0.05)
+    a = synth.make_activations(cfg)
+    want = orc.router_logits(a["x"], act, a["w_router"]).astype(np.float64)
+    xd = L.act_tensor(a["x"], act, dev)
+    wd = torch.from_numpy(a["w_router"]).to(dev)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    moe.moe_router_topk_softmax(xd, moe.ACT_CODES[act], wd, T, H, E, k, True, logits, ids, w)
+    torch.cuda.synchronize()
+    got = logits.cpu().numpy()
+    mag = np.abs(orc.act_to_f64(a["x"], act)) @ np.abs(a["w_router"].astype(np.float64))
+    assert np.all(np.abs(got - want) <= 2.0 * H * 2.0 ** -24 * mag + 1e-30), float(np.max(np.abs(got - want) / mag))
+    ref_ids, ref_w = orc.route_topk_softmax(got, k, True)
+    np.testing.assert_array_equal(ids.cpu().numpy(), ref_ids)
+    np.testing.assert_array_equal(w.cpu().numpy().view(np.uint32), np.asarray(ref_w, np.float32).view(np.uint32))
+
+
 @pytest.mark.parametrize("x_gather,adapter,rank", [(0, False, 16), (1, True, 16), (0, True, 40), (1, False, 64)])
 def test_lora_gather_bgmv_matches_oracle(dev, x_gather, adapter, rank):
     """Decode gather fold on slot-major rows: folded rows within tolerance of the
