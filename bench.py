@@ -16,6 +16,11 @@ barriers and the max over ranks is reported (weak scaling).
 
 --impl reference times the CPU oracle (plain numpy, fp64) on the host cores,
 each step a small sub-batch of the same workload.
+
+Two single-call micro-benchmarks print their own JSON line instead:
+--fold-only times the decode LoRA fold (moe_lora_gather_bgmv) on the
+workload's slot-major rows, --router-only the router GEMM + routing
+(moe_router_topk_softmax) on a workload with a router weight.
 """
 
 from __future__ import annotations
