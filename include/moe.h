@@ -170,11 +170,12 @@ int moe_route_topk_softmax(const float* logits, int32_t* topk_ids, float* topk_w
                            void* stream);
 
 /*
- * Router GEMM, then routing (SURVEY next row 4; the pages route from given
- * logits and print no router, the workloads define one):
+ * Router GEMM, then routing (the pages route from given logits and print no
+ * router; the workloads define one):
  *     logits[t, e] = f32( sum_h x[t, h] * w_router[h, e] )
- * accumulated in f32 by fused multiply-adds in ascending h, then
- * moe_route_topk_softmax on those logits (same outputs and rules).
+ * accumulated in f32 by fused multiply-adds in a fixed order (the same on
+ * every run), then moe_route_topk_softmax on those logits (same outputs and
+ * rules).
  *   x             device act [T, H], 16-byte aligned
  *   act           MOE_ACT_BF16 | MOE_ACT_F16
  *   w_router      device f32 [H, E]
