@@ -148,6 +148,19 @@ const char* moe_last_error(void);
 /* Number of kernels this library has launched in the process so far. */
 uint64_t moe_launch_count(void);
 
+/*
+ * Time limit, in nanoseconds, of every pipeline wait inside the grouped GEMM
+ * kernels launched after this call (process-wide; 0 restores the default of
+ * 2 s). A wait that runs out sets MOE_DEV_ERR_TIMEOUT in the call's err_word;
+ * the kernel then lets its copies and MMAs in flight land, frees its tensor
+ * memory and returns, so the context stays usable. Afterwards the caller
+ * zeroes the GEMM workspaces' split-K areas before the next call. This is a
+ * testing hook (it lets a test make the waits run out on purpose, as the
+ * pages' status-return error model asks of every failure); production
+ * callers leave the default. Returns the previous limit.
+ */
+uint64_t moe_set_wait_limit_ns(uint64_t ns);
+
 /* ---- a1: routing --------------------------------------------------------- */
 
 /*
@@ -238,8 +251,9 @@ int moe_align_block_size(const int32_t* topk_ids, int32_t P, int32_t E, int32_t 
  * P <= MOE_ALIGN_NOALLOC_MAX_PAIRS pairs and E <= MOE_MAX_EXPERTS experts
  * (about 1.1 MiB held on every GPU that loads the library until exit); a
  * larger P is rejected with MOE_ERR_INVALID. The first call on a device looks
- * up the array's device address with that device current, so make that first
- * call before any stream capture. Nothing is allocated or freed. All calls on
+ * up the array's device address with that device current (and so does the
+ * first call after the device's context was destroyed and made again, e.g. by
+ * cudaDeviceReset), so make that first call before any stream capture. Nothing is allocated or freed. All calls on
  * a device share the array: calls that overlap on the GPU (unordered streams)
  * race on it. Nothing in it needs to start at zero.
  */

@@ -336,26 +336,53 @@ static __device__ __align__(256) uint8_t g_align_noalloc_scratch[kNoAllocScratch
 
 namespace {
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[256] = {};  // device address of the array, per device ordinal
+// device address of the array per device ordinal, with the context it was
+// looked up in: a context destroyed and made again (cudaDeviceReset) reloads
+// the module, so the address is looked up again for the new context
+struct NoAllocSlot {
+    CUcontext ctx;
+    void* ptr;
+};
+NoAllocSlot g_noalloc[256] = {};
 
-// Looked up once per device, with that device current: in host code the
-// array's name is only a host-side stand-in, never a device address.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
+
+// Looked up with the device current, once per device and context: in host
+// code the array's name is only a host-side stand-in, never a device address.
 int noalloc_scratch(void** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return moe::fail(MOE_ERR_CUDA, "moe_align_block_size_noalloc: cudaGetDevice: %s",
                                            cudaGetErrorString(e));
     if (dev < 0 || dev >= 256) return moe::fail(MOE_ERR_UNSUPPORTED, "moe_align_block_size_noalloc: device %d", dev);
+    CtxGetCurrentFn get = ctx_get_current();
+    if (!get) return moe::fail(MOE_ERR_CUDA, "moe_align_block_size_noalloc: cuCtxGetCurrent is unavailable");
+    CUcontext ctx = nullptr;  // NULL until the runtime has made the device's context current
+    if (get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_ptr[dev] == nullptr) {
+    if (ctx == nullptr || g_noalloc[dev].ptr == nullptr || g_noalloc[dev].ctx != ctx) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_align_noalloc_scratch);
+        e = cudaGetSymbolAddress(&p, g_align_noalloc_scratch);  // makes the context current if needed
         if (e != cudaSuccess || p == nullptr)
             return moe::fail(MOE_ERR_CUDA, "moe_align_block_size_noalloc: cudaGetSymbolAddress: %s",
                              cudaGetErrorString(e));
-        g_noalloc_ptr[dev] = p;
+        if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+            return moe::fail(MOE_ERR_CUDA, "moe_align_block_size_noalloc: cannot read the current context");
+        g_noalloc[dev] = NoAllocSlot{ctx, p};
     }
-    *out = g_noalloc_ptr[dev];
+    *out = g_noalloc[dev].ptr;
     return MOE_OK;
 }
 }  // namespace

@@ -25,6 +25,7 @@ int check_launch(const char* what);                    // cudaGetLastError after
 void count_launch(uint64_t n = 1);                     // kernels this library launched
 int sm_count();                                        // SMs of the current device
 int set_smem_limit(const void* kernel, int bytes);     // opt in to > 48 KB dynamic smem
+uint64_t wait_limit_ns();                              // pipeline wait limit for the next launches
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -171,25 +172,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// How long any pipeline wait may last before the kernel gives up (the whole
-// layer at the largest supported size runs in a few milliseconds).
+// How long a pipeline wait may last, by default, before the kernel gives up
+// (the whole layer at the largest supported size runs in a few
+// milliseconds). Each launch carries its own limit (WaitCtx::limit_ns); the
+// host takes it from wait_limit_ns().
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// What a bounded wait needs: the CTA's abort flag (raised by whichever role
+// gives up first, so the others stop waiting too), the device error word and
+// the launch's time limit.
+struct WaitCtx {
+    volatile int* abort;
+    int32_t* err;
+    uint64_t limit_ns;
+};
+
 // Wait for the phase of `bar` with parity `parity` to complete. Gives up
-// (returns false) when `abort_flag` is raised by another role of the CTA, or
-// after kWaitLimitNs, in which case it raises the flag itself and records
-// MOE_DEV_ERR_TIMEOUT in `err`.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* err) {
+// (returns false) when the CTA's abort flag is raised by another role, or
+// after w.limit_ns, in which case it raises the flag itself and records
+// MOE_DEV_ERR_TIMEOUT in the error word.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(a, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            set_err(err, MOE_DEV_ERR_TIMEOUT);
+        if (*w.abort) return false;
+        if (globaltimer_ns() - t0 > w.limit_ns) {
+            *w.abort = 1;
+            set_err(w.err, MOE_DEV_ERR_TIMEOUT);
             return false;
         }
     }
@@ -209,15 +220,15 @@ __device__ __forceinline__ void st_release_gpu(int* p, int v) {
 // Wait until the global flag *f is nonzero, with the same limit and abort
 // rule as mbar_wait. Every calling thread observes the flag itself (acquire),
 // so each sees the data released before it.
-__device__ __forceinline__ bool flag_wait(const int* f, volatile int* abort_flag, int32_t* err) {
+__device__ __forceinline__ bool flag_wait(const int* f, const WaitCtx& w) {
     if (ld_acquire_gpu(f)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (ld_acquire_gpu(f)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            set_err(err, MOE_DEV_ERR_TIMEOUT);
+        if (*w.abort) return false;
+        if (globaltimer_ns() - t0 > w.limit_ns) {
+            *w.abort = 1;
+            set_err(w.err, MOE_DEV_ERR_TIMEOUT);
             return false;
         }
         __nanosleep(64);
@@ -252,6 +263,13 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 }
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// the two halves of cluster_sync_all, for work between the arrival and the wait
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ---- TMA ------------------------------------------------------------------

@@ -63,6 +63,7 @@ struct GemmParams {
     const float* scale2;
     int group_size;
     int32_t* err;
+    uint64_t wait_ns;  // how long a pipeline wait may last before the kernel gives up
     int block_size;  // align block size: spans are multiples of it, padding is a span's last < block_size rows
     int pad_free;    // the kernel's tile height is a multiple of block_size: no tile holds padding only
     const float* row_scale;  // FP8: fp32 scale per weight row [E, n_w]
@@ -476,7 +477,7 @@ __device__ __forceinline__ void decode_store_chunk(const float (&a)[16], const f
 // false when a wait gave up.
 template <int MODE, int NTOK, int NACC>
 __device__ __forceinline__ bool decode_split_epilogue(const GemmParams& p, uint64_t* tfull, uint32_t aph,
-                                                   volatile int* abort_flag, bool to_owner, int last_peer,
+                                                   const WaitCtx& wc, bool to_owner, int last_peer,
                                                    uint32_t tacc, int q, int lane, int nvalid,
                                                    __nv_bfloat16* stg, int m0, int colw) {
     const uint32_t taddr = tacc + (static_cast<uint32_t>(q * 32) << 16);
@@ -484,7 +485,7 @@ __device__ __forceinline__ bool decode_split_epilogue(const GemmParams& p, uint6
     const size_t lane_off = static_cast<size_t>(q) * (NTOK / 16) * 256 + lane;
     constexpr size_t SLICE4 = SK_SLICE_FLOATS / 4;
     if (to_owner) {
-        if (!mbar_wait(tfull, aph, abort_flag, p.err)) return false;
+        if (!mbar_wait(tfull, aph, wc)) return false;
         tc_fence_after();
         float4* d = reinterpret_cast<float4*>(p.sk_part) + blockIdx.x * SLICE4 + lane_off;
 #pragma unroll 1
@@ -508,12 +509,12 @@ __device__ __forceinline__ bool decode_split_epilogue(const GemmParams& p, uint6
     // CTA's own MMAs may still run
     const int first_peer = blockIdx.x + 1;
     for (int pc = first_peer; pc <= last_peer; ++pc)
-        if (!flag_wait(p.sk_flag + pc * 4 + q, abort_flag, p.err)) return false;
+        if (!flag_wait(p.sk_flag + pc * 4 + q, wc)) return false;
     const float4* peer0 = reinterpret_cast<const float4*>(p.sk_part) + first_peer * SLICE4 + lane_off;
     float4 nx[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) nx[j] = __ldcg(peer0 + (j & 3) * 32 + (j >> 2) * 128);
-    if (!mbar_wait(tfull, aph, abort_flag, p.err)) return false;
+    if (!mbar_wait(tfull, aph, wc)) return false;
     tc_fence_after();
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll 1
@@ -563,7 +564,7 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
     uint8_t* sW = smem + STAGES * S::X_STAGE;
     uint8_t* sStg = sW + STAGES * W_STAGE;
     SmemTail& s = *reinterpret_cast<SmemTail*>(sStg + S::STG_BYTES);
-    volatile int* abort_flag = &s.abort_flag;
+    const WaitCtx wc{&s.abort_flag, p.err, p.wait_ns};
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -617,7 +618,7 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
                 int c0, c1;
                 half_bases<MODE>(p, t.n0, c0, c1);
                 for (int kb = it.kb0; kb < it.kb1; ++kb) {
-                    if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    if (!mbar_wait(&s.empty[stage], phase ^ 1, wc)) { ok = false; break; }
                     mbar_arrive_expect_tx(&s.full[stage], S::X_STAGE + W_STAGE);
                     tma_load_2d(sX + stage * S::X_STAGE, &tmX, kb * BK, t.m0, &s.full[stage]);
                     uint8_t* w = sW + stage * W_STAGE;
@@ -647,11 +648,11 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
                 const int acc = local & 1;
                 const uint32_t aph = (local >> 1) & 1;
                 ++local;
-                if (!mbar_wait(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
+                if (!mbar_wait(&s.tempty[acc], aph ^ 1, wc)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * S::ACC;
                 for (int kb = it.kb0; kb < it.kb1; ++kb) {
-                    if (!mbar_wait(&s.full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+                    if (!mbar_wait(&s.full[stage], phase, wc)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t xd = sw128_desc(smem_u32(sX + stage * S::X_STAGE));
                     const uint64_t wd = sw128_desc(smem_u32(sW + stage * W_STAGE));
@@ -693,14 +694,14 @@ grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
             const int last_peer = SkWalk::last_peer(plan, KB, it);
             if (it.kb0 > 0 || last_peer > static_cast<int>(blockIdx.x)) {
                 // a piece of a cut tile (stream-K)
-                if (!decode_split_epilogue<MODE, NTOK, S::NACC>(p, &s.tfull[acc], aph, abort_flag, it.kb0 > 0,
+                if (!decode_split_epilogue<MODE, NTOK, S::NACC>(p, &s.tfull[acc], aph, wc, it.kb0 > 0,
                                                                  last_peer, tmem_base + acc * S::ACC, q, lane,
                                                                  nvalid, stg, t.m0, colw)) {
                     ok = false;
                     break;
                 }
             } else {
-                if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
+                if (!mbar_wait(&s.tfull[acc], aph, wc)) break;
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * S::ACC;
 #pragma unroll 1
@@ -813,7 +814,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
     uint8_t* sB = smem + PAIR_STAGES * PAIR_A;
     uint8_t* sStg = sB + PAIR_STAGES * PAIR_B;
     SmemTail& s = *reinterpret_cast<SmemTail*>(sStg + PAIR_STG);
-    volatile int* abort_flag = &s.abort_flag;
+    const WaitCtx wc{&s.abort_flag, p.err, p.wait_ns};
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -877,7 +878,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
                 const bool w5 = MODE == MODE_GATE_UP && swapped;
                 const int g5 = t.n0 / 8 + 8 * static_cast<int>(rank);
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    if (!mbar_wait(&s.empty[stage], phase ^ 1, wc)) { ok = false; break; }
                     if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2 * (PAIR_A + PAIR_B));
                     const uint32_t bar = leader_full0 + stage * 8;
                     tma_load_2d_pair(sA + stage * PAIR_A, &tmX, kb * BK, arow, bar);
@@ -907,13 +908,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
                 const int acc = local & 1;
                 const uint32_t aph = (local >> 1) & 1;
                 ++local;
-                if (!mbar_wait(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
+                if (!mbar_wait(&s.tempty[acc], aph ^ 1, wc)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * 256;
                 const bool swapped = t.rows <= 128;
                 const uint32_t idesc_sw = f16_idesc(ACT, 256, (t.rows + 15) & ~15);
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&s.full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+                    if (!mbar_wait(&s.full[stage], phase, wc)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t ad = sw128_desc(smem_u32(sA + stage * PAIR_A));
                     const uint64_t bd = sw128_desc(smem_u32(sB + stage * PAIR_B));
@@ -949,7 +950,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
             const uint32_t aph = (local >> 1) & 1;
             ++local;
             const int nvalid = valid_rows(p, s, t, lane);  // its loads overlap the wait
-            if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
+            if (!mbar_wait(&s.tfull[acc], aph, wc)) break;
             tc_fence_after();
             const int row = static_cast<int>(rank) * 128 + lrow;
             const bool row_ok = row < nvalid;
@@ -1276,7 +1277,7 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
     uint8_t* sR = sX + XSTAGES * S::X_STAGE;
     uint8_t* sStg = sR + RSTAGES * RAW2;
     SmemTail& s = *reinterpret_cast<SmemTail*>(sStg + S::STG_BYTES);
-    volatile int* abort_flag = &s.abort_flag;
+    const WaitCtx wc{&s.abort_flag, p.err, p.wait_ns};
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -1337,7 +1338,7 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
                 const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
                 if (tile_is_padding(p, t)) continue;
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    if (!mbar_wait(&s.empty[stage], phase ^ 1, wc)) { ok = false; break; }
                     mbar_arrive_expect_tx(&s.full[stage], S::X_STAGE);
                     tma_load_2d(sX + stage * S::X_STAGE, &tmX, kb * BK, t.m0, &s.full[stage]);
                     ++issued;
@@ -1366,14 +1367,14 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
                 ++local;
                 const int first = (rset - g0 % S::NR + S::NR) % S::NR;  // its first kb in this tile
                 if (first < KB) {
-                    if (!mbar_wait(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
+                    if (!mbar_wait(&s.tempty[acc], aph ^ 1, wc)) break;
                     tc_fence_after();
                     const uint32_t d = tmem_base + acc * S::ACC;
                     for (int kb = first; kb < KB; kb += S::NR) {
                         const int g = g0 + kb;
                         const int xs = g % XSTAGES, as = g % ASTAGES;
-                        if (!mbar_wait(&s.full[xs], static_cast<uint32_t>((g / XSTAGES) & 1), abort_flag, p.err) ||
-                            !mbar_wait(&s.afull[as], static_cast<uint32_t>((g / ASTAGES) & 1), abort_flag, p.err)) {
+                        if (!mbar_wait(&s.full[xs], static_cast<uint32_t>((g / XSTAGES) & 1), wc) ||
+                            !mbar_wait(&s.afull[as], static_cast<uint32_t>((g / ASTAGES) & 1), wc)) {
                             ok = false;
                             break;
                         }
@@ -1431,7 +1432,7 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
                 const int n1 = MODE == MODE_GATE_UP ? p.n_out + n : n + 128;
                 if ((MODE == MODE_GATE_UP ? n : n + 128) < p.n_out) s2b = __ldg(rs + n1);
             }
-            if (!mbar_wait(&s.tfull[acc], aph, abort_flag, p.err)) break;
+            if (!mbar_wait(&s.tfull[acc], aph, wc)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * S::ACC;
             const int colw = t.n0 + q * 32;  // this warp's first column (half 0)
@@ -1505,11 +1506,11 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
             const int rs = f_rs0 + f_kb / KPR;
             for (; rs_next < rs; ++rs_next) {  // stages with none of this set's items
                 if (!mbar_wait(&s.raw_full[rs_next % RSTAGES], static_cast<uint32_t>((rs_next / RSTAGES) & 1),
-                               abort_flag, p.err))
+                               wc))
                     return false;
                 release(rs_next);
             }
-            if (!mbar_wait(&s.raw_full[rs % RSTAGES], static_cast<uint32_t>((rs / RSTAGES) & 1), abort_flag, p.err))
+            if (!mbar_wait(&s.raw_full[rs % RSTAGES], static_cast<uint32_t>((rs / RSTAGES) & 1), wc))
                 return false;
             load_raw_row<WFMT>(sR + (rs % RSTAGES) * RAW2, h, r, f_kb % KPR, g64, x);
 #pragma unroll
@@ -1545,7 +1546,7 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
                 fp8_row<ACT>(cur.w, o);
             }
             const int as = it % ASTAGES;
-            if (!mbar_wait(&s.aempty[as], static_cast<uint32_t>(((it / ASTAGES) & 1) ^ 1), abort_flag, p.err)) break;
+            if (!mbar_wait(&s.aempty[as], static_cast<uint32_t>(((it / ASTAGES) & 1) ^ 1), wc)) break;
             tc_fence_after();  // the MMAs that read this TMEM stage have completed
             tmem_st32(trow + as * 64, o);
             tmem_st_wait();
@@ -1573,7 +1574,7 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
                 const TileInfo t = decode_tile<XROWS>(s, E, tile, S::OUT_COLS);
                 if (tile_is_padding(p, t)) continue;
                 for (int kr = 0; kr < KR; ++kr) {
-                    if (!mbar_wait(&s.raw_empty[rstage], rphase ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    if (!mbar_wait(&s.raw_empty[rstage], rphase ^ 1, wc)) { ok = false; break; }
                     uint64_t* bar = &s.raw_full[rstage];
                     uint8_t* rw = sR + rstage * RAW2;
                     mbar_arrive_expect_tx(bar, bytes);
@@ -2006,6 +2007,7 @@ extern "C" int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* 
     p.row_scale = static_cast<const float*>(w_gate_up->scales);
     p.group_size = w_gate_up->group_size;
     p.err = err_word;
+    p.wait_ns = moe::wait_limit_ns();
     p.block_size = block_size;
     moe::set_splitk(p, static_cast<uint8_t*>(workspace) + moe::gather_bytes(max_padded, H));
     return moe::dispatch<moe::MODE_GATE_UP>(w_gate_up->format, act, ntok, m, p, st, who);
@@ -2049,6 +2051,7 @@ extern "C" int moe_grouped_down(const void* h, int32_t act, const MoeWeight* w_d
     p.row_scale = static_cast<const float*>(w_down->scales);
     p.group_size = w_down->group_size;
     p.err = err_word;
+    p.wait_ns = moe::wait_limit_ns();
     p.block_size = block_size;
     moe::set_splitk(p, workspace);
     return moe::dispatch<moe::MODE_DOWN>(w_down->format, act, ntok, m, p, static_cast<cudaStream_t>(stream), who);

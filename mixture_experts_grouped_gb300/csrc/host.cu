@@ -14,6 +14,7 @@ namespace moe {
 namespace {
 thread_local std::string g_last_error;
 std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -47,6 +48,8 @@ int check_launch(const char* what) {
 }
 
 void count_launch(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 int sm_count() {
     static int cached[64] = {0};
@@ -159,6 +162,10 @@ extern "C" {
 const char* moe_last_error(void) { return moe::g_last_error.c_str(); }
 
 uint64_t moe_launch_count(void) { return moe::g_launches.load(std::memory_order_relaxed); }
+
+uint64_t moe_set_wait_limit_ns(uint64_t ns) {
+    return moe::g_wait_limit_ns.exchange(ns ? ns : moe::kWaitLimitNs, std::memory_order_relaxed);
+}
 
 int64_t moe_align_capacity(int64_t P, int32_t E, int32_t block_size) {
     if (P < 0 || E < 1 || block_size < 1) return -1;

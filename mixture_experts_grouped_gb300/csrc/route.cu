@@ -20,21 +20,12 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
     return va > vb || (va == vb && ia < ib);
 }
 
-__global__ void __launch_bounds__(32 * kRowsPerBlock)
-route_topk_softmax_kernel(const float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ w, int T,
-                          int E, int k, int renorm) {
-    pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
-    if (row >= T) return;
-    const float* lrow = logits + static_cast<size_t>(row) * E;
-
-    float v[kPerLane];
-#pragma unroll
-    for (int j = 0; j < kPerLane; ++j) {
-        const int i = lane + 32 * j;
-        v[j] = (i < E) ? __ldg(lrow + i) : 0.0f;
-    }
+// Top-k softmax of one row whose logits sit in registers: lane l holds
+// v[j] = logit of expert l + 32 j (E <= 256). Writes the row's top_k ids and
+// weights (lanes < top_k). Shared by the routing kernel and the fused router
+// kernel, so both take the same decisions in the same arithmetic.
+__device__ __forceinline__ void route_row(const float (&v)[kPerLane], int lane, int E, int k, int renorm,
+                                          int32_t* __restrict__ ids_row, float* __restrict__ w_row) {
     uint32_t taken = 0;  // bit j: element lane + 32 j already selected (or absent)
 #pragma unroll
     for (int j = 0; j < kPerLane; ++j)
@@ -103,155 +94,280 @@ route_topk_softmax_kernel(const float* __restrict__ logits, int32_t* __restrict_
         denom = part;
     }
     if (lane < k) {
-        ids[static_cast<size_t>(row) * k + lane] = si;
-        w[static_cast<size_t>(row) * k + lane] = __fdiv_rn(e_mine, denom);
+        ids_row[lane] = si;
+        w_row[lane] = __fdiv_rn(e_mine, denom);
     }
 }
 
-// ---- router GEMM: logits = x . Wr ----------------------------------------------
+__global__ void __launch_bounds__(32 * kRowsPerBlock)
+route_topk_softmax_kernel(const float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ w, int T,
+                          int E, int k, int renorm) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+    if (row >= T) return;
+    const float* lrow = logits + static_cast<size_t>(row) * E;
+    float v[kPerLane];
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) {
+        const int i = lane + 32 * j;
+        v[j] = (i < E) ? __ldg(lrow + i) : 0.0f;
+    }
+    route_row(v, lane, E, k, renorm, ids + static_cast<size_t>(row) * k, w + static_cast<size_t>(row) * k);
+}
+
+// ---- router GEMM fused with routing ----------------------------------------------
 //
 // The workloads define the router the pages leave out: logits[t, e] =
-// sum_h x[t, h] * Wr[h, e] with Wr f32 [H, E] (E <= 256, a few hundred FLOPs
-// per token: the work is small and latency-bound). A block computes 32 tokens
-// (lane = token) x E logits in fp32 fused multiply-adds. Its eight warps split
-// the experts into NG groups of up to 32 and the contraction into S = 8 / NG
-// slices; each D-deep chunk of activations (as f32, rows padded against bank
-// conflicts) and of Wr is staged in shared memory while the next chunk's
-// loads are in flight in registers. Slice s of a chunk is h = h0 + s * D / S
-// ... h0 + (s + 1) * D / S - 1 in ascending order; the S slice sums are added
-// in order 0, 1, ... at the end, so the result does not depend on timing.
+// sum_h x[t, h] * Wr[h, e] with Wr f32 [H, E] (E <= 256). At E = 8 it is a
+// few FLOPs per activation byte, so the kernel is built to stream x at HBM
+// rate with many CTAs in flight; at E >= 128 it is bound by the fp32
+// fused multiply-adds.
+//   * A cluster of CS CTAs (CS = 1, 2, 4 or 8) takes 32 tokens (lane =
+//     token); CTA c of the cluster takes the contraction range [c HR,
+//     (c + 1) HR). Its eight warps are G expert groups (EG = 8, 16 or 32
+//     experts, one accumulator register each) times S = 8 / G contraction
+//     slices.
+//   * The CTA's router-weight rows are staged in shared memory in chunks of
+//     HC rows (two buffers, cp.async); each lane reads its token's
+//     activations straight from global memory as 16-byte vectors (HC / S / 8
+//     of them per chunk, the next chunk's in flight while the current one is
+//     used).
+//   * Sums: a lane accumulates its slice of each chunk in ascending h by
+//     fused multiply-adds; the S slice sums of a CTA are added in slice
+//     order, then the CS CTA sums in rank order, read through distributed
+//     shared memory, so the result does not depend on timing.
+//   * CTA c then finishes tokens [c 32 / CS, (c + 1) 32 / CS) of the
+//     cluster: it writes their logits and routes them, one warp per token,
+//     with the same route_row as moe_route_topk_softmax.
 constexpr int kRtTok = 32, kRtThreads = 256, kRtWarps = kRtThreads / 32;
-constexpr int kRtMaxD = 512;                            // chunk depth at most
-constexpr int kRtXPer = kRtTok * kRtMaxD / 4 / kRtThreads;  // 4-feature activation loads per thread: 16
-constexpr int kRtWPer = 8192 / kRtThreads;               // weight words per thread at most: 32 (D * E <= 8192)
+constexpr int kRtMaxVec = 4;       // 16-byte activation vectors per lane per chunk at most
+constexpr int kRtChunkFloats = 8192;  // router-weight floats per staged chunk at most (32 KB)
+constexpr int kRtMaxSmem = 100 * 1024;  // shared memory of the largest plan (E = 256: 96 KB)
 
-struct RtShape {
-    int eg, ng, s, d;  // experts per group, groups, slices, chunk depth
+struct RtPlan {
+    int eg, g, s;  // experts per group, groups, contraction slices
+    int ep;        // E rounded up to 4: row stride of the staged weights
+    int hc;        // weight rows per chunk (a multiple of 8 S)
+    int cs;        // CTAs per cluster
+    int hr;        // contraction rows per CTA (a multiple of 8 S)
 };
 
-__host__ __device__ inline RtShape rt_shape(int E) {
-    RtShape r;
-    r.eg = E < 32 ? E : 32;
-    r.ng = (E + r.eg - 1) / r.eg;                        // <= 8
-    r.s = kRtWarps / r.ng;                               // >= 1
-    // as deep as D * E <= 8192 weight words allows, at most 512: few chunks,
-    // so few load latencies in a row
-    const int m = 256 / E;                               // 8192 / (32 E)
-    r.d = 32 * (m < 1 ? 1 : (m > 16 ? 16 : m));          // 32 .. 512
+inline RtPlan rt_plan(int H, int E) {
+    RtPlan r;
+    r.eg = E <= 8 ? 8 : (E <= 16 ? 16 : 32);
+    r.g = (E + r.eg - 1) / r.eg;  // <= 8
+    r.s = kRtWarps / r.g;         // >= 1
+    r.ep = (E + 3) / 4 * 4;
+    const int step = 8 * r.s;
+    int hc = kRtChunkFloats / r.ep / step * step;
+    if (hc > kRtMaxVec * step) hc = kRtMaxVec * step;
+    r.hc = hc < step ? step : hc;
+    // as many CTAs per token block as leave each warp slice at least one
+    // 16-byte vector (8 h) of the contraction
+    r.cs = 8;
+    while (r.cs > 1 && H < r.cs * step) r.cs >>= 1;
+    const int per = (H + r.cs - 1) / r.cs;
+    r.hr = (per + step - 1) / step * step;
     return r;
 }
 
-template <int ACT>
+inline size_t rt_smem_bytes(const RtPlan& r) {
+    const size_t wbuf = static_cast<size_t>(2 * r.hc > kRtTok ? 2 * r.hc : kRtTok) * r.ep;  // two chunks / finals
+    const size_t red = static_cast<size_t>(r.s) * kRtTok * r.ep;
+    return (wbuf + red) * sizeof(float);
+}
+
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+template <int ACT, int EG>
 __global__ void __launch_bounds__(kRtThreads)
-router_logits_kernel(const typename Act<ACT>::T* __restrict__ x, const float* __restrict__ wr,
-                     float* __restrict__ logits, int T, int H, int E) {
+router_topk_kernel(const typename Act<ACT>::T* __restrict__ x, const float* __restrict__ wr,
+                   float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ wout, int T, int H,
+                   int E, int k, int renorm, const RtPlan pl) {
     pdl_wait();
     extern __shared__ float rt_smem[];
-    const RtShape sh = rt_shape(E);
-    const int D = sh.d, XP = D + 1;
-    float* xs = rt_smem;                  // [32 tokens][D + 1]
-    float* ws = rt_smem + kRtTok * XP;    // [D][E]
+    const int wstride = (2 * pl.hc > kRtTok ? 2 * pl.hc : kRtTok) * pl.ep;
+    float* wbuf = rt_smem;                    // two weight chunks [hc][ep]; afterwards the finals [32][ep]
+    float* red = rt_smem + wstride;           // slice sums [s][32 tokens][ep]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t0 = blockIdx.x * kRtTok;
-    const int g = warp / sh.s, sl = warp % sh.s;       // expert group, contraction slice
-    const bool active = g < sh.ng;
-    const int e0 = g * sh.eg;
-    const int hs = D / sh.s;                           // h per slice per chunk
-    // staging map: activation loads of 4 features, thread -> (token, feature)
-    const int xq = D / 4;                              // 4-feature groups per token row
-    uint2 xr[kRtXPer];
-    float wv[kRtWPer];
-    auto load_chunk = [&](int h0) {
-#pragma unroll
-        for (int i = 0; i < kRtXPer; ++i) {
-            const int idx = tid + i * kRtThreads;      // < 32 * xq when i < 32 * xq / 256
-            const int tok = idx / xq, h = h0 + (idx % xq) * 4;
-            const int t = t0 + tok;
-            xr[i] = make_uint2(0u, 0u);
-            if (idx < kRtTok * xq && t < T && h < H)   // H % 8 == 0: the 4 features are in range
-                xr[i] = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(t) * H + h);
-        }
-        const int n = (H - h0 < D ? H - h0 : D) * E;
-#pragma unroll
-        for (int i = 0; i < kRtWPer; ++i) {
-            const int idx = tid + i * kRtThreads;
-            wv[i] = idx < n ? __ldg(wr + static_cast<size_t>(h0) * E + idx) : 0.0f;
-        }
-    };
-    auto store_chunk = [&]() {
-#pragma unroll
-        for (int i = 0; i < kRtXPer; ++i) {
-            const int idx = tid + i * kRtThreads;
-            if (idx < kRtTok * xq) {
-                const int tok = idx / xq, hq = (idx % xq) * 4;
-                const float2 a = Act<ACT>::unpack2(xr[i].x), b = Act<ACT>::unpack2(xr[i].y);
-                float* d = xs + tok * XP + hq;
-                d[0] = a.x; d[1] = a.y; d[2] = b.x; d[3] = b.y;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < kRtWPer; ++i) {
-            const int idx = tid + i * kRtThreads;
-            if (idx < D * E) ws[idx] = wv[i];          // past the contraction: zeros
-        }
-    };
-    float acc[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
-    load_chunk(0);
-    for (int h0 = 0; h0 < H; h0 += D) {
-        store_chunk();
-        __syncthreads();
-        if (h0 + D < H) load_chunk(h0 + D);            // in flight during the FMAs below
-        if (active) {
-            const int hb = sl * hs;
-            if ((E & 3) == 0) {  // rows and groups 16-byte aligned: 4 experts per read
-                for (int hh = hb; hh < hb + hs; ++hh) {  // rows past H were staged as zeros
-                    const float xv = xs[lane * XP + hh];
-                    const float4* wrow = reinterpret_cast<const float4*>(ws + hh * E + e0);
-#pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4)
-                        if (4 * j4 < sh.eg && e0 + 4 * j4 < E) {
-                            const float4 wq = wrow[j4];
-                            acc[4 * j4] = fmaf(xv, wq.x, acc[4 * j4]);
-                            acc[4 * j4 + 1] = fmaf(xv, wq.y, acc[4 * j4 + 1]);
-                            acc[4 * j4 + 2] = fmaf(xv, wq.z, acc[4 * j4 + 2]);
-                            acc[4 * j4 + 3] = fmaf(xv, wq.w, acc[4 * j4 + 3]);
-                        }
-                }
-            } else {
-                for (int hh = hb; hh < hb + hs; ++hh) {
-                    const float xv = xs[lane * XP + hh];
-                    const float* wrow = ws + hh * E + e0;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j < sh.eg && e0 + j < E) acc[j] = fmaf(xv, wrow[j], acc[j]);
-                }
-            }
-        }
-        __syncthreads();
-    }
-    // add the slices in order: slice s writes its sums, slice 0 adds them up
-    float* red = rt_smem;  // [slices 1..S-1][32 tokens][E]
-    for (int s = 1; s < sh.s; ++s) {
-        if (active && sl == s)
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (j < sh.eg && e0 + j < E) red[((s - 1) * kRtTok + lane) * E + e0 + j] = acc[j];
-    }
-    __syncthreads();
+    const int c = static_cast<int>(cluster_ctarank());
+    const int t0 = (blockIdx.x / pl.cs) * kRtTok;
     const int t = t0 + lane;
-    if (active && sl == 0 && t < T) {
+    const int g = warp / pl.s, sl = warp % pl.s;
+    const bool active = g < pl.g;
+    const int e0 = g * EG;
+    const int hs = pl.hc / pl.s;  // contraction rows per warp per chunk (a multiple of 8)
+    const int h_begin = c * pl.hr;
+    const int h_end = min(H, h_begin + pl.hr);
+    const int nchunks = h_end > h_begin ? (h_end - h_begin + pl.hc - 1) / pl.hc : 0;
+
+    // stage weight chunk j (rows h_begin + j hc ...) into buffer j & 1
+    auto stage_w = [&](int j) {
+        const int h0 = h_begin + j * pl.hc;
+        const int rows = min(pl.hc, h_end - h0);
+        float* dst = wbuf + (j & 1) * pl.hc * pl.ep;
+        const float* src = wr + static_cast<size_t>(h0) * E;
+        if ((E & 3) == 0) {
+            const int n4 = rows * E / 4;
+            for (int i = tid; i < n4; i += kRtThreads) cp_async16(dst + 4 * i, src + 4 * i);
+        } else {
+            const int n = rows * E;
+            for (int i = tid; i < n; i += kRtThreads) cp_async4(dst + (i / E) * pl.ep + i % E, src + i);
+        }
+        cp_async_commit();
+    };
+    // this lane's activation vectors of chunk j (zeros past the token count or H)
+    auto load_x = [&](int j, uint4 (&v)[kRtMaxVec]) {
+        const int hb = h_begin + j * pl.hc + sl * hs;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int e = e0 + j;
-            if (j < sh.eg && e < E) {
-                float v = acc[j];
-                for (int s = 1; s < sh.s; ++s) v = __fadd_rn(v, red[((s - 1) * kRtTok + lane) * E + e]);
-                logits[static_cast<size_t>(t) * E + e] = v;
+        for (int i = 0; i < kRtMaxVec; ++i) {
+            const int h = hb + 8 * i;
+            v[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (active && 8 * i < hs && t < T && h < h_end)
+                v[i] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + h));
+        }
+    };
+
+    float acc[EG];
+#pragma unroll
+    for (int j = 0; j < EG; ++j) acc[j] = 0.0f;
+    uint4 cur[kRtMaxVec], nxt[kRtMaxVec];
+    if (nchunks > 0) {
+        stage_w(0);
+        load_x(0, cur);
+    }
+    for (int j = 0; j < nchunks; ++j) {
+        cp_async_wait_all();
+        __syncthreads();  // chunk j staged; everyone is done with chunk j - 1's buffer
+        if (j + 1 < nchunks) {
+            stage_w(j + 1);
+            load_x(j + 1, nxt);
+        }
+        if (active) {
+            const float* wc = wbuf + (j & 1) * pl.hc * pl.ep;
+            const int hb = h_begin + j * pl.hc + sl * hs;
+#pragma unroll
+            for (int i = 0; i < kRtMaxVec; ++i) {
+                if (8 * i >= hs || hb + 8 * i >= h_end) break;
+                const float2 p0 = Act<ACT>::unpack2(cur[i].x), p1 = Act<ACT>::unpack2(cur[i].y);
+                const float2 p2 = Act<ACT>::unpack2(cur[i].z), p3 = Act<ACT>::unpack2(cur[i].w);
+                const float xf[8] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y, p3.x, p3.y};
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4* w4 = reinterpret_cast<const float4*>(wc + (sl * hs + 8 * i + q) * pl.ep + e0);
+#pragma unroll
+                    for (int j4 = 0; j4 < EG / 4; ++j4) {
+                        const float4 wv = w4[j4];  // the same address in every lane: a broadcast
+                        acc[4 * j4] = fmaf(xf[q], wv.x, acc[4 * j4]);
+                        acc[4 * j4 + 1] = fmaf(xf[q], wv.y, acc[4 * j4 + 1]);
+                        acc[4 * j4 + 2] = fmaf(xf[q], wv.z, acc[4 * j4 + 2]);
+                        acc[4 * j4 + 3] = fmaf(xf[q], wv.w, acc[4 * j4 + 3]);
+                    }
+                }
             }
         }
+#pragma unroll
+        for (int i = 0; i < kRtMaxVec; ++i) cur[i] = nxt[i];
     }
+    // slice sums of this CTA, added in slice order into red[0]
+    if (active)
+#pragma unroll
+        for (int j = 0; j < EG; ++j)
+            if (e0 + j < E) red[(sl * kRtTok + lane) * pl.ep + e0 + j] = acc[j];
+    __syncthreads();
+    if (pl.s > 1)
+        for (int i = tid; i < kRtTok * E; i += kRtThreads) {
+            const int tok = i / E, e = i % E;
+            float v = red[tok * pl.ep + e];
+            for (int s = 1; s < pl.s; ++s) v = __fadd_rn(v, red[(s * kRtTok + tok) * pl.ep + e]);
+            red[tok * pl.ep + e] = v;
+        }
+    cluster_sync_all();  // every CTA's sums are in its red[0]
+    // finish tokens [c tpc, (c + 1) tpc): add the CTA sums in rank order
+    const int tpc = kRtTok / pl.cs;
+    float* fin = wbuf;  // [tpc][ep]
+    for (int i = tid; i < tpc * E; i += kRtThreads) {
+        const int tl = i / E, e = i % E;
+        const uint32_t a = smem_u32(red + (c * tpc + tl) * pl.ep + e);
+        float v = ld_dsmem_f32(mapa_shared(a, 0));
+        for (int r = 1; r < pl.cs; ++r) v = __fadd_rn(v, ld_dsmem_f32(mapa_shared(a, r)));
+        fin[tl * pl.ep + e] = v;
+        const int tt = t0 + c * tpc + tl;
+        if (tt < T) logits[static_cast<size_t>(tt) * E + e] = v;
+    }
+    cluster_arrive();  // this CTA has read its peers' sums
+    __syncthreads();
+    for (int tl = warp; tl < tpc; tl += kRtWarps) {
+        const int tt = t0 + c * tpc + tl;
+        if (tt >= T) break;
+        float v[kPerLane];
+#pragma unroll
+        for (int j = 0; j < kPerLane; ++j) {
+            const int e = lane + 32 * j;
+            v[j] = e < E ? fin[tl * pl.ep + e] : 0.0f;
+        }
+        route_row(v, lane, E, k, renorm, ids + static_cast<size_t>(tt) * k, wout + static_cast<size_t>(tt) * k);
+    }
+    cluster_wait();  // no CTA leaves while a peer may still read its shared memory
+}
+
+template <int ACT>
+int launch_router(const void* x, const float* w_router, float* logits, int32_t* ids, float* w, int T, int H, int E,
+                  int k, int renorm, cudaStream_t st) {
+    const RtPlan pl = rt_plan(H, E);
+    const size_t smem = rt_smem_bytes(pl);
+    if (smem > static_cast<size_t>(kRtMaxSmem)) return fail(MOE_ERR_UNSUPPORTED, "moe_router_topk_softmax: plan too large");
+    cudaError_t e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = pl.cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>((T + kRtTok - 1) / kRtTok * pl.cs), 1, 1);
+    cfg.blockDim = dim3(kRtThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    using T_ = typename Act<ACT>::T;
+    const T_* xp = static_cast<const T_*>(x);
+    static int configured_for = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_for != dev) {  // every plan fits in kRtMaxSmem bytes
+        for (const void* f : {reinterpret_cast<const void*>(router_topk_kernel<ACT, 8>),
+                              reinterpret_cast<const void*>(router_topk_kernel<ACT, 16>),
+                              reinterpret_cast<const void*>(router_topk_kernel<ACT, 32>)}) {
+            const int rc = set_smem_limit(f, kRtMaxSmem);
+            if (rc != MOE_OK) return rc;
+        }
+        configured_for = dev;
+    }
+    if (pl.eg == 8)
+        e = cudaLaunchKernelEx(&cfg, router_topk_kernel<ACT, 8>, xp, w_router, logits, ids, w, T, H, E, k, renorm, pl);
+    else if (pl.eg == 16)
+        e = cudaLaunchKernelEx(&cfg, router_topk_kernel<ACT, 16>, xp, w_router, logits, ids, w, T, H, E, k, renorm, pl);
+    else
+        e = cudaLaunchKernelEx(&cfg, router_topk_kernel<ACT, 32>, xp, w_router, logits, ids, w, T, H, E, k, renorm, pl);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "moe_router_topk_softmax: launch failed: %s", cudaGetErrorString(e));
+    count_launch();
+    return check_launch("moe_router_topk_softmax");
 }
 
 }  // namespace
@@ -286,31 +402,11 @@ extern "C" int moe_router_topk_softmax(const void* x, int32_t act, const float* 
     if (T == 0) return MOE_OK;
     MOE_REQUIRE(x && w_router && logits && topk_ids && topk_weights, "%s: NULL pointer", who);
     MOE_REQUIRE(moe::aligned16(x), "%s: x must be 16-byte aligned", who);
+    MOE_REQUIRE((E % 4 != 0) || moe::aligned16(w_router), "%s: w_router must be 16-byte aligned", who);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const moe::RtShape sh = moe::rt_shape(E);
-    const size_t stage = static_cast<size_t>(moe::kRtTok) * (sh.d + 1) + static_cast<size_t>(sh.d) * E;
-    const size_t red = static_cast<size_t>(sh.s - 1) * moe::kRtTok * E;
-    const size_t smem = (stage > red ? stage : red) * sizeof(float);
-    static int configured_for = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_for != dev) {  // up to 32 x 513 + 8192 words: 98 KB
-        const int max_smem = static_cast<int>((moe::kRtTok * (moe::kRtMaxD + 1) + 8192) * sizeof(float));
-        int rc = moe::set_smem_limit(reinterpret_cast<const void*>(moe::router_logits_kernel<MOE_ACT_BF16>), max_smem);
-        if (rc == MOE_OK)
-            rc = moe::set_smem_limit(reinterpret_cast<const void*>(moe::router_logits_kernel<MOE_ACT_F16>), max_smem);
-        if (rc != MOE_OK) return rc;
-        configured_for = dev;
-    }
-    const dim3 grid((T + moe::kRtTok - 1) / moe::kRtTok);
+    const int renorm = renormalize ? 1 : 0;
     if (act == MOE_ACT_BF16)
-        moe::launch_pdl(moe::router_logits_kernel<MOE_ACT_BF16>, grid, moe::kRtThreads, smem, st,
-                        static_cast<const __nv_bfloat16*>(x), w_router, logits, T, H, E);
-    else
-        moe::launch_pdl(moe::router_logits_kernel<MOE_ACT_F16>, grid, moe::kRtThreads, smem, st,
-                        static_cast<const __half*>(x), w_router, logits, T, H, E);
-    moe::count_launch();
-    int rc = moe::check_launch("moe_router_topk_softmax (router GEMM)");
-    if (rc != MOE_OK) return rc;
-    return moe_route_topk_softmax(logits, topk_ids, topk_weights, T, E, top_k, renormalize, stream);
+        return moe::launch_router<MOE_ACT_BF16>(x, w_router, logits, topk_ids, topk_weights, T, H, E, top_k, renorm,
+                                                st);
+    return moe::launch_router<MOE_ACT_F16>(x, w_router, logits, topk_ids, topk_weights, T, H, E, top_k, renorm, st);
 }

@@ -46,6 +46,7 @@ class MoeExpertRoute(ctypes.Structure):
 _SIGNATURES = {
     "moe_last_error": (c_char_p, []),
     "moe_launch_count": (c_uint64, []),
+    "moe_set_wait_limit_ns": (c_uint64, [c_uint64]),
     "moe_route_topk_softmax": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
                                          c_void_p]),
     "moe_router_topk_softmax": (c_int32, [c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32, c_int32,
@@ -130,6 +131,11 @@ def moe_last_error() -> str:
 
 def moe_launch_count() -> int:
     return int(lib().moe_launch_count())
+
+
+def moe_set_wait_limit_ns(ns: int) -> int:
+    """Pipeline wait limit of later GEMM launches (0 = the 2 s default); returns the previous one."""
+    return int(lib().moe_set_wait_limit_ns(int(ns)))
 
 
 def moe_route_topk_softmax(logits, topk_ids, topk_weights, T, E, top_k, renormalize=True, stream=None):

@@ -51,6 +51,7 @@ class MoeConfig:
     lora_rank: int = 0         # 0 = no LoRA fold
     lora_scale: float = 2.0
     group_size: int = 128      # GPTQ group size
+    nvfp4_recipe: str = "amax"  # NVFP4 weights: "amax" quantises a Gaussian, "draw" draws codes directly
     seed: int = 0
 
     def with_T(self, T: int) -> "MoeConfig":
@@ -135,32 +136,92 @@ def _gptq_weight(seed, tensor, E, N, K, G):
 # shaped like a block-scaled Gaussian
 _E2M1_P = np.array([0.10, 0.16, 0.18, 0.16, 0.14, 0.12, 0.09, 0.05])
 
+# positive finite values of the two NVFP4 element formats in code order (OCP
+# MX: E2M1 codes 0..7; E4M3 codes 0x00..0x7E, bias 7, subnormals m * 2^-9,
+# 0x7F is NaN), the tables the quantising recipe rounds to
+_E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+_E4M3_VALUES = np.array([m * 2.0 ** -9 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+                         for e in range(16) for m in range(8)][:127])
 
-def _nvfp4_weight(seed, tensor, E, N, K, n_scale2):
-    """NVFP4 codes drawn directly: E2M1 magnitude codes from ``_E2M1_P`` with a
-    random sign, E4M3 block scales with exponent field 5..9 and any mantissa
-    (values 0.25 .. 3.75, never NaN), fp32 ``scale2`` U(0.5, 1.5) * 0.003. The
-    E2M1 codes have RMS 2.34 and the block scales RMS 2.85, so the decoded
-    weights have RMS close to 0.02, the scale of the bf16 workloads."""
+
+def _round_to_table(a: np.ndarray, table: np.ndarray) -> np.ndarray:
+    """Codes of the nearest table values to a >= 0 (the table ascending in
+    code order), ties to the even code, values past the largest saturating:
+    round-to-nearest-even into a small float format."""
+    a = np.minimum(a, table[-1])
+    hi = np.clip(np.searchsorted(table, a, side="left"), 1, len(table) - 1)
+    lo = hi - 1
+    dlo = a - table[lo]
+    dhi = table[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    return np.where(pick_hi, hi, lo).astype(np.uint8)
+
+
+def _nvfp4_weight(seed, tensor, E, N, K, n_scale2, recipe="amax", std=0.02):
+    """NVFP4 weights ([N, K/2] E2M1 codes, [K/16, N] E4M3 block scales, fp32
+    scale2 [n_scale2, E]).
+
+    ``amax`` (the default): block-amax quantisation of bf16 N(0, std) weights,
+    per expert and per scale2 group (gate rows, up rows): scale2 = amax /
+    (6 * 448); each 16-wide block's scale is the E4M3 rounding (nearest, ties
+    to even) of amax_block / (6 * scale2); each weight's code is the E2M1
+    rounding of w / (e4m3(scale) * scale2), saturating at 6. Every block then
+    holds a code near +-6, as real quantised checkpoints do.
+
+    ``draw``: codes drawn directly, E2M1 magnitude codes from ``_E2M1_P``
+    with a random sign, E4M3 block scales with exponent field 5..9 and any
+    mantissa (values 0.25 .. 3.75), scale2 U(0.5, 1.5) * 0.003: weights of
+    RMS close to 0.02 that use every code and many scale values."""
     if K % 16:
         raise ValueError("NVFP4 needs K % 16 == 0")
+    if recipe == "draw":
+        def packed(e):
+            r = _rng(seed, tensor, e)
+            mag = r.choice(8, size=(N, K), p=_E2M1_P).astype(np.uint8)
+            sign = r.integers(0, 2, size=(N, K), dtype=np.uint8) << 3
+            c = mag | sign
+            return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
 
-    def packed(e):
-        r = _rng(seed, tensor, e)
-        mag = r.choice(8, size=(N, K), p=_E2M1_P).astype(np.uint8)
-        sign = r.integers(0, 2, size=(N, K), dtype=np.uint8) << 3
-        c = mag | sign
-        return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+        def scales(e):
+            r = _rng(seed, tensor + 100, e)
+            ex = r.integers(5, 10, size=(K // 16, N), dtype=np.uint8)
+            man = r.integers(0, 8, size=(K // 16, N), dtype=np.uint8)
+            return ((ex << 3) | man).astype(np.uint8)
 
-    def scales(e):
-        r = _rng(seed, tensor + 100, e)
-        ex = r.integers(5, 10, size=(K // 16, N), dtype=np.uint8)
-        man = r.integers(0, 8, size=(K // 16, N), dtype=np.uint8)
-        return ((ex << 3) | man).astype(np.uint8)
+        s2 = (_rng(seed, _S2, tensor).uniform(0.5, 1.5, size=(n_scale2, E)) * 0.003).astype(np.float32)
+        return {"format": "nvfp4", "packed": _per_expert(packed, E), "scales": _per_expert(scales, E),
+                "scale2": s2}
+    if recipe != "amax":
+        raise ValueError(f"unknown NVFP4 recipe {recipe!r}")
 
-    s2 = (_rng(seed, _S2, tensor).uniform(0.5, 1.5, size=(n_scale2, E)) * 0.003).astype(np.float32)
-    return {"format": "nvfp4", "packed": _per_expert(packed, E), "scales": _per_expert(scales, E),
-            "scale2": s2}
+    def quantise(e):
+        bits = _normal_act(_rng(seed, tensor, e), (N, K), std, "bf16")
+        w = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+        rows = N // n_scale2
+        packed = np.empty((N, K // 2), np.uint8)
+        sc = np.empty((K // 16, N), np.uint8)
+        s2 = np.empty(n_scale2, np.float32)
+        for g in range(n_scale2):
+            wg = w[g * rows:(g + 1) * rows]
+            amax = float(np.max(np.abs(wg)))
+            s2g = np.float32(amax / (6.0 * 448.0)) if amax > 0 else np.float32(1.0)
+            s2[g] = s2g
+            blk = np.abs(wg).reshape(rows, K // 16, 16).max(axis=2)          # [rows, K/16]
+            scode = _round_to_table(blk / (6.0 * float(s2g)), _E4M3_VALUES)   # [rows, K/16]
+            sval = _E4M3_VALUES[scode] * float(s2g)
+            denom = np.repeat(sval, 16, axis=1)
+            mag = np.divide(np.abs(wg), denom, out=np.zeros_like(wg), where=denom > 0)
+            c = _round_to_table(mag, _E2M1_VALUES) | (np.signbit(wg).astype(np.uint8) << 3)
+            c = np.where(c == 8, 0, c).astype(np.uint8)                        # -0 as +0
+            packed[g * rows:(g + 1) * rows] = c[:, 0::2] | (c[:, 1::2] << 4)
+            sc[:, g * rows:(g + 1) * rows] = scode.T
+        return packed, sc, s2
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        parts = list(ex.map(quantise, range(E)))
+    return {"format": "nvfp4", "packed": np.stack([p[0] for p in parts]),
+            "scales": np.stack([p[1] for p in parts]),
+            "scale2": np.ascontiguousarray(np.stack([p[2] for p in parts]).T)}
 
 
 # E4M3 exponent-field probabilities (fields 0..10; 0 = zero and subnormals),
@@ -197,8 +258,8 @@ def make_weights(cfg: MoeConfig) -> dict:
         gu = _gptq_weight(s, _GU, E, 2 * I, H, cfg.group_size)
         dn = _gptq_weight(s, _DOWN, E, H, I, cfg.group_size)
     elif cfg.wfmt == "nvfp4":
-        gu = _nvfp4_weight(s, _GU, E, 2 * I, H, 2)
-        dn = _nvfp4_weight(s, _DOWN, E, H, I, 1)
+        gu = _nvfp4_weight(s, _GU, E, 2 * I, H, 2, cfg.nvfp4_recipe, cfg.weight_std)
+        dn = _nvfp4_weight(s, _DOWN, E, H, I, 1, cfg.nvfp4_recipe, cfg.weight_std)
     elif cfg.wfmt == "fp8":
         gu = _fp8_weight(s, _GU, E, 2 * I, H)
         dn = _fp8_weight(s, _DOWN, E, H, I)

@@ -141,3 +141,11 @@ def test_lora_host_helpers_follow_the_page(moe):
     a, b, s, n = moe.pack_expert_tables([(3, 10, 20, 0.5), (0, 1, 2, 2.0), (3, 11, 21, 0.25)])
     assert n == 4
     assert a == [1, 0, 0, 11] and b == [2, 0, 0, 21] and s == [2.0, 0.0, 0.0, 0.25]
+
+
+def test_wait_limit_hook_returns_previous_and_restores_default(moe):
+    """moe_set_wait_limit_ns (the GEMM kernels' wait limit, a testing hook)
+    returns the previous limit; 0 restores the 2 s default. Host state only."""
+    first = moe.moe_set_wait_limit_ns(12345)
+    assert moe.moe_set_wait_limit_ns(0) == 12345
+    assert moe.moe_set_wait_limit_ns(first) == 2_000_000_000

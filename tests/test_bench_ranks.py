@@ -69,3 +69,15 @@ def test_reference_arm_prints_on_rank_zero_only(rank):
         assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     else:
         assert lines == []
+
+
+def test_tensor_peak_follows_the_sampled_clocks():
+    """The bench holds a kernel to the burst bf16 peak at full clocks, and to
+    the sustained one once the power cap (or a lowered clock) shows."""
+    import bench
+    pk = {"bf16_tflops": 1957.4, "bf16_tflops_sustained": 1729.1}
+    assert bench.tensor_peak(pk, {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}) == (1957.4, "burst")
+    assert bench.tensor_peak(pk, {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}) == \
+        (1729.1, "sustained")
+    assert bench.tensor_peak(pk, {"sm_mhz": 1650.0, "sm_max_mhz": 2070.0, "reasons": []}) == (1729.1, "sustained")
+    assert bench.tensor_peak(pk, {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]})[1] == "burst"

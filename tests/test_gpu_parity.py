@@ -130,8 +130,14 @@ LAYER_CASES = {
     "fine_grained@T1024": _cfg("fine_grained@T1024"),
     "gptq@T16": _cfg("gptq@T16"),
     "gptq@T2048": _cfg("gptq@T2048"),
+    # NVFP4 weights from block-amax quantisation of a Gaussian (every 16-wide
+    # block holds a code near +-6), decode and prefill forms
     "nvfp4@T64": _cfg("nvfp4_lora@T64", lora_rank=0),
     "nvfp4_lora@T2048": _cfg("nvfp4_lora"),
+    # NVFP4 codes and block scales drawn directly (every code, many scale values)
+    "nvfp4_drawn@T64": _cfg("nvfp4_lora@T64", lora_rank=0, nvfp4_recipe="draw"),
+    "nvfp4_drawn_prefill": synth.MoeConfig("nvfp4_drawn_prefill", T=600, H=256, I=192, E=2, k=1, bs=64,
+                                           wfmt="nvfp4", router="normal", nvfp4_recipe="draw"),
     # edge shapes: one expert, ragged I (not a multiple of 128) and a span of several row tiles
     "one_expert_ragged": synth.MoeConfig("one_expert_ragged", T=300, H=128, I=136, E=1, k=1, bs=16,
                                          router="normal"),
@@ -166,6 +172,17 @@ LAYER_CASES = {
                                        wfmt="fp8", router="normal"),
     "fp8_decode_ragged": synth.MoeConfig("fp8_decode_ragged", T=24, H=272, I=144, E=8, k=2, bs=16,
                                          wfmt="fp8", router="normal"),
+    # FP8 prefill form (128-token tiles) with bf16 activations, the path of the
+    # fp8 workload: >= 128 rows per expert, an odd number of 64-deep k blocks
+    # for gate/up (H=320), a ragged last k block for down (I=208) and a
+    # ragged last column tile
+    "fp8_bf16_prefill": synth.MoeConfig("fp8_bf16_prefill", T=300, H=320, I=208, E=2, k=1, bs=16,
+                                        wfmt="fp8", router="normal"),
+    # FP8 decode form with fp16 activations
+    "fp8_f16_decode": synth.MoeConfig("fp8_f16_decode", T=24, H=272, I=144, E=8, k=2, bs=16, act="f16",
+                                      wfmt="fp8", router="normal"),
+    # the fp8 workload at full size (T=2048, E=128, top_k=8: prefill form)
+    "fp8@T2048": _cfg("fp8"),
     # CTA-pair form with short last row tiles (a few to ~100 rows past a multiple of 256)
     # run with swapped operands; I=192 leaves the second gate/up column tile half empty
     "pair_tails": synth.MoeConfig("pair_tails", T=600, H=256, I=192, E=2, k=1, bs=16, router="normal"),
@@ -236,7 +253,8 @@ def test_split_k_repeatable(dev, name):
     assert not lay.gate_up_ws[-4096:].any() and not lay.down_ws[-4096:].any()
 
 
-@pytest.mark.parametrize("name", ["tiny", "fine_grained@T64", "gptq@T16", "nvfp4_lora@T2048", "skewed"])
+@pytest.mark.parametrize("name", ["tiny", "fine_grained@T64", "gptq@T16", "nvfp4_lora@T2048", "skewed",
+                                  "fp8@T2048"])
 def test_layer_end_to_end(dev, name):
     cfg = LAYER_CASES[name]
     inp = synth.make_inputs(cfg)
@@ -249,7 +267,9 @@ def test_layer_end_to_end(dev, name):
 
 
 @pytest.mark.parametrize("T,H,E,k,act", [(16, 128, 8, 2, "bf16"), (64, 4096, 8, 2, "bf16"), (100, 2048, 128, 8, "bf16"),
-                                         (45, 200, 60, 6, "f16"), (33, 1024, 256, 8, "f16")])
+                                         (45, 200, 60, 6, "f16"), (33, 1024, 256, 8, "f16"),
+                                         (4096, 4096, 8, 2, "bf16"), (300, 2048, 128, 8, "bf16"),
+                                         (77, 136, 17, 3, "bf16"), (5, 64, 3, 1, "f16"), (1, 8, 1, 1, "bf16")])
 def test_router_gemm_then_routing(dev, T, H, E, k, act):
     """Router GEMM on the GPU: logits within the f32 accumulation bound of the
     oracle's exactly rounded product, and the routing of those logits
