@@ -411,6 +411,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// Wait for this thread's TMEM loads and tie the registers of r to the wait:
+// tcgen05.ld writes its destination registers asynchronously, and the empty
+// asm statements (ordered after the wait, with r as in/out operands) keep the
+// compiler from reading or moving r before it.
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
 // 32 lanes x 32 consecutive 32-bit columns from registers: thread i of the
 // warp writes lane (taddr.lane + i), columns [taddr.col, taddr.col + 32)
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {

@@ -183,9 +183,12 @@ LAYER_CASES = {
                                       wfmt="fp8", router="normal"),
     # the fp8 workload at full size (T=2048, E=128, top_k=8: prefill form)
     "fp8@T2048": _cfg("fp8"),
-    # CTA-pair form with short last row tiles (a few to ~100 rows past a multiple of 256)
-    # run with swapped operands; I=192 leaves the second gate/up column tile half empty
+    # CTA-pair form: experts of ~300 rows cut into two tiles of nearly equal height;
+    # I=192 leaves the second gate/up column tile half empty
     "pair_tails": synth.MoeConfig("pair_tails", T=600, H=256, I=192, E=2, k=1, bs=16, router="normal"),
+    # CTA-pair form with a block size that is not a multiple of 16: a tile's last
+    # 16-row unit may run into padding or the next expert's rows, which are not stored
+    "pair_bs24": synth.MoeConfig("pair_bs24", T=900, H=320, I=200, E=3, k=2, bs=24, router="normal"),
 }
 
 
