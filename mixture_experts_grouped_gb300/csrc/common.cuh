@@ -171,6 +171,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// The same test, but a thread whose phase is not complete is suspended until
+// it completes or hint_ns nanoseconds pass, instead of returning at once: a
+// waiting warp then takes no issue slots from the warps that share its
+// sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+// longest suspension of one try_wait in a bounded wait: how long another
+// role's abort can go unnoticed
+constexpr uint64_t kWaitSleepNs = 200000ull;
 
 // How long a pipeline wait may last, by default, before the kernel gives up
 // (the whole layer at the largest supported size runs in a few
@@ -195,8 +213,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    const uint32_t sleep = static_cast<uint32_t>(w.limit_ns < kWaitSleepNs ? w.limit_ns : kWaitSleepNs);
     while (true) {
-        if (mbar_try_wait(a, parity)) return true;
+        if (mbar_try_wait_sleep(a, parity, sleep)) return true;
         if (*w.abort) return false;
         if (globaltimer_ns() - t0 > w.limit_ns) {
             *w.abort = 1;
@@ -240,7 +259,7 @@ __device__ __forceinline__ bool flag_wait(const int* f, const WaitCtx& w) {
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     const uint32_t a = smem_u32(bar);
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(a, parity)) {
+    while (!mbar_try_wait_sleep(a, parity, static_cast<uint32_t>(kWaitSleepNs))) {
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
     return true;

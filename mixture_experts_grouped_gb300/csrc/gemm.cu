@@ -1360,7 +1360,7 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
 #pragma unroll
         for (int i = 0; i < RSTAGES; ++i) {
             mbar_init(&s.raw_full[i], 1);
-            mbar_init(&s.raw_empty[i], S::NDQ);  // every dequantising warp
+            mbar_init(&s.raw_empty[i], NUM_DQ_WARPS);  // the set that converts the stage
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.tfull[i], S::NH * NSETS);  // every issuer that had a k block of the tile
@@ -1525,91 +1525,90 @@ grouped_gemm_ts_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
         }
     } else if (warp < S::RAWW) {
         // ---------------- dequantising warps: raw shared bytes -> TMEM ----------------
-        // Item j (the CTA's j-th k block) is k block kb of its tile, in raw
-        // stage tile * KR + kb / KPR, weight stage j mod TS_STAGES, and
-        // belongs to set j mod NSET. A warp releases each raw stage once:
-        // after loading its last item there, or unread when the stage holds
-        // none of its items. Its next item's bytes are loaded into registers
-        // before the current one is converted.
+        // The CTA's raw stages, counted j = 0, 1, ... over its tiles, go to the
+        // sets in turn (set j mod NSET); a set converts all k blocks of a stage
+        // (two for GPTQ and NVFP4, one for FP8), k block g into weight stage
+        // g mod TS_STAGES. Each warp of the set owns 32 rows of one half: it
+        // loads their raw bytes into registers, converts and stores each k
+        // block, hands the raw stage back to TMA, then publishes the weight
+        // stages. Ring positions are running counters (no division).
+        static_assert(TS_STAGES == 4, "weight stage index is g & 3");
         const int dq = warp - S::DQ0;
         const int set = dq / NUM_DQ_WARPS;
         const int h = (dq >> 2) & 1;   // weight half
         const int sp = warp & 3;       // TMEM lane quarter this warp may access
         const int r = sp * 32 + lane;  // weight row within the half
         const uint32_t trow = tmem_base + (static_cast<uint32_t>(sp * 32) << 16) + TS_A_COL + h * 32;
-        int items = 0;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x)
-            if (!tile_is_padding(p, decode_tile<XROWS>(s, E, tile, S::OUT_COLS))) items += KB;
-        int f_kb = 0, f_rs0 = 0;  // position of the next item to fetch (k block, its tile's first raw stage)
-        int rs_next = 0;          // first raw stage this warp has not released
-        auto step = [&]() {
-            if (++f_kb == KB) {
-                f_kb = 0;
-                f_rs0 += KR;
-            }
-        };
-        auto release = [&](int rs) {
-            // the stage was read through the generic proxy and is refilled by
-            // TMA (the async proxy): order the reads before the release, or
-            // the next copy may land under them (seen as stale rows for a
-            // few tiles once the dequantisation is fast)
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s.raw_empty[rs % RSTAGES]);
-        };
-        auto fetch = [&](RawRow& x) -> bool {
-            const int rs = f_rs0 + f_kb / KPR;
-            for (; rs_next < rs; ++rs_next) {  // stages with none of this set's items
-                if (!mbar_wait(&s.raw_full[rs_next % RSTAGES], static_cast<uint32_t>((rs_next / RSTAGES) & 1),
-                               wc))
-                    return false;
-                release(rs_next);
-            }
-            if (!mbar_wait(&s.raw_full[rs % RSTAGES], static_cast<uint32_t>((rs / RSTAGES) & 1), wc))
-                return false;
-            load_raw_row<WFMT>(sR + (rs % RSTAGES) * RAW2, h, r, f_kb % KPR, g64, x);
-#pragma unroll
-            for (int i = 0; i < S::NSET; ++i) step();
-            // release the stage once this warp's next item lies beyond it (with
-            // one set, the second k block of a two-block stage is its next item)
-            if (f_rs0 + f_kb / KPR != rs) {
-                release(rs);
-                rs_next = rs + 1;
-            } else {
-                rs_next = rs;
-            }
-            return true;
-        };
-        RawRow cur, nxt;
-        for (int i = 0; i < set; ++i) step();
-        bool ok = set < items && fetch(cur);
-        for (int it = set; it < items && ok; it += S::NSET) {
-            if (it + S::NSET < items && !fetch(nxt)) break;
-            uint32_t o[32];
+        auto convert = [&](const RawRow& x, uint32_t (&o)[32]) {
             if (WFMT == MOE_W_GPTQ_INT4) {
                 uint32_t w8[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) w8[i] = cur.w[i];
-                gptq_row<ACT, S::PERM>(w8, (cur.z >> (4 * (r & 7))) & 15,
-                                       __ushort_as_half(static_cast<unsigned short>(cur.s)), o);
+                for (int i = 0; i < 8; ++i) w8[i] = x.w[i];
+                gptq_row<ACT, S::PERM>(w8, (x.z >> (4 * (r & 7))) & 15,
+                                       __ushort_as_half(static_cast<unsigned short>(x.s)), o);
             } else if (WFMT == MOE_W_NVFP4) {
                 uint32_t w8[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) w8[i] = cur.w[i];
-                nvfp4_row<ACT>(w8, cur.sc, o);
+                for (int i = 0; i < 8; ++i) w8[i] = x.w[i];
+                nvfp4_row<ACT>(w8, x.sc, o);
             } else {
-                fp8_row<ACT>(cur.w, o);
+                fp8_row<ACT>(x.w, o);
             }
-            const int as = it % ASTAGES;
-            if (!mbar_wait(&s.aempty[as], static_cast<uint32_t>(((it / ASTAGES) & 1) ^ 1), wc)) break;
-            tc_fence_after();  // the MMAs that read this TMEM stage have completed
-            tmem_st32(trow + as * 64, o);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s.afull[as]);
-            cur = nxt;
+        };
+        int rpos = set, rpar = 0;  // ring position and phase of this set's next raw stage
+        int jmod = 0;              // (the CTA's next raw stage) mod NSET
+        int g0 = 0;                // k blocks of this CTA's earlier tiles
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+            if (tile_is_padding(p, decode_tile<XROWS>(s, E, tile, S::OUT_COLS))) continue;
+            for (int kr = 0; kr < KR; ++kr) {
+                const bool mine = jmod == set;
+                if (++jmod == S::NSET) jmod = 0;
+                if (!mine) continue;
+                const int g = g0 + kr * KPR;
+                const bool two = KPR == 2 && kr * KPR + 1 < KB;  // the stage's second k block is used
+                if (!mbar_wait(&s.raw_full[rpos], static_cast<uint32_t>(rpar), wc)) { ok = false; break; }
+                const uint8_t* raw = sR + rpos * RAW2;
+                RawRow a, b;
+                load_raw_row<WFMT>(raw, h, r, 0, g64, a);
+                if (two) load_raw_row<WFMT>(raw, h, r, 1, g64, b);
+                uint32_t o[32];
+                convert(a, o);
+                if (!mbar_wait(&s.aempty[g & 3], static_cast<uint32_t>(((g >> 2) & 1) ^ 1), wc)) { ok = false; break; }
+                tc_fence_after();  // the MMAs that read this weight stage have completed
+                tmem_st32(trow + (g & 3) * 64, o);
+                if (two) {
+                    convert(b, o);
+                    const int g1 = g + 1;
+                    if (!mbar_wait(&s.aempty[g1 & 3], static_cast<uint32_t>(((g1 >> 2) & 1) ^ 1), wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    tmem_st32(trow + (g1 & 3) * 64, o);
+                }
+                // the raw bytes were read through the generic proxy and the stage
+                // is refilled by TMA (the async proxy): order the reads before
+                // the release, or the next copy may land under them
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.raw_empty[rpos]);
+                rpos += S::NSET;
+                if (rpos >= RSTAGES) {
+                    rpos -= RSTAGES;
+                    rpar ^= 1;
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&s.afull[g & 3]);
+                    if (two) mbar_arrive(&s.afull[(g + 1) & 3]);
+                }
+            }
+            g0 += KB;
         }
+        tmem_st_wait();  // nothing in flight into TMEM when it is freed
     } else {
         // ---------------- raw quantised-weight producer (last warp) ----------------
         // A TMA copy costs its issuing thread a roughly fixed time however
