@@ -121,32 +121,35 @@ route_topk_softmax_kernel(const float* __restrict__ logits, int32_t* __restrict_
 // The workloads define the router the pages leave out: logits[t, e] =
 // sum_h x[t, h] * Wr[h, e] with Wr f32 [H, E] (E <= 256). At E = 8 it is a
 // few FLOPs per activation byte, so the kernel is built to stream x at HBM
-// rate with many CTAs in flight; at E >= 128 it is bound by the fp32
-// fused multiply-adds.
-//   * A cluster of CS CTAs (CS = 1, 2, 4 or 8) takes 32 tokens (lane =
-//     token); CTA c of the cluster takes the contraction range [c HR,
-//     (c + 1) HR). Its eight warps are G expert groups (EG = 8, 16 or 32
-//     experts, one accumulator register each) times S = 8 / G contraction
+// rate with every CTA of the grid resident at once; at E >= 128 it is bound
+// by the fp32 fused multiply-adds.
+//   * A cluster of CS CTAs (CS = 1, 2, 4 or 8) takes TT = 32 TPL tokens
+//     (lane l holds tokens l, l + 32, ...: TPL = 2 for E <= 16, else 1); CTA
+//     c of the cluster takes the contraction range [c HR, (c + 1) HR). Its
+//     eight warps are G expert groups (EG = 8, 16 or 32 experts, one
+//     accumulator register each per token) times S = 8 / G contraction
 //     slices.
 //   * The CTA's router-weight rows are staged in shared memory in chunks of
-//     HC rows (two buffers, cp.async); each lane reads its token's
-//     activations straight from global memory as 16-byte vectors (HC / S / 8
-//     of them per chunk, the next chunk's in flight while the current one is
-//     used).
+//     HC rows (two buffers, cp.async); each lane reads its tokens'
+//     activations straight from global memory as 16-byte vectors, the next
+//     chunk's in flight while the current one is used.
 //   * Sums: a lane accumulates its slice of each chunk in ascending h by
 //     fused multiply-adds; the S slice sums of a CTA are added in slice
 //     order, then the CS CTA sums in rank order, read through distributed
 //     shared memory, so the result does not depend on timing.
-//   * CTA c then finishes tokens [c 32 / CS, (c + 1) 32 / CS) of the
+//   * CTA c then finishes tokens [c TT / CS, (c + 1) TT / CS) of the
 //     cluster: it writes their logits and routes them, one warp per token,
 //     with the same route_row as moe_route_topk_softmax.
-constexpr int kRtTok = 32, kRtThreads = 256, kRtWarps = kRtThreads / 32;
-constexpr int kRtMaxVec = 4;       // 16-byte activation vectors per lane per chunk at most
+constexpr int kRtThreads = 256, kRtWarps = kRtThreads / 32;
 constexpr int kRtChunkFloats = 8192;  // router-weight floats per staged chunk at most (32 KB)
 constexpr int kRtMaxSmem = 100 * 1024;  // shared memory of the largest plan (E = 256: 96 KB)
 
+// 16-byte activation vectors per lane and token per chunk at most
+__host__ __device__ constexpr int rt_max_vec(int tpl) { return tpl == 2 ? 2 : 4; }
+
 struct RtPlan {
     int eg, g, s;  // experts per group, groups, contraction slices
+    int tpl, tt;   // tokens per lane, tokens per cluster
     int ep;        // E rounded up to 4: row stride of the staged weights
     int hc;        // weight rows per chunk (a multiple of 8 S)
     int cs;        // CTAs per cluster
@@ -158,10 +161,12 @@ inline RtPlan rt_plan(int H, int E) {
     r.eg = E <= 8 ? 8 : (E <= 16 ? 16 : 32);
     r.g = (E + r.eg - 1) / r.eg;  // <= 8
     r.s = kRtWarps / r.g;         // >= 1
+    r.tpl = r.eg <= 16 ? 2 : 1;
+    r.tt = 32 * r.tpl;
     r.ep = (E + 3) / 4 * 4;
     const int step = 8 * r.s;
     int hc = kRtChunkFloats / r.ep / step * step;
-    if (hc > kRtMaxVec * step) hc = kRtMaxVec * step;
+    if (hc > rt_max_vec(r.tpl) * step) hc = rt_max_vec(r.tpl) * step;
     r.hc = hc < step ? step : hc;
     // as many CTAs per token block as leave each warp slice at least one
     // 16-byte vector (8 h) of the contraction
@@ -172,10 +177,10 @@ inline RtPlan rt_plan(int H, int E) {
     return r;
 }
 
+// weight chunks (two) or, afterwards, the finished logits; then the slice sums
+__host__ __device__ inline int rt_wbuf_floats(const RtPlan& r) { return (2 * r.hc > r.tt ? 2 * r.hc : r.tt) * r.ep; }
 inline size_t rt_smem_bytes(const RtPlan& r) {
-    const size_t wbuf = static_cast<size_t>(2 * r.hc > kRtTok ? 2 * r.hc : kRtTok) * r.ep;  // two chunks / finals
-    const size_t red = static_cast<size_t>(r.s) * kRtTok * r.ep;
-    return (wbuf + red) * sizeof(float);
+    return (static_cast<size_t>(rt_wbuf_floats(r)) + static_cast<size_t>(r.s) * r.tt * r.ep) * sizeof(float);
 }
 
 __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
@@ -192,20 +197,20 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
     return v;
 }
 
-template <int ACT, int EG>
-__global__ void __launch_bounds__(kRtThreads)
+template <int ACT, int EG, int TPL>
+__global__ void __launch_bounds__(kRtThreads, EG == 8 ? 4 : (EG == 16 ? 3 : 2))  // E <= 8: one wave at T = 4096
 router_topk_kernel(const typename Act<ACT>::T* __restrict__ x, const float* __restrict__ wr,
                    float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ wout, int T, int H,
                    int E, int k, int renorm, const RtPlan pl) {
+    constexpr int V = rt_max_vec(TPL);
+    constexpr int TT = 32 * TPL;
     pdl_wait();
     extern __shared__ float rt_smem[];
-    const int wstride = (2 * pl.hc > kRtTok ? 2 * pl.hc : kRtTok) * pl.ep;
-    float* wbuf = rt_smem;                    // two weight chunks [hc][ep]; afterwards the finals [32][ep]
-    float* red = rt_smem + wstride;           // slice sums [s][32 tokens][ep]
+    float* wbuf = rt_smem;                     // two weight chunks [hc][ep]; afterwards the finals [tpc][ep]
+    float* red = rt_smem + rt_wbuf_floats(pl);  // slice sums [s][TT tokens][ep]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = static_cast<int>(cluster_ctarank());
-    const int t0 = (blockIdx.x / pl.cs) * kRtTok;
-    const int t = t0 + lane;
+    const int t0 = (blockIdx.x / pl.cs) * TT;
     const int g = warp / pl.s, sl = warp % pl.s;
     const bool active = g < pl.g;
     const int e0 = g * EG;
@@ -224,27 +229,33 @@ router_topk_kernel(const typename Act<ACT>::T* __restrict__ x, const float* __re
             const int n4 = rows * E / 4;
             for (int i = tid; i < n4; i += kRtThreads) cp_async16(dst + 4 * i, src + 4 * i);
         } else {
-            const int n = rows * E;
-            for (int i = tid; i < n; i += kRtThreads) cp_async4(dst + (i / E) * pl.ep + i % E, src + i);
+            for (int rr = warp; rr < rows; rr += kRtWarps)
+                for (int e = lane; e < E; e += 32) cp_async4(dst + rr * pl.ep + e, src + rr * E + e);
         }
         cp_async_commit();
     };
     // this lane's activation vectors of chunk j (zeros past the token count or H)
-    auto load_x = [&](int j, uint4 (&v)[kRtMaxVec]) {
+    auto load_x = [&](int j, uint4 (&v)[TPL][V]) {
         const int hb = h_begin + j * pl.hc + sl * hs;
 #pragma unroll
-        for (int i = 0; i < kRtMaxVec; ++i) {
-            const int h = hb + 8 * i;
-            v[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (active && 8 * i < hs && t < T && h < h_end)
-                v[i] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + h));
+        for (int q = 0; q < TPL; ++q) {
+            const int t = t0 + lane + 32 * q;
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const int h = hb + 8 * i;
+                v[q][i] = make_uint4(0u, 0u, 0u, 0u);
+                if (active && 8 * i < hs && t < T && h < h_end)
+                    v[q][i] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + h));
+            }
         }
     };
 
-    float acc[EG];
+    float acc[TPL][EG];
 #pragma unroll
-    for (int j = 0; j < EG; ++j) acc[j] = 0.0f;
-    uint4 cur[kRtMaxVec], nxt[kRtMaxVec];
+    for (int q = 0; q < TPL; ++q)
+#pragma unroll
+        for (int j = 0; j < EG; ++j) acc[q][j] = 0.0f;
+    uint4 cur[TPL][V], nxt[TPL][V];
     if (nchunks > 0) {
         stage_w(0);
         load_x(0, cur);
@@ -260,54 +271,72 @@ router_topk_kernel(const typename Act<ACT>::T* __restrict__ x, const float* __re
             const float* wc = wbuf + (j & 1) * pl.hc * pl.ep;
             const int hb = h_begin + j * pl.hc + sl * hs;
 #pragma unroll
-            for (int i = 0; i < kRtMaxVec; ++i) {
+            for (int i = 0; i < V; ++i) {
                 if (8 * i >= hs || hb + 8 * i >= h_end) break;
-                const float2 p0 = Act<ACT>::unpack2(cur[i].x), p1 = Act<ACT>::unpack2(cur[i].y);
-                const float2 p2 = Act<ACT>::unpack2(cur[i].z), p3 = Act<ACT>::unpack2(cur[i].w);
-                const float xf[8] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y, p3.x, p3.y};
+                float xf[TPL][8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4* w4 = reinterpret_cast<const float4*>(wc + (sl * hs + 8 * i + q) * pl.ep + e0);
+                for (int q = 0; q < TPL; ++q) {
+                    const float2 p0 = Act<ACT>::unpack2(cur[q][i].x), p1 = Act<ACT>::unpack2(cur[q][i].y);
+                    const float2 p2 = Act<ACT>::unpack2(cur[q][i].z), p3 = Act<ACT>::unpack2(cur[q][i].w);
+                    xf[q][0] = p0.x; xf[q][1] = p0.y; xf[q][2] = p1.x; xf[q][3] = p1.y;
+                    xf[q][4] = p2.x; xf[q][5] = p2.y; xf[q][6] = p3.x; xf[q][7] = p3.y;
+                }
+#pragma unroll
+                for (int hh = 0; hh < 8; ++hh) {
+                    const float4* w4 = reinterpret_cast<const float4*>(wc + (sl * hs + 8 * i + hh) * pl.ep + e0);
 #pragma unroll
                     for (int j4 = 0; j4 < EG / 4; ++j4) {
                         const float4 wv = w4[j4];  // the same address in every lane: a broadcast
-                        acc[4 * j4] = fmaf(xf[q], wv.x, acc[4 * j4]);
-                        acc[4 * j4 + 1] = fmaf(xf[q], wv.y, acc[4 * j4 + 1]);
-                        acc[4 * j4 + 2] = fmaf(xf[q], wv.z, acc[4 * j4 + 2]);
-                        acc[4 * j4 + 3] = fmaf(xf[q], wv.w, acc[4 * j4 + 3]);
+#pragma unroll
+                        for (int q = 0; q < TPL; ++q) {
+                            acc[q][4 * j4] = fmaf(xf[q][hh], wv.x, acc[q][4 * j4]);
+                            acc[q][4 * j4 + 1] = fmaf(xf[q][hh], wv.y, acc[q][4 * j4 + 1]);
+                            acc[q][4 * j4 + 2] = fmaf(xf[q][hh], wv.z, acc[q][4 * j4 + 2]);
+                            acc[q][4 * j4 + 3] = fmaf(xf[q][hh], wv.w, acc[q][4 * j4 + 3]);
+                        }
                     }
                 }
             }
         }
 #pragma unroll
-        for (int i = 0; i < kRtMaxVec; ++i) cur[i] = nxt[i];
+        for (int q = 0; q < TPL; ++q)
+#pragma unroll
+            for (int i = 0; i < V; ++i) cur[q][i] = nxt[q][i];
     }
     // slice sums of this CTA, added in slice order into red[0]
     if (active)
 #pragma unroll
-        for (int j = 0; j < EG; ++j)
-            if (e0 + j < E) red[(sl * kRtTok + lane) * pl.ep + e0 + j] = acc[j];
+        for (int q = 0; q < TPL; ++q)
+#pragma unroll
+            for (int j = 0; j < EG; ++j)
+                if (e0 + j < E) red[(sl * TT + lane + 32 * q) * pl.ep + e0 + j] = acc[q][j];
     __syncthreads();
     if (pl.s > 1)
-        for (int i = tid; i < kRtTok * E; i += kRtThreads) {
-            const int tok = i / E, e = i % E;
-            float v = red[tok * pl.ep + e];
-            for (int s = 1; s < pl.s; ++s) v = __fadd_rn(v, red[(s * kRtTok + tok) * pl.ep + e]);
-            red[tok * pl.ep + e] = v;
-        }
+        for (int tok = warp; tok < TT; tok += kRtWarps)
+            for (int e = lane; e < E; e += 32) {
+                float v = red[tok * pl.ep + e];
+                for (int s = 1; s < pl.s; ++s) v = __fadd_rn(v, red[(s * TT + tok) * pl.ep + e]);
+                red[tok * pl.ep + e] = v;
+            }
     cluster_sync_all();  // every CTA's sums are in its red[0]
     // finish tokens [c tpc, (c + 1) tpc): add the CTA sums in rank order
-    const int tpc = kRtTok / pl.cs;
+    // (every rank's value is loaded first, then they are added in order)
+    const int tpc = TT / pl.cs;
     float* fin = wbuf;  // [tpc][ep]
-    for (int i = tid; i < tpc * E; i += kRtThreads) {
-        const int tl = i / E, e = i % E;
-        const uint32_t a = smem_u32(red + (c * tpc + tl) * pl.ep + e);
-        float v = ld_dsmem_f32(mapa_shared(a, 0));
-        for (int r = 1; r < pl.cs; ++r) v = __fadd_rn(v, ld_dsmem_f32(mapa_shared(a, r)));
-        fin[tl * pl.ep + e] = v;
-        const int tt = t0 + c * tpc + tl;
-        if (tt < T) logits[static_cast<size_t>(tt) * E + e] = v;
-    }
+    for (int tl = warp; tl < tpc; tl += kRtWarps)
+        for (int e = lane; e < E; e += 32) {
+            const uint32_t a = smem_u32(red + (c * tpc + tl) * pl.ep + e);
+            float part[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) part[r] = r < pl.cs ? ld_dsmem_f32(mapa_shared(a, r)) : 0.0f;
+            float v = part[0];
+#pragma unroll
+            for (int r = 1; r < 8; ++r)
+                if (r < pl.cs) v = __fadd_rn(v, part[r]);
+            fin[tl * pl.ep + e] = v;
+            const int tt = t0 + c * tpc + tl;
+            if (tt < T) logits[static_cast<size_t>(tt) * E + e] = v;
+        }
     cluster_arrive();  // this CTA has read its peers' sums
     __syncthreads();
     for (int tl = warp; tl < tpc; tl += kRtWarps) {
@@ -339,7 +368,7 @@ int launch_router(const void* x, const float* w_router, float* logits, int32_t* 
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>((T + kRtTok - 1) / kRtTok * pl.cs), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>((T + pl.tt - 1) / pl.tt * pl.cs), 1, 1);
     cfg.blockDim = dim3(kRtThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -351,20 +380,23 @@ int launch_router(const void* x, const float* w_router, float* logits, int32_t* 
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_for != dev) {  // every plan fits in kRtMaxSmem bytes
-        for (const void* f : {reinterpret_cast<const void*>(router_topk_kernel<ACT, 8>),
-                              reinterpret_cast<const void*>(router_topk_kernel<ACT, 16>),
-                              reinterpret_cast<const void*>(router_topk_kernel<ACT, 32>)}) {
+        for (const void* f : {reinterpret_cast<const void*>(router_topk_kernel<ACT, 8, 2>),
+                              reinterpret_cast<const void*>(router_topk_kernel<ACT, 16, 2>),
+                              reinterpret_cast<const void*>(router_topk_kernel<ACT, 32, 1>)}) {
             const int rc = set_smem_limit(f, kRtMaxSmem);
             if (rc != MOE_OK) return rc;
         }
         configured_for = dev;
     }
     if (pl.eg == 8)
-        e = cudaLaunchKernelEx(&cfg, router_topk_kernel<ACT, 8>, xp, w_router, logits, ids, w, T, H, E, k, renorm, pl);
+        e = cudaLaunchKernelEx(&cfg, router_topk_kernel<ACT, 8, 2>, xp, w_router, logits, ids, w, T, H, E, k, renorm,
+                               pl);
     else if (pl.eg == 16)
-        e = cudaLaunchKernelEx(&cfg, router_topk_kernel<ACT, 16>, xp, w_router, logits, ids, w, T, H, E, k, renorm, pl);
+        e = cudaLaunchKernelEx(&cfg, router_topk_kernel<ACT, 16, 2>, xp, w_router, logits, ids, w, T, H, E, k, renorm,
+                               pl);
     else
-        e = cudaLaunchKernelEx(&cfg, router_topk_kernel<ACT, 32>, xp, w_router, logits, ids, w, T, H, E, k, renorm, pl);
+        e = cudaLaunchKernelEx(&cfg, router_topk_kernel<ACT, 32, 1>, xp, w_router, logits, ids, w, T, H, E, k, renorm,
+                               pl);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "moe_router_topk_softmax: launch failed: %s", cudaGetErrorString(e));
     count_launch();
     return check_launch("moe_router_topk_softmax");
