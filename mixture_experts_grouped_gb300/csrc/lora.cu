@@ -20,7 +20,9 @@
 namespace moe {
 namespace {
 
-constexpr int kRowTile = 64;
+constexpr int kRowTile = 64;       // rows per expand tile
+constexpr int kColChunk = 512;     // output columns per expand tile (each block walks one chunk)
+constexpr int kShrinkTile = 16;    // rows per shrink tile (two per warp: many rows in flight per SM)
 constexpr int kShrinkWarps = 8;
 constexpr int kExpandThreads = 256;
 
@@ -32,7 +34,7 @@ struct LoraTiles {
 
 // rows of expert e inside the window: [max(off[e], row_offset), min(off[e+1], row_end))
 __device__ void build_lora_tiles(LoraTiles& s, const int32_t* offsets, int n_experts, uint32_t row_offset,
-                                 uint32_t row_end, const uint64_t* a_table) {
+                                 uint32_t row_end, const uint64_t* a_table, int row_tile) {
     const int lane = threadIdx.x & 31;
     if (threadIdx.x < 32) {
         const int per = (n_experts + 31) / 32;
@@ -45,7 +47,7 @@ __device__ void build_lora_tiles(LoraTiles& s, const int32_t* offsets, int n_exp
                 const int lo = max(offsets[e], static_cast<int>(row_offset));
                 const int hi = min(offsets[e + 1], static_cast<int>(row_end));
                 s.lo[e] = lo;
-                if (hi > lo && a_table[e] != 0) c = (hi - lo + kRowTile - 1) / kRowTile;
+                if (hi > lo && a_table[e] != 0) c = (hi - lo + row_tile - 1) / row_tile;
             }
             cnt[j] = c;
             loc += c;
@@ -94,56 +96,91 @@ __device__ __forceinline__ int lora_row_source(int r, const int32_t* sorted_ids,
     return x_gather ? tok : r;
 }
 
-__global__ void __launch_bounds__(32 * kShrinkWarps)
+// One warp per row of a 16-row tile (two rows per warp); the warp's next
+// row's activations are loaded while the current row is reduced. A_e is
+// staged in shared memory when the block's expert changes. The sums run over
+// k in the lane-strided order below for every row, so a row's xa does not
+// depend on which block or warp computed it.
+__global__ void __launch_bounds__(32 * kShrinkWarps, 3)  // three blocks per SM: 48 rows in flight
 lora_shrink_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ offsets,
                    const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ row_adapter,
                    const uint64_t* __restrict__ a_table, __nv_bfloat16* __restrict__ xa, int n_experts, int max_rank,
                    int k_in, uint32_t x_gather, uint32_t row_offset, uint32_t row_end, int P, int top_k,
                    int32_t* err) {
     pdl_wait();
+    constexpr int XV = 3;  // 16-byte activation vectors per lane held at once (k_in <= 768 in one step)
     extern __shared__ __align__(16) uint8_t smem[];
     LoraTiles& s = *reinterpret_cast<LoraTiles*>(smem);
     __nv_bfloat16* sA = reinterpret_cast<__nv_bfloat16*>(smem + ((sizeof(LoraTiles) + 15) / 16) * 16);
-    build_lora_tiles(s, offsets, n_experts, row_offset, row_end, a_table);
+    build_lora_tiles(s, offsets, n_experts, row_offset, row_end, a_table, kShrinkTile);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chunks = k_in / 8;
     int cur_e = -1;
     for (int tile = blockIdx.x; tile < s.n_tiles; tile += gridDim.x) {
         const int e = lora_tile_expert(s, n_experts, tile);
+        const int r0 = s.lo[e] + (tile - s.tstart[e]) * kShrinkTile;
+        const int hi = min(offsets[e + 1], static_cast<int>(row_end));
+        // this warp's rows r0 + warp and r0 + warp + 8: sources, then both rows' first
+        // activations, in flight while A_e is staged
+        int src_row[2];
+        uint4 xv[2][XV];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int r = r0 + warp + q * kShrinkWarps;
+            src_row[q] = r < hi ? lora_row_source(r, sorted_ids, row_adapter, P, top_k, x_gather, err) : -1;
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int i = 0; i < XV; ++i) {
+                const int c = lane + 32 * i;
+                xv[q][i] = (src_row[q] >= 0 && c < chunks)
+                               ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(src_row[q]) * k_in) + c)
+                               : make_uint4(0u, 0u, 0u, 0u);
+            }
         if (e != cur_e) {  // stage A_e [max_rank, k_in] (block-uniform)
             __syncthreads();
             const uint4* src = reinterpret_cast<const uint4*>(a_table[e]);
             for (int i = threadIdx.x; i < max_rank * chunks; i += blockDim.x)
-                reinterpret_cast<uint4*>(sA)[i] = __ldg(src + i);
+                cp_async16(reinterpret_cast<uint4*>(sA) + i, src + i);
+            cp_async_commit();
+            cp_async_wait_all();
             __syncthreads();
             cur_e = e;
         }
-        const int r0 = s.lo[e] + (tile - s.tstart[e]) * kRowTile;
-        const int hi = min(offsets[e + 1], static_cast<int>(row_end));
-        for (int rr = warp; rr < kRowTile; rr += kShrinkWarps) {
-            const int r = r0 + rr;
-            if (r >= hi) break;
-            const int src_row = lora_row_source(r, sorted_ids, row_adapter, P, top_k, x_gather, err);
-            if (src_row < 0) continue;
-            const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(src_row) * k_in);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            if (src_row[q] < 0) continue;  // warp-uniform
+            const int r = r0 + warp + q * kShrinkWarps;
+            const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(src_row[q]) * k_in);
             for (int j0 = 0; j0 < max_rank; j0 += 16) {
                 float acc[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-                for (int c = lane; c < chunks; c += 32) {
-                    const uint4 xv = __ldg(xr + c);
-                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                for (int cb = 0; cb < chunks; cb += 32 * XV) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        if (j0 + j < max_rank) {
-                            const uint4 av = reinterpret_cast<const uint4*>(sA)[(j0 + j) * chunks + c];
-                            const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+                    for (int i = 0; i < XV; ++i) {
+                        const int c = cb + lane + 32 * i;
+                        if (c >= chunks) break;
+                        const uint4 v = cb == 0 ? xv[q][i] : __ldg(xr + c);
+                        float xf[8];
+                        {
+                            const float2 a = Act<MOE_ACT_BF16>::unpack2(v.x), b = Act<MOE_ACT_BF16>::unpack2(v.y);
+                            const float2 cc = Act<MOE_ACT_BF16>::unpack2(v.z), d = Act<MOE_ACT_BF16>::unpack2(v.w);
+                            xf[0] = a.x; xf[1] = a.y; xf[2] = b.x; xf[3] = b.y;
+                            xf[4] = cc.x; xf[5] = cc.y; xf[6] = d.x; xf[7] = d.y;
+                        }
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const float2 a2 = Act<MOE_ACT_BF16>::unpack2(aw[q]);
-                                const float2 x2 = Act<MOE_ACT_BF16>::unpack2(xw[q]);
-                                acc[j] = fmaf(x2.x, a2.x, acc[j]);
-                                acc[j] = fmaf(x2.y, a2.y, acc[j]);
+                        for (int j = 0; j < 16; ++j) {
+                            if (j0 + j < max_rank) {
+                                const uint4 av = reinterpret_cast<const uint4*>(sA)[(j0 + j) * chunks + c];
+                                const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+                                for (int h = 0; h < 4; ++h) {
+                                    const float2 a2 = Act<MOE_ACT_BF16>::unpack2(aw[h]);
+                                    acc[j] = fmaf(xf[2 * h], a2.x, acc[j]);
+                                    acc[j] = fmaf(xf[2 * h + 1], a2.y, acc[j]);
+                                }
                             }
                         }
                     }
@@ -164,61 +201,204 @@ lora_shrink_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restric
     }
 }
 
-// RCAP: rank capacity of this instantiation; CPC: output columns per thread,
-// chosen so a thread holds RCAP * CPC = 64 B_e values in registers.
+// Two fused multiply-adds on a pair of f32 values in one instruction:
+// d.x = fma(a.x, b.x, c.x), d.y = fma(a.y, b.y, c.y), each rounded once.
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f32x2_pack(float lo, float hi) {
+    return (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+
+// Packed storage of N consecutive bf16 values (N = 4, 2 or 1): one load or
+// store moves a thread's columns of a row.
+template <int N> struct BfPack;
+template <> struct BfPack<4> {
+    using V = uint2;
+    static __device__ __forceinline__ float get(const V& v, int i) {
+        const uint32_t w = (i < 2) ? v.x : v.y;
+        return __uint_as_float((i & 1) ? (w & 0xffff0000u) : (w << 16));
+    }
+    static __device__ __forceinline__ void set(V& v, int i, __nv_bfloat16 b) {
+        const uint32_t u = __bfloat16_as_ushort(b);
+        uint32_t& w = (i < 2) ? v.x : v.y;
+        w = (i & 1) ? ((w & 0x0000ffffu) | (u << 16)) : ((w & 0xffff0000u) | u);
+    }
+};
+template <> struct BfPack<2> {
+    using V = uint32_t;
+    static __device__ __forceinline__ float get(const V& v, int i) {
+        return __uint_as_float(i ? (v & 0xffff0000u) : (v << 16));
+    }
+    static __device__ __forceinline__ void set(V& v, int i, __nv_bfloat16 b) {
+        const uint32_t u = __bfloat16_as_ushort(b);
+        v = i ? ((v & 0x0000ffffu) | (u << 16)) : ((v & 0xffff0000u) | u);
+    }
+};
+template <> struct BfPack<1> {
+    using V = unsigned short;
+    static __device__ __forceinline__ float get(const V& v, int) { return __uint_as_float(static_cast<uint32_t>(v) << 16); }
+    static __device__ __forceinline__ void set(V& v, int, __nv_bfloat16 b) { v = __bfloat16_as_ushort(b); }
+};
+
+// One warp-level tensor-core product D[16 x 8] += A[16 x 16] * B[16 x 8]
+// (bf16 inputs, f32 accumulation): a = four bf16 pairs of A (rows g, g + 8;
+// k = 2t, 2t + 1 and 2t + 8, 2t + 9), b = two pairs of B (k = 2t, 2t + 1 and
+// 2t + 8, 2t + 9; column g), d = D[g][2t], D[g][2t + 1], D[g + 8][2t],
+// D[g + 8][2t + 1], with g = lane / 4 and t = lane % 4.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// RCAP: rank capacity of this instantiation (16, 32 or 64: one to four
+// k16 steps). A block takes one work tile: 64 rows of an expert's span
+// (inside the window) times a chunk of 512 output columns. It copies the
+// tile's base values into shared memory with cp.async (64 KB in flight at
+// once) while it stages the rows' xa (bf16, as stored) and which rows fold.
+// The rank-RCAP product delta = xa . B_e^T is a K = RCAP contraction: warp w
+// computes it for all 64 rows and columns [64 w, 64 w + 64) of the chunk
+// with warp-level tensor-core products (16 rows x 8 columns each, f32
+// accumulation; a tcgen05 tile of 128 rows would need TMEM and shared-memory
+// descriptors for a contraction of 16, and the kernel is bound by the base
+// values' read and write anyway), then rounds each sum to bf16, folds it into
+// the staged base value and stores the pair of columns to global memory.
 template <int RCAP>
-__global__ void __launch_bounds__(kExpandThreads)
+__global__ void __launch_bounds__(kExpandThreads, RCAP <= 16 ? 3 : 2)
 lora_expand_fold_kernel(const __nv_bfloat16* __restrict__ xa, const int32_t* __restrict__ offsets,
                         const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ row_adapter,
                         const uint64_t* __restrict__ b_table, const float* __restrict__ scale_table,
                         __nv_bfloat16* __restrict__ base, int n_experts, int n_out, int max_rank, uint32_t row_offset,
                         uint32_t row_end, int P, int top_k, const uint64_t* __restrict__ a_table) {
     pdl_wait();
-    constexpr int CPC = 64 / RCAP;
-    __shared__ LoraTiles s;
-    __shared__ int s_src[kRowTile];
-    __shared__ __align__(16) float s_xa[kRowTile][RCAP];
-    build_lora_tiles(s, offsets, n_experts, row_offset, row_end, a_table);
-    for (int tile = blockIdx.x; tile < s.n_tiles; tile += gridDim.x) {
+    constexpr int KS = RCAP / 16;  // k16 steps
+    extern __shared__ __align__(16) uint8_t lsm[];
+    LoraTiles& s = *reinterpret_cast<LoraTiles*>(lsm);
+    size_t off = (sizeof(LoraTiles) + 15) / 16 * 16;
+    int* s_src = reinterpret_cast<int*>(lsm + off);
+    off += kRowTile * sizeof(int);
+    uint32_t* s_xa = reinterpret_cast<uint32_t*>(lsm + off);  // [kRowTile][RCAP / 2] bf16 pairs
+    off += static_cast<size_t>(kRowTile) * RCAP * 2;
+    uint32_t* s_y = reinterpret_cast<uint32_t*>(lsm + off);   // [kRowTile][kColChunk / 2] bf16 pairs
+    build_lora_tiles(s, offsets, n_experts, row_offset, row_end, a_table, kRowTile);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int n_chunks = (n_out + kColChunk - 1) / kColChunk;
+    for (int wt = blockIdx.x; wt < s.n_tiles * n_chunks; wt += gridDim.x) {
+        const int tile = wt / n_chunks, chunk = wt - tile * n_chunks;
         const int e = lora_tile_expert(s, n_experts, tile);
         const int r0 = s.lo[e] + (tile - s.tstart[e]) * kRowTile;
         const int hi = min(offsets[e + 1], static_cast<int>(row_end));
         const int nrows = min(kRowTile, hi - r0);
-        __syncthreads();  // previous tile done with s_src / s_xa
-        for (int i = threadIdx.x; i < nrows; i += blockDim.x)
-            s_src[i] = lora_row_source(r0 + i, sorted_ids, row_adapter, P, top_k, 0, nullptr);
-        __syncthreads();
-        for (int i = threadIdx.x; i < nrows * RCAP; i += blockDim.x) {
-            const int rr = i / RCAP, j = i - rr * RCAP;
-            s_xa[rr][j] = (s_src[rr] >= 0 && j < max_rank)
-                              ? __bfloat162float(xa[static_cast<size_t>(r0 + rr - row_offset) * max_rank + j])
-                              : 0.0f;
+        const int c0 = chunk * kColChunk;
+        const int ncols = min(kColChunk, n_out - c0);  // a multiple of 4
+        __syncthreads();  // the previous tile is done with the shared buffers
+        // 1. the tile's base values: 8-byte copies, every one in flight at once
+        {
+            const int per_row = ncols / 4;
+            for (int i = threadIdx.x; i < nrows * per_row; i += blockDim.x) {
+                const int rr = i / per_row, q = i - rr * per_row;
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(s_y + rr * (kColChunk / 2) + 2 * q)),
+                             "l"(base + static_cast<size_t>(r0 + rr) * n_out + c0 + 4 * q)
+                             : "memory");
+            }
+            cp_async_commit();
         }
+        // 2. meanwhile: which rows fold and their xa (zero for rows that do not fold,
+        // for rows past the tile and for ranks past max_rank)
+        for (int i = threadIdx.x; i < kRowTile; i += blockDim.x)
+            s_src[i] = i < nrows ? lora_row_source(r0 + i, sorted_ids, row_adapter, P, top_k, 0, nullptr) : -1;
         __syncthreads();
+        for (int i = threadIdx.x; i < kRowTile * (RCAP / 2); i += blockDim.x) {
+            const int rr = i / (RCAP / 2), jp = i - rr * (RCAP / 2);
+            uint32_t v = 0u;
+            if (s_src[rr] >= 0) {
+                const __nv_bfloat16* src = xa + static_cast<size_t>(r0 + rr - row_offset) * max_rank;
+                const uint32_t lo = 2 * jp < max_rank ? __bfloat16_as_ushort(src[2 * jp]) : 0u;
+                const uint32_t hi2 = 2 * jp + 1 < max_rank ? __bfloat16_as_ushort(src[2 * jp + 1]) : 0u;
+                v = lo | (hi2 << 16);
+            }
+            s_xa[rr * (RCAP / 2) + jp] = v;
+        }
         const float sc = scale_table[e];
         const __nv_bfloat16* B = reinterpret_cast<const __nv_bfloat16*>(b_table[e]);
-        for (int n0 = threadIdx.x * CPC; n0 < n_out; n0 += blockDim.x * CPC) {
-            float bw[CPC][RCAP];
+        cp_async_wait_all();
+        __syncthreads();
+        // 3. xa fragments of the four 16-row blocks, held for the whole chunk
+        uint32_t af[4][KS][4];
 #pragma unroll
-            for (int i = 0; i < CPC; ++i)
+        for (int mb = 0; mb < 4; ++mb)
 #pragma unroll
-                for (int j = 0; j < RCAP; ++j)
-                    bw[i][j] = (j < max_rank) ? __bfloat162float(B[static_cast<size_t>(n0 + i) * max_rank + j]) : 0.0f;
-            for (int rr = 0; rr < nrows; ++rr) {
-                if (s_src[rr] < 0) continue;
-                __nv_bfloat16* yrow = base + static_cast<size_t>(r0 + rr) * n_out + n0;
+            for (int ks = 0; ks < KS; ++ks) {
+                const uint32_t* r_lo = s_xa + (16 * mb + g) * (RCAP / 2) + 8 * ks + t;
+                const uint32_t* r_hi = r_lo + 8 * (RCAP / 2);
+                af[mb][ks][0] = r_lo[0];
+                af[mb][ks][1] = r_hi[0];
+                af[mb][ks][2] = r_lo[4];
+                af[mb][ks][3] = r_hi[4];
+            }
+        // 4. this warp's columns [64 w, 64 w + 64) of the chunk, 8 at a time; the B_e
+        // fragments of all eight blocks are loaded first (one round trip to L2)
+        uint32_t bfa[8][KS][2];
 #pragma unroll
-                for (int i = 0; i < CPC; ++i) {
-                    float acc = 0.0f;
+        for (int nb = 0; nb < 8; ++nb) {
+            const int n = c0 + 64 * warp + 8 * nb + g;  // this lane's column of B (the MMA's n index)
 #pragma unroll
-                    for (int j = 0; j < RCAP; ++j) acc = fmaf(s_xa[rr][j], bw[i][j], acc);
-                    const float d = __bfloat162float(__float2bfloat16_rn(acc));  // bf16 delta
-                    const float y = __bfloat162float(yrow[i]);
-                    yrow[i] = __float2bfloat16_rn(__fadd_rn(y, __fmul_rn(sc, d)));
+            for (int ks = 0; ks < KS; ++ks) {
+                // pairs (k = 16 ks + 2t, +1) and (+8, +9) of B_e row n; zero past the chunk or max_rank
+                uint32_t b0 = 0u, b1 = 0u;
+                if (64 * warp + 8 * nb + g < ncols) {
+                    const __nv_bfloat16* brow = B + static_cast<size_t>(n) * max_rank;
+                    const int k0 = 16 * ks + 2 * t, k1 = k0 + 8;
+                    b0 = (k0 < max_rank ? __bfloat16_as_ushort(brow[k0]) : 0u) |
+                         ((k0 + 1 < max_rank ? static_cast<uint32_t>(__bfloat16_as_ushort(brow[k0 + 1])) : 0u) << 16);
+                    b1 = (k1 < max_rank ? __bfloat16_as_ushort(brow[k1]) : 0u) |
+                         ((k1 + 1 < max_rank ? static_cast<uint32_t>(__bfloat16_as_ushort(brow[k1 + 1])) : 0u) << 16);
+                }
+                bfa[nb][ks][0] = b0;
+                bfa[nb][ks][1] = b1;
+            }
+        }
+#pragma unroll
+        for (int nb = 0; nb < 8; ++nb) {
+            const int cl0 = 64 * warp + 8 * nb;  // first chunk column of the block
+            if (cl0 >= ncols) break;             // warp-uniform
+            const uint32_t (&bf)[KS][2] = bfa[nb];
+#pragma unroll
+            for (int mb = 0; mb < 4; ++mb) {
+                float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) mma_bf16_16816(d, af[mb][ks], bf[ks]);
+                // d: rows 16 mb + g (d0, d1) and 16 mb + g + 8 (d2, d3), columns cl0 + 2t, + 1
+                const int cl = cl0 + 2 * t;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int rr = 16 * mb + g + 8 * h;
+                    if (rr >= nrows || s_src[rr] < 0 || cl >= ncols) continue;
+                    const uint32_t yv = s_y[rr * (kColChunk / 2) + cl / 2];
+                    const float d0 = __bfloat162float(__float2bfloat16_rn(d[2 * h]));      // bf16 delta
+                    const float d1 = __bfloat162float(__float2bfloat16_rn(d[2 * h + 1]));
+                    const float y0 = __uint_as_float(yv << 16), y1 = __uint_as_float(yv & 0xffff0000u);
+                    const uint32_t o0 = __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(y0, __fmul_rn(sc, d0))));
+                    const uint32_t o1 = __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(y1, __fmul_rn(sc, d1))));
+                    *reinterpret_cast<uint32_t*>(base + static_cast<size_t>(r0 + rr) * n_out + c0 + cl) =
+                        o0 | (o1 << 16);
                 }
             }
         }
     }
+}
+
+// dynamic shared memory of an expand instantiation
+template <int RCAP>
+size_t lora_expand_smem() {
+    return (sizeof(LoraTiles) + 15) / 16 * 16 + kRowTile * sizeof(int) + static_cast<size_t>(kRowTile) * RCAP * 2 +
+           static_cast<size_t>(kRowTile) * kColChunk * 2;
 }
 
 // ---- decode gather fold: slot-major rows --------------------------------------
@@ -367,13 +547,17 @@ extern "C" int moe_lora_grouped_down(const MoeExpertRoute* route, const void* x,
                     sorted_token_ids && xa,
                 "%s: NULL pointer", who);
     MOE_REQUIRE(moe::aligned16(x), "%s: x must be 16-byte aligned", who);
+    MOE_REQUIRE((reinterpret_cast<uintptr_t>(base_out) & 7) == 0, "%s: base_out must be 8-byte aligned", who);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int P = num_tokens * top_k;
     const int sms = moe::sm_count();
     if (sms <= 0) return moe::fail(MOE_ERR_CUDA, "%s: cannot query the SM count", who);
     const int window = static_cast<int>(row_end - row_offset);
-    const int max_tiles = (window + moe::kRowTile - 1) / moe::kRowTile + static_cast<int>(route->n_experts);
-    const int grid = max_tiles < sms * 2 ? max_tiles : sms * 2;
+    const int n_chunks = (static_cast<int>(route->n_out) + moe::kColChunk - 1) / moe::kColChunk;
+    const long max_tiles = static_cast<long>((window + moe::kRowTile - 1) / moe::kRowTile + route->n_experts) * n_chunks;
+    const int grid = static_cast<int>(max_tiles < sms * 4 ? max_tiles : sms * 4);
+    const int s_tiles = (window + moe::kShrinkTile - 1) / moe::kShrinkTile + static_cast<int>(route->n_experts);
+    const int s_grid = s_tiles < sms * 4 ? s_tiles : sms * 4;
 
     const size_t shrink_smem = ((sizeof(moe::LoraTiles) + 15) / 16) * 16 +
                                static_cast<size_t>(route->max_rank) * route->k_in * 2;
@@ -383,10 +567,19 @@ extern "C" int moe_lora_grouped_down(const MoeExpertRoute* route, const void* x,
     cudaGetDevice(&dev);
     if (configured_for != dev) {
         int rc = moe::set_smem_limit(reinterpret_cast<const void*>(moe::lora_shrink_kernel), 200 * 1024);
+        if (rc == MOE_OK)
+            rc = moe::set_smem_limit(reinterpret_cast<const void*>(moe::lora_expand_fold_kernel<16>),
+                                     static_cast<int>(moe::lora_expand_smem<16>()));
+        if (rc == MOE_OK)
+            rc = moe::set_smem_limit(reinterpret_cast<const void*>(moe::lora_expand_fold_kernel<32>),
+                                     static_cast<int>(moe::lora_expand_smem<32>()));
+        if (rc == MOE_OK)
+            rc = moe::set_smem_limit(reinterpret_cast<const void*>(moe::lora_expand_fold_kernel<64>),
+                                     static_cast<int>(moe::lora_expand_smem<64>()));
         if (rc != MOE_OK) return rc;
         configured_for = dev;
     }
-    moe::launch_pdl(moe::lora_shrink_kernel, grid, 32 * moe::kShrinkWarps, shrink_smem, st,
+    moe::launch_pdl(moe::lora_shrink_kernel, s_grid, 32 * moe::kShrinkWarps, shrink_smem, st,
         static_cast<const __nv_bfloat16*>(x), expert_offsets, sorted_token_ids, row_adapter, route->a_table,
         static_cast<__nv_bfloat16*>(xa), route->n_experts, route->max_rank, route->k_in, x_gather, row_offset,
         row_end, P, top_k, nullptr);
@@ -396,15 +589,15 @@ extern "C" int moe_lora_grouped_down(const MoeExpertRoute* route, const void* x,
     const auto* xa_p = static_cast<const __nv_bfloat16*>(xa);
     auto* base_p = static_cast<__nv_bfloat16*>(base_out);
     if (route->max_rank <= 16)
-        moe::launch_pdl(moe::lora_expand_fold_kernel<16>, grid, moe::kExpandThreads, 0, st,
+        moe::launch_pdl(moe::lora_expand_fold_kernel<16>, grid, moe::kExpandThreads, moe::lora_expand_smem<16>(), st,
             xa_p, expert_offsets, sorted_token_ids, row_adapter, route->b_table, route->scale_table, base_p,
             route->n_experts, route->n_out, route->max_rank, row_offset, row_end, P, top_k, route->a_table);
     else if (route->max_rank <= 32)
-        moe::launch_pdl(moe::lora_expand_fold_kernel<32>, grid, moe::kExpandThreads, 0, st,
+        moe::launch_pdl(moe::lora_expand_fold_kernel<32>, grid, moe::kExpandThreads, moe::lora_expand_smem<32>(), st,
             xa_p, expert_offsets, sorted_token_ids, row_adapter, route->b_table, route->scale_table, base_p,
             route->n_experts, route->n_out, route->max_rank, row_offset, row_end, P, top_k, route->a_table);
     else
-        moe::launch_pdl(moe::lora_expand_fold_kernel<64>, grid, moe::kExpandThreads, 0, st,
+        moe::launch_pdl(moe::lora_expand_fold_kernel<64>, grid, moe::kExpandThreads, moe::lora_expand_smem<64>(), st,
             xa_p, expert_offsets, sorted_token_ids, row_adapter, route->b_table, route->scale_table, base_p,
             route->n_experts, route->n_out, route->max_rank, row_offset, row_end, P, top_k, route->a_table);
     moe::count_launch();
