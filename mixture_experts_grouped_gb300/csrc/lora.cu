@@ -22,7 +22,7 @@ namespace {
 
 constexpr int kRowTile = 64;       // rows per expand tile
 constexpr int kColChunk = 512;     // output columns per expand tile (each block walks one chunk)
-constexpr int kShrinkTile = 16;    // rows per shrink tile (two per warp: many rows in flight per SM)
+constexpr int kShrinkTile = 64;    // rows per shrink tile: four 16-row blocks
 constexpr int kShrinkWarps = 8;
 constexpr int kExpandThreads = 256;
 
@@ -32,25 +32,25 @@ struct LoraTiles {
     int lo[MOE_MAX_EXPERTS];
 };
 
-// rows of expert e inside the window: [max(off[e], row_offset), min(off[e+1], row_end))
+// rows of expert e inside the window: [max(off[e], row_offset), min(off[e+1], row_end)).
+// Every thread of the block first computes the tile counts of its experts
+// (all loads issued together), then warp 0 scans them.
 __device__ void build_lora_tiles(LoraTiles& s, const int32_t* offsets, int n_experts, uint32_t row_offset,
                                  uint32_t row_end, const uint64_t* a_table, int row_tile) {
+    for (int e = threadIdx.x; e < n_experts; e += blockDim.x) {
+        const int lo = max(offsets[e], static_cast<int>(row_offset));
+        const int hi = min(offsets[e + 1], static_cast<int>(row_end));
+        s.lo[e] = lo;
+        s.tstart[e] = (hi > lo && a_table[e] != 0) ? (hi - lo + row_tile - 1) / row_tile : 0;  // counts for now
+    }
+    __syncthreads();
     const int lane = threadIdx.x & 31;
     if (threadIdx.x < 32) {
-        const int per = (n_experts + 31) / 32;
-        int cnt[8];
+        const int per = (n_experts + 31) / 32;  // <= 8
         int loc = 0;
-        for (int j = 0; j < per && j < 8; ++j) {
+        for (int j = 0; j < per; ++j) {
             const int e = lane * per + j;
-            int c = 0;
-            if (e < n_experts) {
-                const int lo = max(offsets[e], static_cast<int>(row_offset));
-                const int hi = min(offsets[e + 1], static_cast<int>(row_end));
-                s.lo[e] = lo;
-                if (hi > lo && a_table[e] != 0) c = (hi - lo + row_tile - 1) / row_tile;
-            }
-            cnt[j] = c;
-            loc += c;
+            if (e < n_experts) loc += s.tstart[e];
         }
         int inc = loc;
         for (int d = 1; d < 32; d <<= 1) {
@@ -58,11 +58,12 @@ __device__ void build_lora_tiles(LoraTiles& s, const int32_t* offsets, int n_exp
             if (lane >= d) inc += o;
         }
         int run = inc - loc;
-        for (int j = 0; j < per && j < 8; ++j) {
+        for (int j = 0; j < per; ++j) {
             const int e = lane * per + j;
             if (e < n_experts) {
+                const int c = s.tstart[e];
                 s.tstart[e] = run;
-                run += cnt[j];
+                run += c;
             }
         }
         if (lane == 31) {
@@ -96,106 +97,91 @@ __device__ __forceinline__ int lora_row_source(int r, const int32_t* sorted_ids,
     return x_gather ? tok : r;
 }
 
-// One warp per row of a 16-row tile (two rows per warp); the warp's next
-// row's activations are loaded while the current row is reduced. A_e is
-// staged in shared memory when the block's expert changes. The sums run over
-// k in the lane-strided order below for every row, so a row's xa does not
-// depend on which block or warp computed it.
-__global__ void __launch_bounds__(32 * kShrinkWarps, 3)  // three blocks per SM: 48 rows in flight
+// One warp-level tensor-core product D[16 x 8] += A[16 x 16] * B[16 x 8]
+// (bf16 inputs, f32 accumulation): a = four bf16 pairs of A (rows g, g + 8;
+// k = 2t, 2t + 1 and 2t + 8, 2t + 9), b = two pairs of B (k = 2t, 2t + 1 and
+// 2t + 8, 2t + 9; column g), d = D[g][2t], D[g][2t + 1], D[g + 8][2t],
+// D[g + 8][2t + 1], with g = lane / 4 and t = lane % 4.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// xa = bf16(xrow . A_e^T) for the rows of 64-row tiles: a contraction of
+// k_in (768 in the workloads) into max_rank sums, run as warp-level
+// tensor-core products (bf16 in, f32 accumulation). Warp task (m, n) covers
+// 16 rows x 8 ranks over the whole contraction: its x fragments come straight
+// from global memory (rows that fold nothing, or lie past the span, read as
+// zeros), its A_e fragments from shared memory (staged by cp.async when the
+// block's expert changes). Each sum is rounded once to bf16.
+__global__ void __launch_bounds__(32 * kShrinkWarps, 3)
 lora_shrink_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ offsets,
                    const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ row_adapter,
                    const uint64_t* __restrict__ a_table, __nv_bfloat16* __restrict__ xa, int n_experts, int max_rank,
                    int k_in, uint32_t x_gather, uint32_t row_offset, uint32_t row_end, int P, int top_k,
                    int32_t* err) {
     pdl_wait();
-    constexpr int XV = 3;  // 16-byte activation vectors per lane held at once (k_in <= 768 in one step)
     extern __shared__ __align__(16) uint8_t smem[];
     LoraTiles& s = *reinterpret_cast<LoraTiles*>(smem);
-    __nv_bfloat16* sA = reinterpret_cast<__nv_bfloat16*>(smem + ((sizeof(LoraTiles) + 15) / 16) * 16);
+    __shared__ int s_src[kShrinkTile];
+    const uint32_t* sA = reinterpret_cast<const uint32_t*>(smem + ((sizeof(LoraTiles) + 15) / 16) * 16);
     build_lora_tiles(s, offsets, n_experts, row_offset, row_end, a_table, kShrinkTile);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int chunks = k_in / 8;
+    const int g = lane >> 2, t = lane & 3;
+    const int kw = k_in / 2;                 // bf16 pairs per row
+    const int ksteps = (k_in + 15) / 16;     // a last step past k_in reads zeros
+    const int nblocks = (max_rank + 7) / 8;  // 8-rank blocks
     int cur_e = -1;
     for (int tile = blockIdx.x; tile < s.n_tiles; tile += gridDim.x) {
         const int e = lora_tile_expert(s, n_experts, tile);
         const int r0 = s.lo[e] + (tile - s.tstart[e]) * kShrinkTile;
         const int hi = min(offsets[e + 1], static_cast<int>(row_end));
-        // this warp's rows r0 + warp and r0 + warp + 8: sources, then both rows' first
-        // activations, in flight while A_e is staged
-        int src_row[2];
-        uint4 xv[2][XV];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int r = r0 + warp + q * kShrinkWarps;
-            src_row[q] = r < hi ? lora_row_source(r, sorted_ids, row_adapter, P, top_k, x_gather, err) : -1;
-        }
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-#pragma unroll
-            for (int i = 0; i < XV; ++i) {
-                const int c = lane + 32 * i;
-                xv[q][i] = (src_row[q] >= 0 && c < chunks)
-                               ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(src_row[q]) * k_in) + c)
-                               : make_uint4(0u, 0u, 0u, 0u);
-            }
+        __syncthreads();  // the previous tile is done with s_src and A_e
+        for (int i = threadIdx.x; i < kShrinkTile; i += blockDim.x)
+            s_src[i] = r0 + i < hi ? lora_row_source(r0 + i, sorted_ids, row_adapter, P, top_k, x_gather, err) : -1;
         if (e != cur_e) {  // stage A_e [max_rank, k_in] (block-uniform)
-            __syncthreads();
             const uint4* src = reinterpret_cast<const uint4*>(a_table[e]);
-            for (int i = threadIdx.x; i < max_rank * chunks; i += blockDim.x)
-                cp_async16(reinterpret_cast<uint4*>(sA) + i, src + i);
+            for (int i = threadIdx.x; i < max_rank * (k_in / 8); i += blockDim.x)
+                cp_async16(reinterpret_cast<uint4*>(const_cast<uint32_t*>(sA)) + i, src + i);
             cp_async_commit();
             cp_async_wait_all();
-            __syncthreads();
             cur_e = e;
         }
+        __syncthreads();
+        for (int task = warp; task < 4 * nblocks; task += kShrinkWarps) {
+            const int mb = task & 3, nb = task >> 2;
+            const int rl = 16 * mb + g, rh = rl + 8;  // this lane's two tile rows
+            const int sl = s_src[rl], sh = s_src[rh];
+            if (__all_sync(0xffffffffu, sl < 0 && sh < 0)) continue;  // no row of the block folds
+            const uint32_t* xl = reinterpret_cast<const uint32_t*>(x + static_cast<size_t>(sl < 0 ? 0 : sl) * k_in);
+            const uint32_t* xh = reinterpret_cast<const uint32_t*>(x + static_cast<size_t>(sh < 0 ? 0 : sh) * k_in);
+            const int j = 8 * nb + g;  // this lane's rank (the MMA's n index)
+            const uint32_t* ar = sA + static_cast<size_t>(j < max_rank ? j : 0) * kw;
+            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+            for (int ks = 0; ks < ksteps; ++ks) {
+                const int p0 = 8 * ks + t, p1 = p0 + 4;  // pair indices of k = 16 ks + 2t and + 8
+                uint32_t a[4], b[2];
+                a[0] = (sl >= 0 && p0 < kw) ? __ldg(xl + p0) : 0u;
+                a[1] = (sh >= 0 && p0 < kw) ? __ldg(xh + p0) : 0u;
+                a[2] = (sl >= 0 && p1 < kw) ? __ldg(xl + p1) : 0u;
+                a[3] = (sh >= 0 && p1 < kw) ? __ldg(xh + p1) : 0u;
+                b[0] = (j < max_rank && p0 < kw) ? ar[p0] : 0u;
+                b[1] = (j < max_rank && p1 < kw) ? ar[p1] : 0u;
+                mma_bf16_16816(d, a, b);
+            }
+            // d: (row rl; ranks 8 nb + 2t, + 1) and (row rh; same ranks)
+            const int jr = 8 * nb + 2 * t;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            if (src_row[q] < 0) continue;  // warp-uniform
-            const int r = r0 + warp + q * kShrinkWarps;
-            const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(src_row[q]) * k_in);
-            for (int j0 = 0; j0 < max_rank; j0 += 16) {
-                float acc[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-                for (int cb = 0; cb < chunks; cb += 32 * XV) {
-#pragma unroll
-                    for (int i = 0; i < XV; ++i) {
-                        const int c = cb + lane + 32 * i;
-                        if (c >= chunks) break;
-                        const uint4 v = cb == 0 ? xv[q][i] : __ldg(xr + c);
-                        float xf[8];
-                        {
-                            const float2 a = Act<MOE_ACT_BF16>::unpack2(v.x), b = Act<MOE_ACT_BF16>::unpack2(v.y);
-                            const float2 cc = Act<MOE_ACT_BF16>::unpack2(v.z), d = Act<MOE_ACT_BF16>::unpack2(v.w);
-                            xf[0] = a.x; xf[1] = a.y; xf[2] = b.x; xf[3] = b.y;
-                            xf[4] = cc.x; xf[5] = cc.y; xf[6] = d.x; xf[7] = d.y;
-                        }
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            if (j0 + j < max_rank) {
-                                const uint4 av = reinterpret_cast<const uint4*>(sA)[(j0 + j) * chunks + c];
-                                const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-                                for (int h = 0; h < 4; ++h) {
-                                    const float2 a2 = Act<MOE_ACT_BF16>::unpack2(aw[h]);
-                                    acc[j] = fmaf(xf[2 * h], a2.x, acc[j]);
-                                    acc[j] = fmaf(xf[2 * h + 1], a2.y, acc[j]);
-                                }
-                            }
-                        }
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], off);
-                if (lane < 16 && j0 + lane < max_rank) {
-                    float v = 0.0f;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (j == lane) v = acc[j];
-                    xa[static_cast<size_t>(r - row_offset) * max_rank + j0 + lane] = __float2bfloat16_rn(v);
-                }
+            for (int h = 0; h < 2; ++h) {
+                const int rr = h ? rh : rl;
+                if ((h ? sh : sl) < 0) continue;
+                __nv_bfloat16* dst = xa + static_cast<size_t>(r0 + rr - row_offset) * max_rank + jr;
+                if (jr < max_rank) dst[0] = __float2bfloat16_rn(d[2 * h]);
+                if (jr + 1 < max_rank) dst[1] = __float2bfloat16_rn(d[2 * h + 1]);
             }
         }
     }
@@ -242,19 +228,6 @@ template <> struct BfPack<1> {
     static __device__ __forceinline__ float get(const V& v, int) { return __uint_as_float(static_cast<uint32_t>(v) << 16); }
     static __device__ __forceinline__ void set(V& v, int, __nv_bfloat16 b) { v = __bfloat16_as_ushort(b); }
 };
-
-// One warp-level tensor-core product D[16 x 8] += A[16 x 16] * B[16 x 8]
-// (bf16 inputs, f32 accumulation): a = four bf16 pairs of A (rows g, g + 8;
-// k = 2t, 2t + 1 and 2t + 8, 2t + 9), b = two pairs of B (k = 2t, 2t + 1 and
-// 2t + 8, 2t + 9; column g), d = D[g][2t], D[g][2t + 1], D[g + 8][2t],
-// D[g + 8][2t + 1], with g = lane / 4 and t = lane % 4.
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
 
 // RCAP: rank capacity of this instantiation (16, 32 or 64: one to four
 // k16 steps). A block takes one work tile: 64 rows of an expert's span
