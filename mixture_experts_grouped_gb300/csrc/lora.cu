@@ -6,41 +6,58 @@
 // row_end) of the sorted rows, with expert spans read from expert_offsets on
 // the device. The page sizes a static worst-case grid (ceil(window/64) x
 // n_experts) whose tiles mostly return at once; here a persistent grid walks
-// only the non-empty 64-row tiles of span intersect window, listed in shared
+// only the non-empty row tiles of span intersect window, listed in shared
 // memory from expert_offsets at kernel start.
 //
 // The work is HBM-bound (rank 16: 2 x rank FLOPs per element of base read and
-// written), so both kernels are shaped for coalesced 16-byte / 8-byte access:
-//   shrink: a warp per row, lanes split k_in in 16-byte chunks, A_e staged in
-//           shared memory, rank partial sums reduced across the warp;
-//   expand: each thread owns 64 / rank-capacity consecutive output columns
-//           and keeps their B_e rows in registers, walking the tile's rows.
+// written), so both kernels keep many copies in flight through cp.async rings
+// in shared memory and run their small contractions on warp-level tensor-core
+// products:
+//   shrink: 64-row tiles, the contraction streamed in 128-column stages (x rows
+//           and A_e rows side by side), ldmatrix fragments;
+//   expand: contiguous ranges of (32-row tile, 256-column) units per block,
+//           three units in flight, folded in shared memory and written back
+//           with full-width stores.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kRowTile = 64;       // rows per expand tile
-constexpr int kColChunk = 512;     // output columns per expand tile (each block walks one chunk)
-constexpr int kShrinkTile = 64;    // rows per shrink tile: four 16-row blocks
+constexpr int kShrinkRows = 64;               // rows per shrink tile: four 16-row blocks
+constexpr int kShrinkK = 128;                 // contraction columns per shrink stage
+constexpr int kShrinkPitch = kShrinkK + 8;    // bf16 per staged row: 272 bytes, rows 4 banks apart
+constexpr int kShrinkStages = 4;
 constexpr int kShrinkWarps = 8;
-constexpr int kExpandThreads = 256;
+constexpr int kExRows = 32;                   // rows per expand tile
+constexpr int kExCols = 256;                  // output columns per expand unit
+constexpr int kExStages = 4;
+constexpr int kExThreads = 256;
 
 struct LoraTiles {
     int n_tiles;
     int tstart[MOE_MAX_EXPERTS + 1];
     int lo[MOE_MAX_EXPERTS];
+    int hi[MOE_MAX_EXPERTS];
+    uint64_t ptr[MOE_MAX_EXPERTS];  // the expert's A_e (shrink) or B_e (expand)
+    float scale[MOE_MAX_EXPERTS];   // scale_e (expand)
 };
+constexpr int kTilesBytes = (sizeof(LoraTiles) + 15) / 16 * 16;
 
 // rows of expert e inside the window: [max(off[e], row_offset), min(off[e+1], row_end)).
 // Every thread of the block first computes the tile counts of its experts
-// (all loads issued together), then warp 0 scans them.
+// (all loads issued together) and caches their table pointer and scale (so
+// the tile loops read no table from global memory), then warp 0 scans the
+// counts.
 __device__ void build_lora_tiles(LoraTiles& s, const int32_t* offsets, int n_experts, uint32_t row_offset,
-                                 uint32_t row_end, const uint64_t* a_table, int row_tile) {
+                                 uint32_t row_end, const uint64_t* a_table, int row_tile,
+                                 const uint64_t* ptr_table, const float* scale_table) {
     for (int e = threadIdx.x; e < n_experts; e += blockDim.x) {
         const int lo = max(offsets[e], static_cast<int>(row_offset));
         const int hi = min(offsets[e + 1], static_cast<int>(row_end));
         s.lo[e] = lo;
+        s.hi[e] = hi;
+        s.ptr[e] = ptr_table[e];
+        s.scale[e] = scale_table ? scale_table[e] : 0.0f;
         s.tstart[e] = (hi > lo && a_table[e] != 0) ? (hi - lo + row_tile - 1) / row_tile : 0;  // counts for now
     }
     __syncthreads();
@@ -83,10 +100,9 @@ __device__ __forceinline__ int lora_tile_expert(const LoraTiles& s, int n_expert
     return lo;
 }
 
-// returns the x row of sorted row r, or -1 when the row folds nothing
-__device__ __forceinline__ int lora_row_source(int r, const int32_t* sorted_ids, const int32_t* row_adapter, int P,
-                                               int top_k, uint32_t x_gather, int32_t* err) {
-    const int p = sorted_ids[r];
+// the x row of sorted row r holding pair p, or -1 when the row folds nothing
+__device__ __forceinline__ int lora_source_of_pair(int r, int p, const int32_t* row_adapter, int P, int top_k,
+                                                   uint32_t x_gather, int32_t* err) {
     if (p == P) return -1;
     if (p < 0 || p > P) {
         set_err(err, MOE_DEV_ERR_PAIR_ID);
@@ -112,12 +128,19 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 
 // xa = bf16(xrow . A_e^T) for the rows of 64-row tiles: a contraction of
 // k_in (768 in the workloads) into max_rank sums, run as warp-level
-// tensor-core products (bf16 in, f32 accumulation). Warp task (m, n) covers
-// 16 rows x 8 ranks over the whole contraction: its x fragments come straight
-// from global memory (rows that fold nothing, or lie past the span, read as
-// zeros), its A_e fragments from shared memory (staged by cp.async when the
-// block's expert changes). Each sum is rounded once to bf16.
-__global__ void __launch_bounds__(32 * kShrinkWarps, 3)
+// tensor-core products (bf16 in, f32 accumulation, ldmatrix fragments).
+// The contraction streams through a ring of kShrinkStages shared-memory
+// stages of 128 columns each, filled by cp.async: a stage holds the tile's 64
+// x rows and the expert's 8 * ceil(max_rank / 8) A_e rows for those columns
+// (rows that fold nothing, rows past the span and columns past k_in arrive as
+// zeros). Every thread copies pieces of one x row, so a block keeps three
+// stages (about 65 KB at rank 16) in flight while its warps multiply the
+// fourth: the work is a read of x at HBM speed, not a chain of dependent
+// loads. The ring runs across the block's tiles, so the next tile's first
+// stages load while the current one finishes. Warp task (m, n) covers 16 rows
+// x 8 ranks; each sum is rounded once to bf16 when the tile's last stage is
+// done.
+__global__ void __launch_bounds__(32 * kShrinkWarps, 2)
 lora_shrink_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ offsets,
                    const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ row_adapter,
                    const uint64_t* __restrict__ a_table, __nv_bfloat16* __restrict__ xa, int n_experts, int max_rank,
@@ -126,241 +149,393 @@ lora_shrink_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restric
     pdl_wait();
     extern __shared__ __align__(16) uint8_t smem[];
     LoraTiles& s = *reinterpret_cast<LoraTiles*>(smem);
-    __shared__ int s_src[kShrinkTile];
-    const uint32_t* sA = reinterpret_cast<const uint32_t*>(smem + ((sizeof(LoraTiles) + 15) / 16) * 16);
-    build_lora_tiles(s, offsets, n_experts, row_offset, row_end, a_table, kShrinkTile);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* s_ok = smem + kTilesBytes;  // [stage][row]: the row folds
+    __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem + kTilesBytes + kShrinkStages * kShrinkRows);
+    const int nb = (max_rank + 7) / 8;                            // 8-rank blocks
+    const int stage_elems = (kShrinkRows + 8 * nb) * kShrinkPitch;  // x rows, then A_e rows
+    build_lora_tiles(s, offsets, n_experts, row_offset, row_end, a_table, kShrinkRows, a_table, nullptr);
+    const int kch = (k_in + kShrinkK - 1) / kShrinkK;  // stages per tile
+    const int my_tiles = s.n_tiles > static_cast<int>(blockIdx.x)
+                             ? (s.n_tiles - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x
+                             : 0;
+    const int items = my_tiles * kch;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int kw = k_in / 2;                 // bf16 pairs per row
-    const int ksteps = (k_in + 15) / 16;     // a last step past k_in reads zeros
-    const int nblocks = (max_rank + 7) / 8;  // 8-rank blocks
-    int cur_e = -1;
-    for (int tile = blockIdx.x; tile < s.n_tiles; tile += gridDim.x) {
+    const int xr = tid >> 2;  // the x row this thread copies (four threads per row)
+    int src = -1, src_tl = -1;
+    const __nv_bfloat16* zero_src = x;  // a valid address for the zero-filling copies
+    // pair id at this thread's row of a local tile (-1 past the span): loaded one
+    // tile ahead, so that starting a tile waits on no global load
+    auto row_pair = [&](int tl) -> int {
+        const int tile = static_cast<int>(blockIdx.x) + tl * static_cast<int>(gridDim.x);
+        if (tile >= s.n_tiles) return -1;
         const int e = lora_tile_expert(s, n_experts, tile);
-        const int r0 = s.lo[e] + (tile - s.tstart[e]) * kShrinkTile;
-        const int hi = min(offsets[e + 1], static_cast<int>(row_end));
-        __syncthreads();  // the previous tile is done with s_src and A_e
-        for (int i = threadIdx.x; i < kShrinkTile; i += blockDim.x)
-            s_src[i] = r0 + i < hi ? lora_row_source(r0 + i, sorted_ids, row_adapter, P, top_k, x_gather, err) : -1;
-        if (e != cur_e) {  // stage A_e [max_rank, k_in] (block-uniform)
-            const uint4* src = reinterpret_cast<const uint4*>(a_table[e]);
-            for (int i = threadIdx.x; i < max_rank * (k_in / 8); i += blockDim.x)
-                cp_async16(reinterpret_cast<uint4*>(const_cast<uint32_t*>(sA)) + i, src + i);
-            cp_async_commit();
-            cp_async_wait_all();
-            cur_e = e;
+        const int r = s.lo[e] + (tile - s.tstart[e]) * kShrinkRows + xr;
+        return r < s.hi[e] ? sorted_ids[r] : -1;
+    };
+    int p_pre = items > 0 ? row_pair(0) : -1;
+
+    auto issue = [&](int item) {
+        const int tl = item / kch, kc = item - tl * kch;
+        const int tile = static_cast<int>(blockIdx.x) + tl * static_cast<int>(gridDim.x);
+        const int e = lora_tile_expert(s, n_experts, tile);
+        const int r0 = s.lo[e] + (tile - s.tstart[e]) * kShrinkRows;
+        if (tl != src_tl) {
+            src_tl = tl;
+            src = r0 + xr < s.hi[e] ? lora_source_of_pair(r0 + xr, p_pre, row_adapter, P, top_k, x_gather, err) : -1;
+            if (tl + 1 < my_tiles) p_pre = row_pair(tl + 1);
         }
-        __syncthreads();
-        for (int task = warp; task < 4 * nblocks; task += kShrinkWarps) {
-            const int mb = task & 3, nb = task >> 2;
-            const int rl = 16 * mb + g, rh = rl + 8;  // this lane's two tile rows
-            const int sl = s_src[rl], sh = s_src[rh];
-            if (__all_sync(0xffffffffu, sl < 0 && sh < 0)) continue;  // no row of the block folds
-            const uint32_t* xl = reinterpret_cast<const uint32_t*>(x + static_cast<size_t>(sl < 0 ? 0 : sl) * k_in);
-            const uint32_t* xh = reinterpret_cast<const uint32_t*>(x + static_cast<size_t>(sh < 0 ? 0 : sh) * k_in);
-            const int j = 8 * nb + g;  // this lane's rank (the MMA's n index)
-            const uint32_t* ar = sA + static_cast<size_t>(j < max_rank ? j : 0) * kw;
-            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 4
-            for (int ks = 0; ks < ksteps; ++ks) {
-                const int p0 = 8 * ks + t, p1 = p0 + 4;  // pair indices of k = 16 ks + 2t and + 8
-                uint32_t a[4], b[2];
-                a[0] = (sl >= 0 && p0 < kw) ? __ldg(xl + p0) : 0u;
-                a[1] = (sh >= 0 && p0 < kw) ? __ldg(xh + p0) : 0u;
-                a[2] = (sl >= 0 && p1 < kw) ? __ldg(xl + p1) : 0u;
-                a[3] = (sh >= 0 && p1 < kw) ? __ldg(xh + p1) : 0u;
-                b[0] = (j < max_rank && p0 < kw) ? ar[p0] : 0u;
-                b[1] = (j < max_rank && p1 < kw) ? ar[p1] : 0u;
-                mma_bf16_16816(d, a, b);
-            }
-            // d: (row rl; ranks 8 nb + 2t, + 1) and (row rh; same ranks)
-            const int jr = 8 * nb + 2 * t;
+        const int stage = item % kShrinkStages;
+        __nv_bfloat16* sb = stg + stage * stage_elems;
+        const int k0 = kc * kShrinkK;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int rr = h ? rh : rl;
-                if ((h ? sh : sl) < 0) continue;
-                __nv_bfloat16* dst = xa + static_cast<size_t>(r0 + rr - row_offset) * max_rank + jr;
-                if (jr < max_rank) dst[0] = __float2bfloat16_rn(d[2 * h]);
-                if (jr + 1 < max_rank) dst[1] = __float2bfloat16_rn(d[2 * h + 1]);
+        for (int q = 0; q < 4; ++q) {
+            const int p = (tid & 3) + 4 * q, k = k0 + 8 * p;
+            const bool full = src >= 0 && k < k_in;
+            cp_async16_zfill(sb + xr * kShrinkPitch + 8 * p,
+                             full ? x + static_cast<size_t>(src) * k_in + k : zero_src, full);
+        }
+        const __nv_bfloat16* A = reinterpret_cast<const __nv_bfloat16*>(s.ptr[e]);
+        for (int i = tid; i < 8 * nb * (kShrinkK / 8); i += blockDim.x) {
+            const int j = i / (kShrinkK / 8), p = i - j * (kShrinkK / 8), k = k0 + 8 * p;
+            const bool full = j < max_rank && k < k_in;
+            cp_async16_zfill(sb + (kShrinkRows + j) * kShrinkPitch + 8 * p,
+                             full ? A + static_cast<size_t>(j) * k_in + k : zero_src, full);
+        }
+        if ((tid & 3) == 0) s_ok[stage * kShrinkRows + xr] = src >= 0;
+    };
+
+    float acc[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.0f;
+    const int ntasks = 4 * nb;  // (16-row block, 8-rank block) pairs, at most 32: four per warp
+    // ldmatrix row addresses of this lane inside a stage (bytes): x rows for
+    // the four 8x8 pieces of a 16x16 A fragment, A_e rows for the two of B
+    const uint32_t a_lane = ((lane & 7) + 8 * ((lane >> 3) & 1)) * kShrinkPitch * 2 + 16 * (lane >> 4);
+    const uint32_t b_lane = (kShrinkRows + (lane & 7)) * kShrinkPitch * 2 + 16 * ((lane >> 3) & 1);
+
+    for (int i = 0; i < kShrinkStages - 1; ++i) {
+        if (i < items) issue(i);
+        cp_async_commit();
+    }
+    for (int it = 0; it < items; ++it) {
+        cp_async_wait_group<kShrinkStages - 2>();  // this thread's copies of item `it` landed
+        __syncthreads();                          // everyone's; and item it - 1 is consumed
+        if (it + kShrinkStages - 1 < items) issue(it + kShrinkStages - 1);
+        cp_async_commit();
+        const int tl = it / kch, kc = it - tl * kch, stage = it % kShrinkStages;
+        const uint32_t sbase = smem_u32(stg + stage * stage_elems);
+        const int ksteps = (min(kShrinkK, k_in - kc * kShrinkK) + 15) / 16;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int task = warp + kShrinkWarps * q;
+            if (task >= ntasks) break;  // warp-uniform
+            const int mb = task & 3, nbk = task >> 2;
+            const uint32_t aa = sbase + a_lane + 16 * mb * kShrinkPitch * 2;
+            const uint32_t ba = sbase + b_lane + 8 * nbk * kShrinkPitch * 2;
+            for (int ks = 0; ks < ksteps; ++ks) {
+                uint32_t a[4], b[2];
+                ldmatrix_x4(a, aa + 32 * ks);
+                ldmatrix_x2(b, ba + 32 * ks);
+                mma_bf16_16816(acc[q], a, b);
+            }
+        }
+        if (kc == kch - 1) {  // the tile's contraction is complete: round and store
+            const int tile = static_cast<int>(blockIdx.x) + tl * static_cast<int>(gridDim.x);
+            const int e = lora_tile_expert(s, n_experts, tile);
+            const int r0 = s.lo[e] + (tile - s.tstart[e]) * kShrinkRows;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int task = warp + kShrinkWarps * q;
+                if (task >= ntasks) break;
+                const int mb = task & 3, nbk = task >> 2;
+                const int jr = 8 * nbk + 2 * t;  // d: rows 16 mb + g (d0, d1), + 8 (d2, d3); ranks jr, jr + 1
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row = 16 * mb + g + 8 * h;
+                    if (!s_ok[stage * kShrinkRows + row]) continue;
+                    __nv_bfloat16* dst = xa + static_cast<size_t>(r0 + row - static_cast<int>(row_offset)) * max_rank + jr;
+                    if (jr < max_rank) dst[0] = __float2bfloat16_rn(acc[q][2 * h]);
+                    if (jr + 1 < max_rank) dst[1] = __float2bfloat16_rn(acc[q][2 * h + 1]);
+                }
+                acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.0f;
             }
         }
     }
 }
 
-// Two fused multiply-adds on a pair of f32 values in one instruction:
-// d.x = fma(a.x, b.x, c.x), d.y = fma(a.y, b.y, c.y), each rounded once.
-__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+// dynamic shared memory of the shrink for a rank
+inline size_t lora_shrink_smem(int max_rank) {
+    const int nb = (max_rank + 7) / 8;
+    return kTilesBytes + kShrinkStages * kShrinkRows +
+           static_cast<size_t>(kShrinkStages) * (kShrinkRows + 8 * nb) * kShrinkPitch * 2;
+}
+
+// Two f32 operations on a pair of f32 values in one instruction, each
+// rounded to nearest on its own: (a.x op b.x, a.y op b.y).
+__device__ __forceinline__ unsigned long long f32x2_mul(unsigned long long a, unsigned long long b) {
     unsigned long long d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
-__device__ __forceinline__ unsigned long long f32x2_pack(float lo, float hi) {
-    return (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+__device__ __forceinline__ unsigned long long f32x2_add(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// a bf16 pair (low half first) as an f32 pair, exactly
+__device__ __forceinline__ unsigned long long bf16x2_to_f32x2(uint32_t v) {
+    return (static_cast<unsigned long long>(v & 0xffff0000u) << 32) | static_cast<unsigned long long>(v << 16);
+}
+// an f32 pair rounded to a bf16 pair (round to nearest even, low half first)
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-// Packed storage of N consecutive bf16 values (N = 4, 2 or 1): one load or
-// store moves a thread's columns of a row.
-template <int N> struct BfPack;
-template <> struct BfPack<4> {
-    using V = uint2;
-    static __device__ __forceinline__ float get(const V& v, int i) {
-        const uint32_t w = (i < 2) ? v.x : v.y;
-        return __uint_as_float((i & 1) ? (w & 0xffff0000u) : (w << 16));
-    }
-    static __device__ __forceinline__ void set(V& v, int i, __nv_bfloat16 b) {
-        const uint32_t u = __bfloat16_as_ushort(b);
-        uint32_t& w = (i < 2) ? v.x : v.y;
-        w = (i & 1) ? ((w & 0x0000ffffu) | (u << 16)) : ((w & 0xffff0000u) | u);
-    }
-};
-template <> struct BfPack<2> {
-    using V = uint32_t;
-    static __device__ __forceinline__ float get(const V& v, int i) {
-        return __uint_as_float(i ? (v & 0xffff0000u) : (v << 16));
-    }
-    static __device__ __forceinline__ void set(V& v, int i, __nv_bfloat16 b) {
-        const uint32_t u = __bfloat16_as_ushort(b);
-        v = i ? ((v & 0x0000ffffu) | (u << 16)) : ((v & 0xffff0000u) | u);
-    }
-};
-template <> struct BfPack<1> {
-    using V = unsigned short;
-    static __device__ __forceinline__ float get(const V& v, int) { return __uint_as_float(static_cast<uint32_t>(v) << 16); }
-    static __device__ __forceinline__ void set(V& v, int, __nv_bfloat16 b) { v = __bfloat16_as_ushort(b); }
+// Position of one work unit of the expand in the block's range: chunk c,
+// tile (of the window's tile list) and its expert e. Units run tile first
+// within a chunk, so stepping to the next unit moves the expert forward by
+// at most a few entries of the tile list instead of searching it.
+struct ExCursor {
+    int c, tile, e;
 };
 
-// RCAP: rank capacity of this instantiation (16, 32 or 64: one to four
-// k16 steps). A block takes one work tile: 64 rows of an expert's span
-// (inside the window) times a chunk of 512 output columns. It copies the
-// tile's base values into shared memory with cp.async (64 KB in flight at
-// once) while it stages the rows' xa (bf16, as stored) and which rows fold.
-// The rank-RCAP product delta = xa . B_e^T is a K = RCAP contraction: warp w
-// computes it for all 64 rows and columns [64 w, 64 w + 64) of the chunk
-// with warp-level tensor-core products (16 rows x 8 columns each, f32
-// accumulation; a tcgen05 tile of 128 rows would need TMEM and shared-memory
-// descriptors for a contraction of 16, and the kernel is bound by the base
-// values' read and write anyway), then rounds each sum to bf16, folds it into
-// the staged base value and stores the pair of columns to global memory.
+// RCAP: rank capacity of this instantiation (16, 32 or 64: one to four k16
+// steps). The block takes a contiguous range of work units (a 32-row tile of
+// an expert's span inside the window x 256 output columns; units ordered
+// column chunk first, so consecutive units mostly share the expert and its
+// B_e columns) and streams them through a ring of kExStages shared-memory
+// stages filled by cp.async, three units ahead of the one it folds:
+//   issue   the unit's base rows that fold (16-byte pieces, or 8-byte ones
+//           when n_out % 8 != 0), the tile's xa rows, and the B_e columns of
+//           the unit when they differ from the previous unit's (a ring of
+//           kExStages B buffers, one per change, so that a buffer is refilled
+//           only after every unit that reads it is done);
+//   compute the rank-RCAP product delta = xa . B_e^T with warp-level
+//           tensor-core products (warp w: columns [32 w, 32 w + 32), both
+//           16-row blocks), round each sum to bf16 and fold it into the
+//           staged base value (f32 multiply, f32 add, bf16; two columns per
+//           instruction) in place;
+//   store   the folded rows back with full-width 16-byte stores.
+// No step waits on a global load of its own: the expert's B_e address and
+// scale come from the tile list in shared memory, and the pair ids that
+// decide which rows fold are loaded one unit ahead. The fold runs straight
+// through all eight 16 x 8 blocks of the warp (rows past the tile and
+// columns past n_out compute stale values that are never stored), so that
+// their shared-memory round trips overlap. The stage rows are 512 bytes with
+// their 16-byte pieces XOR-swizzled by the row, so that the fragment-ordered
+// reads of the compute step hit 32 banks.
 template <int RCAP>
-__global__ void __launch_bounds__(kExpandThreads, RCAP <= 16 ? 3 : 2)
+__global__ void __launch_bounds__(kExThreads, RCAP <= 16 ? 2 : 1)
 lora_expand_fold_kernel(const __nv_bfloat16* __restrict__ xa, const int32_t* __restrict__ offsets,
                         const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ row_adapter,
                         const uint64_t* __restrict__ b_table, const float* __restrict__ scale_table,
                         __nv_bfloat16* __restrict__ base, int n_experts, int n_out, int max_rank, uint32_t row_offset,
-                        uint32_t row_end, int P, int top_k, const uint64_t* __restrict__ a_table) {
+                        uint32_t row_end, int P, int top_k, const uint64_t* __restrict__ a_table, uint32_t vec16) {
     pdl_wait();
-    constexpr int KS = RCAP / 16;  // k16 steps
+    constexpr int KS = RCAP / 16;                   // k16 steps
+    constexpr int kRowBytes = kExCols * 2;          // 512: one staged row
+    constexpr int kStageBytes = kExRows * kRowBytes;
+    constexpr int kBElems = kExCols * RCAP;         // one B buffer
+    constexpr int kXaElems = kExRows * RCAP;        // one stage's xa rows
     extern __shared__ __align__(16) uint8_t lsm[];
     LoraTiles& s = *reinterpret_cast<LoraTiles*>(lsm);
-    size_t off = (sizeof(LoraTiles) + 15) / 16 * 16;
-    int* s_src = reinterpret_cast<int*>(lsm + off);
-    off += kRowTile * sizeof(int);
-    uint32_t* s_xa = reinterpret_cast<uint32_t*>(lsm + off);  // [kRowTile][RCAP / 2] bf16 pairs
-    off += static_cast<size_t>(kRowTile) * RCAP * 2;
-    uint32_t* s_y = reinterpret_cast<uint32_t*>(lsm + off);   // [kRowTile][kColChunk / 2] bf16 pairs
-    build_lora_tiles(s, offsets, n_experts, row_offset, row_end, a_table, kRowTile);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int* s_bbuf = reinterpret_cast<int*>(lsm + kTilesBytes);  // B buffer of each stage
+    uint8_t* sy = lsm + kTilesBytes + 16;
+    __nv_bfloat16* sbuf = reinterpret_cast<__nv_bfloat16*>(sy + kExStages * kStageBytes);
+    __nv_bfloat16* sxa = sbuf + kExStages * kBElems;  // [stage][row][max_rank]
+    build_lora_tiles(s, offsets, n_experts, row_offset, row_end, a_table, kExRows, b_table, scale_table);
+    const int n_chunks = (n_out + kExCols - 1) / kExCols;
+    const int n_tiles = s.n_tiles;
+    const long long U = static_cast<long long>(n_tiles) * n_chunks;
+    const int u0 = static_cast<int>(U * blockIdx.x / gridDim.x);
+    const int n_my = static_cast<int>(U * (blockIdx.x + 1) / gridDim.x) - u0;
+    if (n_my <= 0) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int n_chunks = (n_out + kColChunk - 1) / kColChunk;
-    for (int wt = blockIdx.x; wt < s.n_tiles * n_chunks; wt += gridDim.x) {
-        const int tile = wt / n_chunks, chunk = wt - tile * n_chunks;
-        const int e = lora_tile_expert(s, n_experts, tile);
-        const int r0 = s.lo[e] + (tile - s.tstart[e]) * kRowTile;
-        const int hi = min(offsets[e + 1], static_cast<int>(row_end));
-        const int nrows = min(kRowTile, hi - r0);
-        const int c0 = chunk * kColChunk;
-        const int ncols = min(kColChunk, n_out - c0);  // a multiple of 4
-        __syncthreads();  // the previous tile is done with the shared buffers
-        // 1. the tile's base values: 8-byte copies, every one in flight at once
-        {
-            const int per_row = ncols / 4;
-            for (int i = threadIdx.x; i < nrows * per_row; i += blockDim.x) {
-                const int rr = i / per_row, q = i - rr * per_row;
-                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(s_y + rr * (kColChunk / 2) + 2 * q)),
-                             "l"(base + static_cast<size_t>(r0 + rr) * n_out + c0 + 4 * q)
-                             : "memory");
-            }
-            cp_async_commit();
+    const int rr = tid >> 3, l8 = tid & 7;  // copy role: row rr, pieces l8 + 8 q
+    const bool even_rank = (max_rank & 1) == 0;  // rank pairs start on 4-byte boundaries
+    const bool xa_pairs = even_rank && (reinterpret_cast<uintptr_t>(xa) & 3u) == 0;
+
+    auto advance = [&](ExCursor& q) {
+        if (++q.tile == n_tiles) {
+            q.tile = 0;
+            ++q.c;
+            q.e = 0;
         }
-        // 2. meanwhile: which rows fold and their xa (zero for rows that do not fold,
-        // for rows past the tile and for ranks past max_rank)
-        for (int i = threadIdx.x; i < kRowTile; i += blockDim.x)
-            s_src[i] = i < nrows ? lora_row_source(r0 + i, sorted_ids, row_adapter, P, top_k, 0, nullptr) : -1;
-        __syncthreads();
-        for (int i = threadIdx.x; i < kRowTile * (RCAP / 2); i += blockDim.x) {
-            const int rr = i / (RCAP / 2), jp = i - rr * (RCAP / 2);
-            uint32_t v = 0u;
-            if (s_src[rr] >= 0) {
-                const __nv_bfloat16* src = xa + static_cast<size_t>(r0 + rr - row_offset) * max_rank;
-                const uint32_t lo = 2 * jp < max_rank ? __bfloat16_as_ushort(src[2 * jp]) : 0u;
-                const uint32_t hi2 = 2 * jp + 1 < max_rank ? __bfloat16_as_ushort(src[2 * jp + 1]) : 0u;
-                v = lo | (hi2 << 16);
-            }
-            s_xa[rr * (RCAP / 2) + jp] = v;
+        while (s.tstart[q.e + 1] <= q.tile) ++q.e;  // tstart[n_experts] = n_tiles ends it
+    };
+    ExCursor cur_issue, cur_next, cur_fold;  // units j + kExStages - 1, the one after it, and j
+    cur_issue.c = u0 / n_tiles;
+    cur_issue.tile = u0 - cur_issue.c * n_tiles;
+    cur_issue.e = lora_tile_expert(s, n_experts, cur_issue.tile);
+    cur_fold = cur_issue;
+    cur_next = cur_issue;
+    struct Unit { int e, r0, nrows, c0, ncols; };
+    auto unit = [&](const ExCursor& q) {
+        Unit d;
+        d.e = q.e;
+        d.r0 = s.lo[q.e] + (q.tile - s.tstart[q.e]) * kExRows;
+        d.nrows = min(kExRows, s.hi[q.e] - d.r0);
+        d.c0 = q.c * kExCols;
+        d.ncols = min(kExCols, n_out - d.c0);  // a multiple of 4
+        return d;
+    };
+    // byte offset of 16-byte piece ch of staged row r
+    auto piece = [](int r, int ch) { return r * kRowBytes + ((ch ^ (r & 7)) << 4); };
+    // pair id at this thread's row of a unit, -1 past the tile
+    auto row_pair = [&](const ExCursor& q) -> int {
+        const Unit d = unit(q);
+        return rr < d.nrows ? sorted_ids[d.r0 + rr] : -1;
+    };
+
+    uint32_t okbits = 0;   // bit st: this thread's row of the unit in stage st folds
+    int bkey = -1, bver = -1;
+    int p_pre = row_pair(cur_next);
+    advance(cur_next);
+    auto issue = [&](int j) {  // unit j = cur_issue
+        const Unit d = unit(cur_issue);
+        const int stage = j % kExStages;
+        const int key = d.e * n_chunks + cur_issue.c;
+        if (key != bkey) {  // the unit's B_e columns [c0, c0 + ncols) x max_rank: one contiguous span
+            bkey = key;
+            ++bver;
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(s.ptr[d.e]) + static_cast<size_t>(d.c0) * max_rank * 2;
+            uint8_t* dst = reinterpret_cast<uint8_t*>(sbuf + (bver % kExStages) * kBElems);
+            const int bytes = d.ncols * max_rank * 2;  // a multiple of 8
+            for (int i = tid; i < (bytes >> 4); i += blockDim.x) cp_async16(dst + 16 * i, src + 16 * i);
+            if ((bytes & 15) && tid == 0) cp_async8(dst + (bytes & ~15), src + (bytes & ~15));
         }
-        const float sc = scale_table[e];
-        const __nv_bfloat16* B = reinterpret_cast<const __nv_bfloat16*>(b_table[e]);
-        cp_async_wait_all();
-        __syncthreads();
-        // 3. xa fragments of the four 16-row blocks, held for the whole chunk
-        uint32_t af[4][KS][4];
-#pragma unroll
-        for (int mb = 0; mb < 4; ++mb)
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                const uint32_t* r_lo = s_xa + (16 * mb + g) * (RCAP / 2) + 8 * ks + t;
-                const uint32_t* r_hi = r_lo + 8 * (RCAP / 2);
-                af[mb][ks][0] = r_lo[0];
-                af[mb][ks][1] = r_hi[0];
-                af[mb][ks][2] = r_lo[4];
-                af[mb][ks][3] = r_hi[4];
+        if (tid == 0) s_bbuf[stage] = bver % kExStages;
+        {  // the tile's xa rows, as stored: nrows * max_rank contiguous values
+            __nv_bfloat16* dst = sxa + stage * kXaElems;
+            const __nv_bfloat16* src = xa + static_cast<size_t>(d.r0 - static_cast<int>(row_offset)) * max_rank;
+            const int n = d.nrows * max_rank;
+            if (xa_pairs) {
+                for (int i = tid; i < n / 2; i += blockDim.x) cp_async4(dst + 2 * i, src + 2 * i);
+            } else {
+                for (int i = tid; i < n; i += blockDim.x) dst[i] = src[i];
             }
-        // 4. this warp's columns [64 w, 64 w + 64) of the chunk, 8 at a time; the B_e
-        // fragments of all eight blocks are loaded first (one round trip to L2)
-        uint32_t bfa[8][KS][2];
+        }
+        const int p = p_pre;
+        const bool ok = p >= 0 && p < P && (row_adapter == nullptr || row_adapter[p / top_k] >= 0);
+        okbits = ok ? (okbits | (1u << stage)) : (okbits & ~(1u << stage));
+        if (j + 1 < n_my) {  // the next unit's pair id, used one issue later
+            p_pre = row_pair(cur_next);
+            advance(cur_next);
+        }
+        advance(cur_issue);
+        if (!ok) return;
+        const __nv_bfloat16* grow = base + static_cast<size_t>(d.r0 + rr) * n_out + d.c0;
+        uint8_t* srow = sy + stage * kStageBytes;
+        if (vec16) {
 #pragma unroll
-        for (int nb = 0; nb < 8; ++nb) {
-            const int n = c0 + 64 * warp + 8 * nb + g;  // this lane's column of B (the MMA's n index)
+            for (int q = 0; q < kExCols / 64; ++q) {
+                const int ch = l8 + 8 * q;
+                if (8 * ch < d.ncols) cp_async16(srow + piece(rr, ch), grow + 8 * ch);
+            }
+        } else {
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                // pairs (k = 16 ks + 2t, +1) and (+8, +9) of B_e row n; zero past the chunk or max_rank
-                uint32_t b0 = 0u, b1 = 0u;
-                if (64 * warp + 8 * nb + g < ncols) {
-                    const __nv_bfloat16* brow = B + static_cast<size_t>(n) * max_rank;
-                    const int k0 = 16 * ks + 2 * t, k1 = k0 + 8;
-                    b0 = (k0 < max_rank ? __bfloat16_as_ushort(brow[k0]) : 0u) |
-                         ((k0 + 1 < max_rank ? static_cast<uint32_t>(__bfloat16_as_ushort(brow[k0 + 1])) : 0u) << 16);
-                    b1 = (k1 < max_rank ? __bfloat16_as_ushort(brow[k1]) : 0u) |
-                         ((k1 + 1 < max_rank ? static_cast<uint32_t>(__bfloat16_as_ushort(brow[k1 + 1])) : 0u) << 16);
+            for (int q = 0; q < kExCols / 32; ++q) {
+                const int pc = l8 + 8 * q;  // 8-byte piece
+                if (4 * pc < d.ncols) cp_async8(srow + piece(rr, pc >> 1) + 8 * (pc & 1), grow + 4 * pc);
+            }
+        }
+    };
+    // the bf16 pair (k, k + 1) at element offset i of a shared array; zero past max_rank
+    auto pair_at = [&](const __nv_bfloat16* a, int i, int k) -> uint32_t {
+        if (k >= max_rank) return 0u;
+        if (even_rank) return *reinterpret_cast<const uint32_t*>(a + i);
+        const uint32_t lo = __bfloat16_as_ushort(a[i]);
+        const uint32_t hi = k + 1 < max_rank ? static_cast<uint32_t>(__bfloat16_as_ushort(a[i + 1])) : 0u;
+        return lo | (hi << 16);
+    };
+
+    for (int i = 0; i < kExStages - 1; ++i) {
+        if (i < n_my) issue(i);
+        cp_async_commit();
+    }
+    for (int j = 0; j < n_my; ++j) {
+        const int stage = j % kExStages;
+        cp_async_wait_group<kExStages - 2>();
+        __syncthreads();  // unit j has landed; unit j - 1 is stored
+        if (j + kExStages - 1 < n_my) issue(j + kExStages - 1);
+        cp_async_commit();
+        const Unit d = unit(cur_fold);
+        advance(cur_fold);
+        const int cw = 32 * warp;  // this warp's first column of the unit
+        if (cw < d.ncols) {
+            const float sc = s.scale[d.e];
+            const unsigned long long sc2 =
+                (static_cast<unsigned long long>(__float_as_uint(sc)) << 32) | __float_as_uint(sc);
+            const __nv_bfloat16* bb = sbuf + s_bbuf[stage] * kBElems;
+            const __nv_bfloat16* xs = sxa + stage * kXaElems;
+            // xa fragments of both 16-row blocks (rows past the tile hold stale values
+            // that only reach rows that are not stored)
+            uint32_t af[2][KS][4];
+#pragma unroll
+            for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int rl = 16 * mb + g, k0 = 16 * ks + 2 * t;
+                    af[mb][ks][0] = pair_at(xs, rl * max_rank + k0, k0);
+                    af[mb][ks][1] = pair_at(xs, (rl + 8) * max_rank + k0, k0);
+                    af[mb][ks][2] = pair_at(xs, rl * max_rank + k0 + 8, k0 + 8);
+                    af[mb][ks][3] = pair_at(xs, (rl + 8) * max_rank + k0 + 8, k0 + 8);
                 }
-                bfa[nb][ks][0] = b0;
-                bfa[nb][ks][1] = b1;
+            // B fragments of this warp's four 8-column blocks (columns past n_out read
+            // stale buffer values that only reach columns that are not stored)
+            uint32_t bfr[4][KS][2];
+#pragma unroll
+            for (int nbk = 0; nbk < 4; ++nbk) {
+                const int n = cw + 8 * nbk + g;  // this lane's column of B (the MMA's n index)
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int k = 16 * ks + 2 * t + 8 * h;
+                        bfr[nbk][ks][h] = pair_at(bb, n * max_rank + k, k);
+                    }
             }
+            uint8_t* srow = sy + stage * kStageBytes;
+#pragma unroll
+            for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+                for (int nbk = 0; nbk < 4; ++nbk) {
+                    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) mma_bf16_16816(acc, af[mb][ks], bfr[nbk][ks]);
+                    // acc: rows 16 mb + g (acc0, acc1) and + 8 (acc2, acc3); columns cw + 8 nbk + 2t, + 1
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int row = 16 * mb + g + 8 * h;
+                        uint32_t* yp = reinterpret_cast<uint32_t*>(srow + piece(row, (cw >> 3) + nbk) + 4 * t);
+                        const unsigned long long dl = bf16x2_to_f32x2(f32x2_to_bf16x2(acc[2 * h], acc[2 * h + 1]));
+                        const unsigned long long o = f32x2_add(bf16x2_to_f32x2(*yp), f32x2_mul(sc2, dl));
+                        *yp = f32x2_to_bf16x2(__uint_as_float(static_cast<uint32_t>(o)),
+                                              __uint_as_float(static_cast<uint32_t>(o >> 32)));
+                    }
+                }
         }
+        __syncthreads();  // the unit is folded in shared memory
+        if ((okbits >> stage) & 1u) {
+            __nv_bfloat16* grow = base + static_cast<size_t>(d.r0 + rr) * n_out + d.c0;
+            const uint8_t* srow = sy + stage * kStageBytes;
+            if (vec16) {
 #pragma unroll
-        for (int nb = 0; nb < 8; ++nb) {
-            const int cl0 = 64 * warp + 8 * nb;  // first chunk column of the block
-            if (cl0 >= ncols) break;             // warp-uniform
-            const uint32_t (&bf)[KS][2] = bfa[nb];
+                for (int q = 0; q < kExCols / 64; ++q) {
+                    const int ch = l8 + 8 * q;
+                    if (8 * ch < d.ncols)
+                        *reinterpret_cast<uint4*>(grow + 8 * ch) = *reinterpret_cast<const uint4*>(srow + piece(rr, ch));
+                }
+            } else {
 #pragma unroll
-            for (int mb = 0; mb < 4; ++mb) {
-                float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                for (int ks = 0; ks < KS; ++ks) mma_bf16_16816(d, af[mb][ks], bf[ks]);
-                // d: rows 16 mb + g (d0, d1) and 16 mb + g + 8 (d2, d3), columns cl0 + 2t, + 1
-                const int cl = cl0 + 2 * t;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int rr = 16 * mb + g + 8 * h;
-                    if (rr >= nrows || s_src[rr] < 0 || cl >= ncols) continue;
-                    const uint32_t yv = s_y[rr * (kColChunk / 2) + cl / 2];
-                    const float d0 = __bfloat162float(__float2bfloat16_rn(d[2 * h]));      // bf16 delta
-                    const float d1 = __bfloat162float(__float2bfloat16_rn(d[2 * h + 1]));
-                    const float y0 = __uint_as_float(yv << 16), y1 = __uint_as_float(yv & 0xffff0000u);
-                    const uint32_t o0 = __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(y0, __fmul_rn(sc, d0))));
-                    const uint32_t o1 = __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(y1, __fmul_rn(sc, d1))));
-                    *reinterpret_cast<uint32_t*>(base + static_cast<size_t>(r0 + rr) * n_out + c0 + cl) =
-                        o0 | (o1 << 16);
+                for (int q = 0; q < kExCols / 32; ++q) {
+                    const int pc = l8 + 8 * q;
+                    if (4 * pc < d.ncols)
+                        *reinterpret_cast<uint2*>(grow + 4 * pc) =
+                            *reinterpret_cast<const uint2*>(srow + piece(rr, pc >> 1) + 8 * (pc & 1));
                 }
             }
         }
@@ -369,9 +544,9 @@ lora_expand_fold_kernel(const __nv_bfloat16* __restrict__ xa, const int32_t* __r
 
 // dynamic shared memory of an expand instantiation
 template <int RCAP>
-size_t lora_expand_smem() {
-    return (sizeof(LoraTiles) + 15) / 16 * 16 + kRowTile * sizeof(int) + static_cast<size_t>(kRowTile) * RCAP * 2 +
-           static_cast<size_t>(kRowTile) * kColChunk * 2;
+constexpr size_t lora_expand_smem() {
+    return kTilesBytes + 16 + static_cast<size_t>(kExStages) * kExRows * kExCols * 2 +
+           static_cast<size_t>(kExStages) * kExCols * RCAP * 2 + static_cast<size_t>(kExStages) * kExRows * RCAP * 2;
 }
 
 // ---- decode gather fold: slot-major rows --------------------------------------
@@ -526,32 +701,42 @@ extern "C" int moe_lora_grouped_down(const MoeExpertRoute* route, const void* x,
     const int sms = moe::sm_count();
     if (sms <= 0) return moe::fail(MOE_ERR_CUDA, "%s: cannot query the SM count", who);
     const int window = static_cast<int>(row_end - row_offset);
-    const int n_chunks = (static_cast<int>(route->n_out) + moe::kColChunk - 1) / moe::kColChunk;
-    const long max_tiles = static_cast<long>((window + moe::kRowTile - 1) / moe::kRowTile + route->n_experts) * n_chunks;
-    const int grid = static_cast<int>(max_tiles < sms * 4 ? max_tiles : sms * 4);
-    const int s_tiles = (window + moe::kShrinkTile - 1) / moe::kShrinkTile + static_cast<int>(route->n_experts);
-    const int s_grid = s_tiles < sms * 4 ? s_tiles : sms * 4;
-
-    const size_t shrink_smem = ((sizeof(moe::LoraTiles) + 15) / 16) * 16 +
-                               static_cast<size_t>(route->max_rank) * route->k_in * 2;
-    MOE_REQUIRE(shrink_smem <= 200 * 1024, "%s: max_rank * k_in too large for shared memory", who);
+    // resident blocks per SM of each kernel, from its registers and shared memory (queried once per device)
     static int configured_for = -1;
+    static int occ_shrink = 0, occ_expand[3] = {0, 0, 0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_for != dev) {
-        int rc = moe::set_smem_limit(reinterpret_cast<const void*>(moe::lora_shrink_kernel), 200 * 1024);
-        if (rc == MOE_OK)
-            rc = moe::set_smem_limit(reinterpret_cast<const void*>(moe::lora_expand_fold_kernel<16>),
-                                     static_cast<int>(moe::lora_expand_smem<16>()));
-        if (rc == MOE_OK)
-            rc = moe::set_smem_limit(reinterpret_cast<const void*>(moe::lora_expand_fold_kernel<32>),
-                                     static_cast<int>(moe::lora_expand_smem<32>()));
-        if (rc == MOE_OK)
-            rc = moe::set_smem_limit(reinterpret_cast<const void*>(moe::lora_expand_fold_kernel<64>),
-                                     static_cast<int>(moe::lora_expand_smem<64>()));
+        const void* ek[3] = {reinterpret_cast<const void*>(moe::lora_expand_fold_kernel<16>),
+                             reinterpret_cast<const void*>(moe::lora_expand_fold_kernel<32>),
+                             reinterpret_cast<const void*>(moe::lora_expand_fold_kernel<64>)};
+        const size_t es[3] = {moe::lora_expand_smem<16>(), moe::lora_expand_smem<32>(), moe::lora_expand_smem<64>()};
+        const size_t ss = moe::lora_shrink_smem(MOE_MAX_LORA_RANK);
+        int rc = moe::set_smem_limit(reinterpret_cast<const void*>(moe::lora_shrink_kernel), static_cast<int>(ss));
+        for (int i = 0; i < 3 && rc == MOE_OK; ++i) rc = moe::set_smem_limit(ek[i], static_cast<int>(es[i]));
         if (rc != MOE_OK) return rc;
+        // the shrink at rank 16, the common case; larger ranks take more shared memory per block
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_shrink, moe::lora_shrink_kernel, 32 * moe::kShrinkWarps,
+                                                          moe::lora_shrink_smem(16)) != cudaSuccess)
+            return moe::fail(MOE_ERR_CUDA, "%s: occupancy query failed", who);
+        for (int i = 0; i < 3; ++i)
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_expand[i], ek[i], moe::kExThreads, es[i]) !=
+                cudaSuccess)
+                return moe::fail(MOE_ERR_CUDA, "%s: occupancy query failed", who);
         configured_for = dev;
     }
+    const int rslot = route->max_rank <= 16 ? 0 : (route->max_rank <= 32 ? 1 : 2);
+    // upper bounds of the tile counts the kernels find on the device: every expert
+    // adds at most one partial tile to the window's full ones
+    const long s_tiles = (window + moe::kShrinkRows - 1) / moe::kShrinkRows + static_cast<long>(route->n_experts);
+    const size_t shrink_smem = moe::lora_shrink_smem(static_cast<int>(route->max_rank));
+    const long s_cap = static_cast<long>(route->max_rank <= 16 ? (occ_shrink > 0 ? occ_shrink : 1) : 1) * sms;
+    const int s_grid = static_cast<int>(s_tiles < s_cap ? s_tiles : s_cap);
+    const int n_chunks = (static_cast<int>(route->n_out) + moe::kExCols - 1) / moe::kExCols;
+    const long units = ((window + moe::kExRows - 1) / moe::kExRows + static_cast<long>(route->n_experts)) * n_chunks;
+    const long e_cap = static_cast<long>(occ_expand[rslot] > 0 ? occ_expand[rslot] : 1) * sms;
+    const int grid = static_cast<int>(units < e_cap ? units : e_cap);
+    const uint32_t vec16 = (route->n_out % 8 == 0 && moe::aligned16(base_out)) ? 1u : 0u;
     moe::launch_pdl(moe::lora_shrink_kernel, s_grid, 32 * moe::kShrinkWarps, shrink_smem, st,
         static_cast<const __nv_bfloat16*>(x), expert_offsets, sorted_token_ids, row_adapter, route->a_table,
         static_cast<__nv_bfloat16*>(xa), route->n_experts, route->max_rank, route->k_in, x_gather, row_offset,
@@ -562,17 +747,17 @@ extern "C" int moe_lora_grouped_down(const MoeExpertRoute* route, const void* x,
     const auto* xa_p = static_cast<const __nv_bfloat16*>(xa);
     auto* base_p = static_cast<__nv_bfloat16*>(base_out);
     if (route->max_rank <= 16)
-        moe::launch_pdl(moe::lora_expand_fold_kernel<16>, grid, moe::kExpandThreads, moe::lora_expand_smem<16>(), st,
+        moe::launch_pdl(moe::lora_expand_fold_kernel<16>, grid, moe::kExThreads, moe::lora_expand_smem<16>(), st,
             xa_p, expert_offsets, sorted_token_ids, row_adapter, route->b_table, route->scale_table, base_p,
-            route->n_experts, route->n_out, route->max_rank, row_offset, row_end, P, top_k, route->a_table);
+            route->n_experts, route->n_out, route->max_rank, row_offset, row_end, P, top_k, route->a_table, vec16);
     else if (route->max_rank <= 32)
-        moe::launch_pdl(moe::lora_expand_fold_kernel<32>, grid, moe::kExpandThreads, moe::lora_expand_smem<32>(), st,
+        moe::launch_pdl(moe::lora_expand_fold_kernel<32>, grid, moe::kExThreads, moe::lora_expand_smem<32>(), st,
             xa_p, expert_offsets, sorted_token_ids, row_adapter, route->b_table, route->scale_table, base_p,
-            route->n_experts, route->n_out, route->max_rank, row_offset, row_end, P, top_k, route->a_table);
+            route->n_experts, route->n_out, route->max_rank, row_offset, row_end, P, top_k, route->a_table, vec16);
     else
-        moe::launch_pdl(moe::lora_expand_fold_kernel<64>, grid, moe::kExpandThreads, moe::lora_expand_smem<64>(), st,
+        moe::launch_pdl(moe::lora_expand_fold_kernel<64>, grid, moe::kExThreads, moe::lora_expand_smem<64>(), st,
             xa_p, expert_offsets, sorted_token_ids, row_adapter, route->b_table, route->scale_table, base_p,
-            route->n_experts, route->n_out, route->max_rank, row_offset, row_end, P, top_k, route->a_table);
+            route->n_experts, route->n_out, route->max_rank, row_offset, row_end, P, top_k, route->a_table, vec16);
     moe::count_launch();
     return moe::check_launch("moe_lora_grouped_down (expand)");
 }
