@@ -98,6 +98,7 @@ int dispatch(int wfmt, int act, int ntok, const Maps& m, const GemmParams& p, cu
         if (ntok == 0) return launch_pair_form(MODE, m, p, st, who);
         return launch_decode_form(MODE, ntok, m, p, st, who);
     }
+    if (wfmt == MOE_W_NVFP4 && ntok == 0) return launch_tspair_form(MODE, act, m, p, st, who);
     return launch_ts_form(MODE, wfmt, act, ntok, m, p, st, who);
 }
 
@@ -171,6 +172,8 @@ int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Map
             // 256-wide boxes for down)
             const uint64_t kg = static_cast<uint64_t>(E) * (K / 16);
             int rc;
+            // The TS pair form takes 128 rows per CTA: 64 gate and 64 up rows, or
+            // 128 down rows (q0 / q1: the same tensors in those boxes).
             if (N == 2 * n_out) {
                 const uint64_t I = n_out;
                 rc = make_tmap_3d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, I,
@@ -178,10 +181,20 @@ int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Map
                 if (rc == MOE_OK)
                     rc = make_tmap_3d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, I, 2, kg, I, 2 * I, hc,
                                           2, 8);
+                if (rc == MOE_OK)
+                    rc = make_tmap_3d_raw(&m.q0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, I,
+                                          2 * static_cast<uint64_t>(E), K / 2, I * (K / 2), 64, hc / 2, 2);
+                if (rc == MOE_OK)
+                    rc = make_tmap_3d_raw(&m.q1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, I, 2, kg, I, 2 * I,
+                                          hc / 2, 2, 8);
             } else {
                 rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(E) * N,
                                       K / 2, 64, dc);
                 if (rc == MOE_OK) rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kg, N, dc, 8);
+                if (rc == MOE_OK)
+                    rc = make_tmap_2d_raw(&m.q0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(E) * N,
+                                          K / 2, 64, hc);
+                if (rc == MOE_OK) rc = make_tmap_2d_raw(&m.q1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kg, N, hc, 8);
             }
             m.r2 = m.r1;
             m.w = m.r0;

@@ -1,8 +1,9 @@
 // Shared pieces of the grouped expert GEMMs (steps a3 and a4): launch
-// parameters, the shared-memory tail, the device-built tile list, the
-// decode form's stream-K partition, and epilogue helpers. The three kernel
-// forms live in gemm_pair.cu (bf16 prefill, CTA pairs), gemm_decode.cu (bf16
-// decode) and gemm_ts.cu (GPTQ / NVFP4 / FP8 weights dequantised into TMEM);
+// parameters, the shared-memory tail, the device-built tile lists, the
+// decode form's stream-K partition, and epilogue helpers. The kernel forms
+// live in gemm_pair.cu (bf16 prefill, CTA pairs), gemm_decode.cu (bf16
+// decode), gemm_ts.cu (GPTQ / NVFP4 / FP8 weights dequantised into TMEM) and
+// gemm_tspair.cu (NVFP4 prefill, dequantised into the TMEM of CTA pairs);
 // gemm.cu holds the entry points.
 #pragma once
 
@@ -48,8 +49,8 @@ struct SmemTail {
     uint64_t empty[MAX_STAGES];
     uint64_t raw_full[MAX_RSTAGES];
     uint64_t raw_empty[MAX_RSTAGES];
-    uint64_t afull[4];   // TMEM weight stages (TS form)
-    uint64_t aempty[4];
+    uint64_t afull[8];   // TMEM weight stages (TS forms)
+    uint64_t aempty[8];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t mma_done;
@@ -375,8 +376,119 @@ __device__ __forceinline__ void load_swapped(uint32_t taddr, int c, float (&fa)[
     }
 }
 
+// ---- tile list of the CTA-pair forms ------------------------------------------
+//
+// Row tiles of a pair form are cut from each expert's valid rows (its span
+// minus the padding suffix) into ceil(rows / (16 MAXU)) tiles of nearly equal
+// height, in steps of 16 rows; the MMA's N is the tile's height, so padding
+// rows are not computed.
+
+// Shared-memory tail of the pair kernel: the generic one plus each expert's
+// count of valid (non-padding) rows.
+struct PairTail : SmemTail {
+    int vcnt[MOE_MAX_EXPERTS];
+};
+
+struct PairTile {
+    int e, m0, n0;
+    int rows;  // valid rows of the tile (the epilogue stores these)
+    int n16;   // the MMA's N: rows rounded up to 16
+};
+
+// row tiles of an expert with v valid rows: units of 16 rows, at most MAXU units a tile
+template <int MAXU>
+__device__ __forceinline__ int pair_row_tiles(int v) {
+    const int u = (v + 15) / 16;
+    return (u + MAXU - 1) / MAXU;
+}
+
+// The pair kernel's tile list: like build_tile_list, with each expert's row
+// tiles cut from its valid rows. Padding rows are a suffix of the span shorter
+// than block_size, so one thread per expert finds the first one by a binary
+// search over the span's last block_size - 1 rows.
+template <int MAXU>
+__device__ __forceinline__ int build_pair_tiles(PairTail& s, const GemmParams& p, int out_cols) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int E = p.E;
+    for (int i = tid; i <= E; i += blockDim.x) s.off[i] = p.offsets[i];
+    if (tid == 0) {
+        s.abort_flag = 0;
+        s.nt = (p.n_out + out_cols - 1) / out_cols;
+    }
+    __syncthreads();
+    int bad = 0;
+    for (int i = tid; i < E; i += blockDim.x) bad |= (s.off[i + 1] < s.off[i]);
+    if (tid == 0) bad |= (s.off[0] < 0) | (s.off[E] > p.max_padded);
+    bad = __syncthreads_or(bad);
+    for (int e = tid; e < E; e += blockDim.x) {
+        int v = 0;
+        if (!bad) {
+            const int r0 = s.off[e], r1 = s.off[e + 1];
+            int lo = max(r0, r1 - (p.block_size - 1)), hi = r1;  // rows < lo hold pairs, rows >= hi padding
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (__ldg(p.sorted_ids + mid) == p.P) hi = mid; else lo = mid + 1;
+            }
+            v = lo - r0;
+        }
+        s.vcnt[e] = v;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int per = (E + 31) / 32;
+        int loc = 0;
+        for (int j = 0; j < per; ++j) {
+            const int e = lane * per + j;
+            if (e < E) loc += pair_row_tiles<MAXU>(s.vcnt[e]) * s.nt;
+        }
+        int inc = loc;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, inc, d);
+            if (lane >= d) inc += o;
+        }
+        int run = inc - loc;
+        for (int j = 0; j < per; ++j) {
+            const int e = lane * per + j;
+            if (e < E) {
+                s.tstart[e] = run;
+                run += pair_row_tiles<MAXU>(s.vcnt[e]) * s.nt;
+            }
+        }
+        if (lane == 31) s.n_tiles = bad ? 0 : inc;
+    }
+    return bad;
+}
+
+// Tile `tile` of a pair kernel's list: expert-major, then column tiles,
+// row tiles fastest. Row tile i of mt covers units [U i / mt, U (i + 1) / mt)
+// of the expert's U = ceil(valid / 16) units of 16 rows.
+template <int MAXU>
+__device__ __forceinline__ PairTile pair_tile(const PairTail& s, int E, int tile, int out_cols) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s.tstart[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    PairTile t;
+    t.e = lo;
+    const int v = s.vcnt[lo];
+    const int U = (v + 15) / 16;
+    const int mt = (U + MAXU - 1) / MAXU;
+    const int local = tile - s.tstart[lo];
+    const int n_tile = local / mt;
+    const int m_tile = local - n_tile * mt;
+    const int u0 = U * m_tile / mt, u1 = U * (m_tile + 1) / mt;
+    t.m0 = s.off[lo] + 16 * u0;
+    t.rows = min(v, 16 * u1) - 16 * u0;
+    t.n16 = 16 * (u1 - u0);
+    t.n0 = n_tile * out_cols;
+    return t;
+}
+
 struct Maps {
     CUtensorMap x, w, w5, r0, r1, r2;  // w5: gate/up rows interleaved by 8 (bf16 pair form)
+    CUtensorMap q0, q1;                // NVFP4 codes / scales in 128-row boxes per CTA (TS pair form)
 };
 
 // Launchers of the three forms (each in its own translation unit). mode is
@@ -386,6 +498,7 @@ int launch_pair_form(int mode, const Maps& m, const GemmParams& p, cudaStream_t 
 int launch_decode_form(int mode, int ntok, const Maps& m, const GemmParams& p, cudaStream_t st, const char* who);
 int launch_ts_form(int mode, int wfmt, int act, int ntok, const Maps& m, const GemmParams& p, cudaStream_t st,
                    const char* who);
+int launch_tspair_form(int mode, int act, const Maps& m, const GemmParams& p, cudaStream_t st, const char* who);
 
 }  // namespace gemm
 }  // namespace moe

@@ -30,106 +30,6 @@ namespace {
 // columns, interleaved in groups of 8 by one 5-D TMA copy, so the SiLU pairs
 // TMEM lane j with lane j + 8.
 
-// Shared-memory tail of the pair kernel: the generic one plus each expert's
-// count of valid (non-padding) rows.
-struct PairTail : SmemTail {
-    int vcnt[MOE_MAX_EXPERTS];
-};
-
-struct PairTile {
-    int e, m0, n0;
-    int rows;  // valid rows of the tile (the epilogue stores these)
-    int n16;   // the MMA's N: rows rounded up to 16
-};
-
-// row tiles of an expert with v valid rows: units of 16 rows, at most 16 units a tile
-__device__ __forceinline__ int pair_row_tiles(int v) {
-    const int u = (v + 15) / 16;
-    return (u + 15) / 16;
-}
-
-// The pair kernel's tile list: like build_tile_list, with each expert's row
-// tiles cut from its valid rows. Padding rows are a suffix of the span shorter
-// than block_size, so one thread per expert finds the first one by a binary
-// search over the span's last block_size - 1 rows.
-__device__ __forceinline__ int build_pair_tiles(PairTail& s, const GemmParams& p, int out_cols) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int E = p.E;
-    for (int i = tid; i <= E; i += blockDim.x) s.off[i] = p.offsets[i];
-    if (tid == 0) {
-        s.abort_flag = 0;
-        s.nt = (p.n_out + out_cols - 1) / out_cols;
-    }
-    __syncthreads();
-    int bad = 0;
-    for (int i = tid; i < E; i += blockDim.x) bad |= (s.off[i + 1] < s.off[i]);
-    if (tid == 0) bad |= (s.off[0] < 0) | (s.off[E] > p.max_padded);
-    bad = __syncthreads_or(bad);
-    for (int e = tid; e < E; e += blockDim.x) {
-        int v = 0;
-        if (!bad) {
-            const int r0 = s.off[e], r1 = s.off[e + 1];
-            int lo = max(r0, r1 - (p.block_size - 1)), hi = r1;  // rows < lo hold pairs, rows >= hi padding
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (__ldg(p.sorted_ids + mid) == p.P) hi = mid; else lo = mid + 1;
-            }
-            v = lo - r0;
-        }
-        s.vcnt[e] = v;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        const int per = (E + 31) / 32;
-        int loc = 0;
-        for (int j = 0; j < per; ++j) {
-            const int e = lane * per + j;
-            if (e < E) loc += pair_row_tiles(s.vcnt[e]) * s.nt;
-        }
-        int inc = loc;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, inc, d);
-            if (lane >= d) inc += o;
-        }
-        int run = inc - loc;
-        for (int j = 0; j < per; ++j) {
-            const int e = lane * per + j;
-            if (e < E) {
-                s.tstart[e] = run;
-                run += pair_row_tiles(s.vcnt[e]) * s.nt;
-            }
-        }
-        if (lane == 31) s.n_tiles = bad ? 0 : inc;
-    }
-    return bad;
-}
-
-// Tile `tile` of the pair kernel's list: expert-major, then column tiles,
-// row tiles fastest. Row tile i of mt covers units [U i / mt, U (i + 1) / mt)
-// of the expert's U = ceil(valid / 16) units of 16 rows.
-__device__ __forceinline__ PairTile pair_tile(const PairTail& s, int E, int tile, int out_cols) {
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s.tstart[mid] <= tile) lo = mid; else hi = mid - 1;
-    }
-    PairTile t;
-    t.e = lo;
-    const int v = s.vcnt[lo];
-    const int U = (v + 15) / 16;
-    const int mt = (U + 15) / 16;
-    const int local = tile - s.tstart[lo];
-    const int n_tile = local / mt;
-    const int m_tile = local - n_tile * mt;
-    const int u0 = U * m_tile / mt, u1 = U * (m_tile + 1) / mt;
-    t.m0 = s.off[lo] + 16 * u0;
-    t.rows = min(v, 16 * u1) - 16 * u0;
-    t.n16 = 16 * (u1 - u0);
-    t.n0 = n_tile * out_cols;
-    return t;
-}
-
 // Epilogue of a pair tile for the calling warp: TMEM lanes 32q..32q+31 of
 // this CTA are weight rows, columns 0..N-1 the tile's rows (tokens).
 //   gate/up: lane j holds, for output column n0 + 64 rank + 16 q + 8 (j >> 4) +
@@ -221,7 +121,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     const int E = p.E;
 
-    const int bad = build_pair_tiles(s, p, OUT_COLS);  // identical in both CTAs
+    const int bad = build_pair_tiles<16>(s, p, OUT_COLS);  // identical in both CTAs
     if (tid == 0) {
         if (bad && rank == 0) set_err(p.err, MOE_DEV_ERR_OFFSETS);
         for (int i = 0; i < PAIR_STAGES; ++i) {
@@ -263,7 +163,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
             long issued = 0;
             bool ok = true;
             for (int tile = pair; tile < n_tiles && ok; tile += npairs) {
-                const PairTile t = pair_tile(s, E, tile, OUT_COLS);
+                const PairTile t = pair_tile<16>(s, E, tile, OUT_COLS);
                 int c0, c1;
                 half_bases<MODE>(p, t.n0, c0, c1);
                 const int wrow = t.e * p.n_w + (rank == 0 ? c0 : c1);
@@ -298,7 +198,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
             int local = 0;
             bool ok = true;
             for (int tile = pair; tile < n_tiles && ok; tile += npairs) {
-                const PairTile t = pair_tile(s, E, tile, OUT_COLS);
+                const PairTile t = pair_tile<16>(s, E, tile, OUT_COLS);
                 const int acc = local & 1;
                 const uint32_t aph = (local >> 1) & 1;
                 ++local;
@@ -329,7 +229,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
         __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(sStg) + (warp - 2) * (32 * 32);
         int local = 0;
         for (int tile = pair; tile < n_tiles; tile += npairs) {
-            const PairTile t = pair_tile(s, E, tile, OUT_COLS);
+            const PairTile t = pair_tile<16>(s, E, tile, OUT_COLS);
             const int acc = local & 1;
             const uint32_t aph = (local >> 1) & 1;
             ++local;
