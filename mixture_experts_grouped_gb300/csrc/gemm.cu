@@ -16,18 +16,22 @@
 //     (gate/up: 128 gate + 128 up rows of the same output columns, so the
 //     epilogue fuses silu(gate) * up; down: 256 output columns) against a
 //     block of activation rows, K in steps of 64 elements.
-//   * Three kernels, chosen on the host from the average rows per touched
+//   * Four kernel forms, chosen on the host from the average rows per touched
 //     expert and the weight format:
 //       - bf16 prefill (>= 128 rows per expert): grouped_gemm_pair_kernel, a
-//         cluster of two CTAs issuing tcgen05.mma.cta_group::2 M=256 (128
-//         activation rows per CTA) x N=256 (half the weight tile per CTA);
+//         cluster of two CTAs issuing tcgen05.mma.cta_group::2 with M=256
+//         weight rows (128 per CTA) and N = up to 256 activation rows of one
+//         expert (N/2 per CTA);
 //       - bf16 decode: grouped_gemm_decode_kernel, operands swapped: each
 //         weight half is an M=128 operand and NTOK tokens (16..128, one align
 //         block) the N operand;
-//       - GPTQ / NVFP4 / FP8, any size: grouped_gemm_ts_kernel, weights
-//         dequantised by eight or sixteen warps into TMEM and used as the
-//         M=128 A operand, NTOK tokens (128 for prefill) the N operand from
-//         shared memory.
+//       - NVFP4 / FP8 prefill: grouped_gemm_tspair_kernel, CTA pairs again,
+//         each CTA dequantising its 128 weight rows into its own TMEM as the
+//         A operand of M=256 MMAs, N = up to 192 activation rows;
+//       - GPTQ (any size) and NVFP4 / FP8 decode: grouped_gemm_ts_kernel,
+//         weights dequantised by eight or sixteen warps into TMEM and used as
+//         the M=128 A operand, NTOK tokens (128 for GPTQ prefill) the N operand
+//         from shared memory.
 //   * Roles: TMA producer warps feed multi-stage rings; MMA issues go to
 //     double-buffered TMEM accumulators where TMEM allows; four epilogue warps
 //     drain them (tcgen05.ld -> activation -> global).
@@ -98,7 +102,8 @@ int dispatch(int wfmt, int act, int ntok, const Maps& m, const GemmParams& p, cu
         if (ntok == 0) return launch_pair_form(MODE, m, p, st, who);
         return launch_decode_form(MODE, ntok, m, p, st, who);
     }
-    if (wfmt == MOE_W_NVFP4 && ntok == 0) return launch_tspair_form(MODE, act, m, p, st, who);
+    if ((wfmt == MOE_W_NVFP4 || wfmt == MOE_W_FP8_E4M3) && ntok == 0)
+        return launch_tspair_form(MODE, wfmt, act, m, p, st, who);
     return launch_ts_form(MODE, wfmt, act, ntok, m, p, st, who);
 }
 
@@ -206,15 +211,23 @@ int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Map
             // one copy per 64-deep raw stage: a 3-D map over the gate and up
             // halves for gate/up, a 256-row box for down
             int rc;
+            // (q0: the same codes in the TS pair form's 128-row boxes per CTA)
             if (N == 2 * n_out) {
                 const uint64_t I = n_out;
                 rc = make_tmap_3d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, I, 2 * static_cast<uint64_t>(E),
                                       K, I * K, 64, hc, 2);
+                if (rc == MOE_OK)
+                    rc = make_tmap_3d_raw(&m.q0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, I,
+                                          2 * static_cast<uint64_t>(E), K, I * K, 64, hc / 2, 2);
             } else {
                 rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(E) * N, K,
                                       64, dc);
+                if (rc == MOE_OK)
+                    rc = make_tmap_2d_raw(&m.q0, w->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(E) * N,
+                                          K, 64, hc);
             }
             m.r1 = m.r2 = m.r0;
+            m.q1 = m.q0;
             m.w = m.r0;
             return rc;
         }

@@ -1,6 +1,6 @@
-// Step a3 / a4, quantised-weight prefill form on CTA pairs: NVFP4 weights
-// dequantised into TMEM by warps of both CTAs, tcgen05.mma.cta_group::2 with
-// A from TMEM.
+// Step a3 / a4, quantised-weight prefill form on CTA pairs: NVFP4 or FP8
+// weights dequantised into TMEM by warps of both CTAs, tcgen05.mma.cta_group::2
+// with A from TMEM.
 #include "gemm_common.cuh"
 #include "gemm_dequant.cuh"
 
@@ -40,38 +40,59 @@ constexpr int TSP_A_COL = 2 * TSP_ACC;
 constexpr int TSP_ASTAGES = 4;  // weight stages in TMEM
 constexpr int TSP_MAXU = TSP_ACC / 16;  // 16-row units per row tile
 constexpr int TSP_X_STAGE = 128 * BK * 2;  // this CTA's token rows of a k block (a 128-row box)
-constexpr int TSP_RAW = 9216;   // raw stage: two k blocks of 128 rows: codes [128][64 B], scales [8][128]
 constexpr int TSP_NSET = 2;     // sets of four converting warps, taking the raw stages in turn
 constexpr int TSP_STG = NUM_EPI_WARPS * 32 * 32 * 2;
 constexpr int TSP_TAIL_BYTES = (static_cast<int>(sizeof(PairTail)) + 127) / 128 * 128;
 constexpr int TSP_AVAIL = SMEM_LIMIT - 1024 - TSP_STG - TSP_TAIL_BYTES;
 constexpr int TSP_XSTAGES = 8;
-constexpr int TSP_RFIT = (TSP_AVAIL - TSP_XSTAGES * TSP_X_STAGE) / TSP_RAW;
-constexpr int TSP_RSTAGES = (TSP_RFIT < MAX_RSTAGES ? TSP_RFIT : MAX_RSTAGES) / TSP_NSET * TSP_NSET;
-constexpr int TSP_SMEM = 1024 + TSP_XSTAGES * TSP_X_STAGE + TSP_RSTAGES * TSP_RAW + TSP_STG + TSP_TAIL_BYTES;
 // warps: 0 activation TMA, 1 TMEM + MMA issuer, 2..5 epilogue, 6 raw TMA, 8..15 converting
 constexpr int TSP_EPI0 = 2, TSP_RAWW = 6, TSP_DQ0 = 8;
 constexpr int TSP_THREADS = 32 * (TSP_DQ0 + 4 * TSP_NSET);
-static_assert(TSP_RSTAGES >= 2 * TSP_NSET, "not enough shared memory for the raw ring");
-static_assert(TSP_XSTAGES <= MAX_STAGES && TSP_RSTAGES <= MAX_RSTAGES, "ring sizes");
-static_assert(TSP_SMEM <= SMEM_LIMIT, "TS pair kernel shared memory over the limit");
+static_assert(TSP_XSTAGES <= MAX_STAGES, "ring size");
 static_assert(TSP_A_COL + TSP_ASTAGES * 32 <= 512, "weight stages exceed TMEM");
 static_assert(TSP_ASTAGES <= 8, "weight stage barriers");
 
+// The raw-weight ring of a format. A raw stage holds this CTA's 128 rows of
+//   NVFP4: two k blocks, codes [128 rows][64 bytes] then scales [8 groups][128 rows];
+//   FP8:   one k block, codes [128 rows][64 bytes] (row scales go to the epilogue).
+template <int WFMT>
+struct TspRaw {
+    static constexpr int KPR = WFMT == MOE_W_FP8_E4M3 ? 1 : 2;  // k blocks per raw stage
+    static constexpr int BYTES = WFMT == MOE_W_FP8_E4M3 ? 8192 : 9216;
+    static constexpr int FIT = (TSP_AVAIL - TSP_XSTAGES * TSP_X_STAGE) / BYTES;
+    static constexpr int STAGES = (FIT < MAX_RSTAGES ? FIT : MAX_RSTAGES) / TSP_NSET * TSP_NSET;
+    static constexpr int SMEM = 1024 + TSP_XSTAGES * TSP_X_STAGE + STAGES * BYTES + TSP_STG + TSP_TAIL_BYTES;
+    static_assert(STAGES >= 2 * TSP_NSET && STAGES <= MAX_RSTAGES, "raw ring size");
+    static_assert(SMEM <= SMEM_LIMIT, "TS pair kernel shared memory over the limit");
+};
+
 // Epilogue of a TS pair tile for the calling warp (lanes 32q..32q+31 of this
-// CTA's TMEM are its weight rows, columns the tile's tokens): the NVFP4
-// per-tensor scale (gate or up for gate/up) applied to every sum, then as the
-// bf16 pair form: gate/up lanes j and j ^ 8 pair for SiLU(gate) * up; every
-// 32-token step goes through the warp's staging area and leaves as 16-byte
-// stores of 8 columns.
-template <int MODE, int ACT>
+// CTA's TMEM are its weight rows, columns the tile's tokens): the lane's
+// weight scale (NVFP4: the per-tensor scale of the gate or up half; FP8: the
+// row's scale) applied to every sum, then as the bf16 pair form: gate/up
+// lanes j and j ^ 8 pair for SiLU(gate) * up; every 32-token step goes
+// through the warp's staging area and leaves as 16-byte stores of 8 columns.
+template <int MODE, int WFMT, int ACT>
 __device__ __forceinline__ void tspair_epilogue(const GemmParams& p, uint32_t ta, typename Act<ACT>::T* stg,
                                                 const PairTile& t, int rank, int q, int lane) {
     using A = Act<ACT>;
     using T = typename A::T;
     T* out = static_cast<T*>(p.out);
     const int nvalid = t.rows;
-    const float sc = (MODE == MODE_GATE_UP && (lane & 8)) ? __ldg(p.scale2 + p.E + t.e) : __ldg(p.scale2 + t.e);
+    float sc;
+    if (WFMT == MOE_W_FP8_E4M3) {
+        // this lane's weight row: gate/up column oc (gate row oc, up row n_out + oc), down row n
+        const float* rs = p.row_scale + static_cast<size_t>(t.e) * p.n_w;
+        if (MODE == MODE_GATE_UP) {
+            const int oc = t.n0 + 64 * rank + 16 * q + 8 * (lane >> 4) + (lane & 7);
+            sc = oc < p.n_out ? __ldg(rs + ((lane & 8) ? p.n_out + oc : oc)) : 0.0f;
+        } else {
+            const int n = t.n0 + 128 * rank + 32 * q + lane;
+            sc = n < p.n_out ? __ldg(rs + n) : 0.0f;
+        }
+    } else {
+        sc = (MODE == MODE_GATE_UP && (lane & 8)) ? __ldg(p.scale2 + p.E + t.e) : __ldg(p.scale2 + t.e);
+    }
     uint32_t u[32], nx[32];
     tmem_ld32(ta, nx);
 #pragma unroll 1
@@ -117,17 +138,18 @@ __device__ __forceinline__ void tspair_epilogue(const GemmParams& p, uint32_t ta
     }
 }
 
-template <int MODE, int ACT>
+template <int MODE, int WFMT, int ACT>
 __global__ void __launch_bounds__(TSP_THREADS, 1)
 grouped_gemm_tspair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmQ0,
                            const __grid_constant__ CUtensorMap tmQ1, const GemmParams p) {
     pdl_wait();
     constexpr int OUT_COLS = MODE == MODE_GATE_UP ? 128 : 256;
+    using R = TspRaw<WFMT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024_shared(smem_raw);
     uint8_t* sX = smem;
     uint8_t* sR = sX + TSP_XSTAGES * TSP_X_STAGE;
-    uint8_t* sStg = sR + TSP_RSTAGES * TSP_RAW;
+    uint8_t* sStg = sR + R::STAGES * R::BYTES;
     PairTail& s = *reinterpret_cast<PairTail*>(sStg + TSP_STG);
     const WaitCtx wc{&s.abort_flag, p.err, p.wait_ns};
 
@@ -137,7 +159,7 @@ grouped_gemm_tspair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     const int E = p.E;
     const int KB = (p.K + BK - 1) / BK;  // 64-deep k blocks
-    const int KR = (KB + 1) / 2;         // raw stages (two k blocks each) per tile
+    const int KR = (KB + R::KPR - 1) / R::KPR;  // raw stages per tile
 
     const int bad = build_pair_tiles<TSP_MAXU>(s, p, OUT_COLS);  // identical in both CTAs
     if (tid == 0) {
@@ -146,7 +168,7 @@ grouped_gemm_tspair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
             mbar_init(&s.full[i], 1);
             mbar_init(&s.empty[i], 1);
         }
-        for (int i = 0; i < TSP_RSTAGES; ++i) {
+        for (int i = 0; i < R::STAGES; ++i) {
             mbar_init(&s.raw_full[i], 1);
             mbar_init(&s.raw_empty[i], 4);  // the four warps of the set that converts the stage
         }
@@ -257,7 +279,7 @@ grouped_gemm_tspair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
             if (!mbar_wait(&s.tfull[acc], aph, wc)) break;
             tc_fence_after();
             const uint32_t ta = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TSP_ACC;
-            tspair_epilogue<MODE, ACT>(p, ta, stg, t, static_cast<int>(rank), q, lane);
+            tspair_epilogue<MODE, WFMT, ACT>(p, ta, stg, t, static_cast<int>(rank), q, lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -266,7 +288,7 @@ grouped_gemm_tspair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
             }
         }
     } else if (warp == TSP_RAWW) {
-        // ---------------- raw NVFP4 TMA (each CTA its own 128 rows) ----------------
+        // ---------------- raw-weight TMA (each CTA its own 128 rows) ----------------
         if (lane == 0) {
             uint32_t rstage = 0, rphase = 0;
             long issued = 0;
@@ -276,10 +298,16 @@ grouped_gemm_tspair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
                 for (int kr = 0; kr < KR; ++kr) {
                     if (!mbar_wait(&s.raw_empty[rstage], rphase ^ 1, wc)) { ok = false; break; }
                     uint64_t* bar = &s.raw_full[rstage];
-                    uint8_t* rw = sR + rstage * TSP_RAW;
-                    mbar_arrive_expect_tx(bar, TSP_RAW);
-                    const int sg = t.e * (p.K / 16) + kr * 8;  // the stage's first 16-deep scale group
-                    if (MODE == MODE_GATE_UP) {
+                    uint8_t* rw = sR + rstage * R::BYTES;
+                    mbar_arrive_expect_tx(bar, R::BYTES);
+                    const int sg = t.e * (p.K / 16) + kr * 8;  // NVFP4: the stage's first 16-deep scale group
+                    if (WFMT == MOE_W_FP8_E4M3) {
+                        // codes [gate | up][64 rows][64 bytes] or [128 rows][64 bytes]
+                        if (MODE == MODE_GATE_UP)
+                            tma_load_3d(rw, &tmQ0, kr * BK, t.n0 + 64 * static_cast<int>(rank), 2 * t.e, bar);
+                        else
+                            tma_load_2d(rw, &tmQ0, kr * BK, t.e * p.n_w + t.n0 + 128 * static_cast<int>(rank), bar);
+                    } else if (MODE == MODE_GATE_UP) {
                         // codes [gate | up][64 rows][64 bytes], scales [8 groups][gate | up][64 rows]
                         const int r0 = t.n0 + 64 * static_cast<int>(rank);
                         tma_load_3d(rw, &tmQ0, kr * BK, r0, 2 * t.e, bar);
@@ -291,12 +319,12 @@ grouped_gemm_tspair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
                         tma_load_2d(rw + 8192, &tmQ1, r0, sg, bar);
                     }
                     ++issued;
-                    if (++rstage == TSP_RSTAGES) { rstage = 0; rphase ^= 1; }
+                    if (++rstage == R::STAGES) { rstage = 0; rphase ^= 1; }
                 }
             }
-            const long first = issued > TSP_RSTAGES ? issued - TSP_RSTAGES : 0;
+            const long first = issued > R::STAGES ? issued - R::STAGES : 0;
             for (long j = first; j < issued; ++j)
-                mbar_drain(&s.raw_full[j % TSP_RSTAGES], static_cast<uint32_t>((j / TSP_RSTAGES) & 1),
+                mbar_drain(&s.raw_full[j % R::STAGES], static_cast<uint32_t>((j / R::STAGES) & 1),
                            kWaitLimitNs / 8);
         }
     } else if (warp >= TSP_DQ0) {
@@ -311,14 +339,25 @@ grouped_gemm_tspair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
                                             : 32 * sp + lane;
         const uint32_t trow = tmem_base + (static_cast<uint32_t>(sp * 32) << 16) + TSP_A_COL;
         auto convert = [&](const uint8_t* raw, int kp, uint32_t (&o)[32]) {
-            uint32_t w8[8], sc[4];
-            const uint4* row = reinterpret_cast<const uint4*>(raw + ri * 64 + kp * 32);
-            const uint4 v0 = row[0], v1 = row[1];
-            w8[0] = v0.x; w8[1] = v0.y; w8[2] = v0.z; w8[3] = v0.w;
-            w8[4] = v1.x; w8[5] = v1.y; w8[6] = v1.z; w8[7] = v1.w;
+            if (WFMT == MOE_W_FP8_E4M3) {
+                uint32_t w16[16];
+                const uint4* row = reinterpret_cast<const uint4*>(raw + ri * 64);
 #pragma unroll
-            for (int g4 = 0; g4 < 4; ++g4) sc[g4] = raw[8192 + (4 * kp + g4) * 128 + ri];
-            nvfp4_row<ACT>(w8, sc, o);
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 v = row[i];
+                    w16[4 * i] = v.x; w16[4 * i + 1] = v.y; w16[4 * i + 2] = v.z; w16[4 * i + 3] = v.w;
+                }
+                fp8_row<ACT>(w16, o);
+            } else {
+                uint32_t w8[8], sc[4];
+                const uint4* row = reinterpret_cast<const uint4*>(raw + ri * 64 + kp * 32);
+                const uint4 v0 = row[0], v1 = row[1];
+                w8[0] = v0.x; w8[1] = v0.y; w8[2] = v0.z; w8[3] = v0.w;
+                w8[4] = v1.x; w8[5] = v1.y; w8[6] = v1.z; w8[7] = v1.w;
+#pragma unroll
+                for (int g4 = 0; g4 < 4; ++g4) sc[g4] = raw[8192 + (4 * kp + g4) * 128 + ri];
+                nvfp4_row<ACT>(w8, sc, o);
+            }
         };
         int rpos = set, rpar = 0;  // ring position and phase of this set's next raw stage
         int jmod = 0;              // (the CTA's next raw stage) mod TSP_NSET
@@ -329,10 +368,10 @@ grouped_gemm_tspair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
                 const bool mine = jmod == set;
                 if (++jmod == TSP_NSET) jmod = 0;
                 if (!mine) continue;
-                const int g = g0 + 2 * kr;
-                const bool two = 2 * kr + 1 < KB;  // the stage's second k block is used
+                const int g = g0 + R::KPR * kr;
+                const bool two = R::KPR == 2 && 2 * kr + 1 < KB;  // the stage's second k block is used
                 if (!mbar_wait(&s.raw_full[rpos], static_cast<uint32_t>(rpar), wc)) { ok = false; break; }
-                const uint8_t* raw = sR + rpos * TSP_RAW;
+                const uint8_t* raw = sR + rpos * R::BYTES;
                 // each k block is published as soon as it is in TMEM, before the next one
                 // is converted: the MMA of k block g waits on it, and the conversion of
                 // g + TSP_ASTAGES waits on that MMA
@@ -374,8 +413,8 @@ grouped_gemm_tspair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s.raw_empty[rpos]);
                 rpos += TSP_NSET;
-                if (rpos >= TSP_RSTAGES) {
-                    rpos -= TSP_RSTAGES;
+                if (rpos >= R::STAGES) {
+                    rpos -= R::STAGES;
                     rpar ^= 1;
                 }
                 if (two) publish(g + 1);
@@ -392,9 +431,10 @@ grouped_gemm_tspair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid
     if (warp == 1) tmem_dealloc_pair(tmem_base, 512);
 }
 
-template <int MODE, int ACT>
+template <int MODE, int WFMT, int ACT>
 int launch_tspair(const Maps& m, const GemmParams& p, cudaStream_t st, const char* who) {
-    auto kernel = grouped_gemm_tspair_kernel<MODE, ACT>;
+    using R = TspRaw<WFMT>;
+    auto kernel = grouped_gemm_tspair_kernel<MODE, WFMT, ACT>;
     static int configured_for = -1;
     static int max_pairs = 0;
     int dev = 0;
@@ -406,12 +446,12 @@ int launch_tspair(const Maps& m, const GemmParams& p, cudaStream_t st, const cha
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(TSP_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = TSP_SMEM;
+    cfg.dynamicSmemBytes = R::SMEM;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (configured_for != dev) {
-        int rc = set_smem_limit(reinterpret_cast<const void*>(kernel), TSP_SMEM);
+        int rc = set_smem_limit(reinterpret_cast<const void*>(kernel), R::SMEM);
         if (rc != MOE_OK) return rc;
         const int sms = sm_count();
         cfg.gridDim = dim3(sms > 0 ? (sms / 2) * 2 : 2, 1, 1);
@@ -440,12 +480,18 @@ int launch_tspair(const Maps& m, const GemmParams& p, cudaStream_t st, const cha
 
 }  // namespace
 
-int launch_tspair_form(int mode, int act, const Maps& m, const GemmParams& p, cudaStream_t st, const char* who) {
-    if (mode == MODE_GATE_UP)
-        return act == MOE_ACT_F16 ? launch_tspair<MODE_GATE_UP, MOE_ACT_F16>(m, p, st, who)
-                                  : launch_tspair<MODE_GATE_UP, MOE_ACT_BF16>(m, p, st, who);
-    return act == MOE_ACT_F16 ? launch_tspair<MODE_DOWN, MOE_ACT_F16>(m, p, st, who)
-                              : launch_tspair<MODE_DOWN, MOE_ACT_BF16>(m, p, st, who);
+int launch_tspair_form(int mode, int wfmt, int act, const Maps& m, const GemmParams& p, cudaStream_t st,
+                       const char* who) {
+#define MOE_TSP_ACT(MODE, WFMT)                                                                   \
+    return act == MOE_ACT_F16 ? launch_tspair<MODE, WFMT, MOE_ACT_F16>(m, p, st, who)             \
+                              : launch_tspair<MODE, WFMT, MOE_ACT_BF16>(m, p, st, who)
+    if (mode == MODE_GATE_UP) {
+        if (wfmt == MOE_W_FP8_E4M3) MOE_TSP_ACT(MODE_GATE_UP, MOE_W_FP8_E4M3);
+        MOE_TSP_ACT(MODE_GATE_UP, MOE_W_NVFP4);
+    }
+    if (wfmt == MOE_W_FP8_E4M3) MOE_TSP_ACT(MODE_DOWN, MOE_W_FP8_E4M3);
+    MOE_TSP_ACT(MODE_DOWN, MOE_W_NVFP4);
+#undef MOE_TSP_ACT
 }
 
 }  // namespace gemm
