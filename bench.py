@@ -191,16 +191,17 @@ def tensor_peak(pk: dict, clk: dict):
     return (sustained, "sustained") if capped else (burst, "burst")
 
 
-def traffic_for(kernel_key: str):
+def traffic_for(kernel_key: str, workload: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, valid only while the kernel source is the one that was profiled."""
+    summary, valid only for the workload it was captured on and while the
+    kernel source is the one that was profiled."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f).get(kernel_key)
     except (OSError, ValueError):
         return None
-    if not d:
+    if not d or d.get("workload") != workload:
         return None
     src = os.path.join(ROOT, d["source"])
     try:
@@ -451,7 +452,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         "tflops": tflops, "weight_gbs": weight_gbs, "layer_roofline_frac": layer_frac,
         "roofline": dict(roof, kernel="moe_grouped_gate_up (activation gather + tcgen05 grouped GEMM, fused "
                                        "SiLU-mul)",
-                         traffic=traffic_for("grouped_gemm_gate_up"), ms_per_launch=gu_ms,
+                         traffic=traffic_for("grouped_gemm_gate_up", config_dict(cfg, world)["workload"]), ms_per_launch=gu_ms,
                          flops_per_launch=alg["flops_gate_up"], bytes_per_launch=alg["gate_up_bytes"],
                          intensity_flop_per_byte=intensity),
         "e2e": {"value": e2e_value, "unit": "tokens/s",

@@ -81,3 +81,22 @@ def test_tensor_peak_follows_the_sampled_clocks():
         (1729.1, "sustained")
     assert bench.tensor_peak(pk, {"sm_mhz": 1650.0, "sm_max_mhz": 2070.0, "reasons": []}) == (1729.1, "sustained")
     assert bench.tensor_peak(pk, {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]})[1] == "burst"
+
+
+def test_traffic_figure_only_for_its_workload_and_source(tmp_path, monkeypatch):
+    """roofline.traffic is reported only for the workload the ncu capture was
+    taken on, and only while the profiled kernel source is unchanged."""
+    import hashlib
+    import bench
+    src = tmp_path / "kernel.cu"
+    src.write_text("// kernel\n")
+    h = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    (tmp_path / "profiles").mkdir()
+    entry = {"source": "kernel.cu", "source_sha256_16": h, "workload": "w: T=1", "bytes_per_launch": 1234}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"k": entry}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_for("k", "w: T=1") == 1234
+    assert bench.traffic_for("k", "w: T=2") is None       # another workload
+    assert bench.traffic_for("other", "w: T=1") is None   # another kernel
+    src.write_text("// changed\n")
+    assert bench.traffic_for("k", "w: T=1") is None       # the source changed since the capture
