@@ -102,8 +102,13 @@ int dispatch(int wfmt, int act, int ntok, const Maps& m, const GemmParams& p, cu
         if (ntok == 0) return launch_pair_form(MODE, m, p, st, who);
         return launch_decode_form(MODE, ntok, m, p, st, who);
     }
-    if ((wfmt == MOE_W_NVFP4 || wfmt == MOE_W_FP8_E4M3) && ntok == 0)
-        return launch_tspair_form(MODE, wfmt, act, m, p, st, who);
+    if (ntok == 0) {
+        // quantised prefill on CTA pairs; 256-row tiles once experts average 176
+        // rows or more (beyond 192 a 192-row cap would cut most experts in two)
+        const long touched = p.P < p.E ? p.P : p.E;
+        const int wide = touched > 0 && p.P / touched >= 176;
+        return launch_tspair_form(MODE, wfmt, act, wide, m, p, st, who);
+    }
     return launch_ts_form(MODE, wfmt, act, ntok, m, p, st, who);
 }
 
@@ -147,23 +152,31 @@ int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Map
             // A stage spans one group row, or two for group_size 64.
             const uint64_t kq = static_cast<uint64_t>(E) * (K / 8), kg = static_cast<uint64_t>(E) * (K / G);
             const uint32_t sg = G == 64 ? 2 : 1;
-            int rc;
-            if (N == 2 * n_out) {
-                const uint64_t I = n_out;
-                rc = make_tmap_3d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, I, 2, kq, I * 4, 2 * I * 4, hc, 2,
-                                      16);
-                if (rc == MOE_OK)
-                    rc = make_tmap_3d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, I, 2, kg, I * 2,
-                                          2 * I * 2, hc, 2, sg);
-                if (rc == MOE_OK)
-                    rc = make_tmap_3d_raw(&m.r2, w->zeros, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, I / 8, 2, kg, I / 8 * 4,
-                                          2 * I / 8 * 4, hc / 8, 2, sg);
-            } else {
-                rc = make_tmap_2d_raw(&m.r0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, kq, N, dc, 16);
-                if (rc == MOE_OK)
-                    rc = make_tmap_2d_raw(&m.r1, w->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kg, N, dc, sg);
-                if (rc == MOE_OK)
-                    rc = make_tmap_2d_raw(&m.r2, w->zeros, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, kg, N / 8, dc / 8, sg);
+            int rc = MOE_OK;
+            // (q0 / q1 / q2: the same tensors in the TS pair form's 128-column boxes per
+            // CTA, 64 gate and 64 up columns for gate/up)
+            for (int pass = 0; pass < 2 && rc == MOE_OK; ++pass) {
+                const uint32_t b = pass == 0 ? hc : hc / 2;  // columns per half (gate/up) in the box
+                CUtensorMap* t0 = pass == 0 ? &m.r0 : &m.q0;
+                CUtensorMap* t1 = pass == 0 ? &m.r1 : &m.q1;
+                CUtensorMap* t2 = pass == 0 ? &m.r2 : &m.q2;
+                if (N == 2 * n_out) {
+                    const uint64_t I = n_out;
+                    rc = make_tmap_3d_raw(t0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, I, 2, kq, I * 4, 2 * I * 4, b, 2,
+                                          16);
+                    if (rc == MOE_OK)
+                        rc = make_tmap_3d_raw(t1, w->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, I, 2, kg, I * 2,
+                                              2 * I * 2, b, 2, sg);
+                    if (rc == MOE_OK)
+                        rc = make_tmap_3d_raw(t2, w->zeros, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, I / 8, 2, kg, I / 8 * 4,
+                                              2 * I / 8 * 4, b / 8, 2, sg);
+                } else {
+                    rc = make_tmap_2d_raw(t0, w->w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, kq, N, 2 * b, 16);
+                    if (rc == MOE_OK)
+                        rc = make_tmap_2d_raw(t1, w->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kg, N, 2 * b, sg);
+                    if (rc == MOE_OK)
+                        rc = make_tmap_2d_raw(t2, w->zeros, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, kg, N / 8, 2 * b / 8, sg);
+                }
             }
             m.w = m.r0;
             return rc;
@@ -202,6 +215,7 @@ int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Map
                 if (rc == MOE_OK) rc = make_tmap_2d_raw(&m.q1, w->scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kg, N, hc, 8);
             }
             m.r2 = m.r1;
+            m.q2 = m.q1;
             m.w = m.r0;
             return rc;
         }
@@ -227,7 +241,7 @@ int weight_maps(const MoeWeight* w, int act, int E, int N, int K, int n_out, Map
                                           K, 64, hc);
             }
             m.r1 = m.r2 = m.r0;
-            m.q1 = m.q0;
+            m.q1 = m.q2 = m.q0;
             m.w = m.r0;
             return rc;
         }

@@ -3,7 +3,7 @@
 // decode form's stream-K partition, and epilogue helpers. The kernel forms
 // live in gemm_pair.cu (bf16 prefill, CTA pairs), gemm_decode.cu (bf16
 // decode), gemm_ts.cu (GPTQ / NVFP4 / FP8 weights dequantised into TMEM) and
-// gemm_tspair.cu (NVFP4 / FP8 prefill, dequantised into the TMEM of CTA pairs);
+// gemm_tspair.cu (quantised prefill, dequantised into the TMEM of CTA pairs);
 // gemm.cu holds the entry points.
 #pragma once
 
@@ -488,7 +488,7 @@ __device__ __forceinline__ PairTile pair_tile(const PairTail& s, int E, int tile
 
 struct Maps {
     CUtensorMap x, w, w5, r0, r1, r2;  // w5: gate/up rows interleaved by 8 (bf16 pair form)
-    CUtensorMap q0, q1;                // NVFP4 / FP8 codes (and NVFP4 scales) in 128-row boxes per CTA (TS pair form)
+    CUtensorMap q0, q1, q2;            // the quantised tensors in 128-row boxes per CTA (TS pair form)
 };
 
 // Launchers of the three forms (each in its own translation unit). mode is
@@ -498,7 +498,8 @@ int launch_pair_form(int mode, const Maps& m, const GemmParams& p, cudaStream_t 
 int launch_decode_form(int mode, int ntok, const Maps& m, const GemmParams& p, cudaStream_t st, const char* who);
 int launch_ts_form(int mode, int wfmt, int act, int ntok, const Maps& m, const GemmParams& p, cudaStream_t st,
                    const char* who);
-int launch_tspair_form(int mode, int wfmt, int act, const Maps& m, const GemmParams& p, cudaStream_t st,
+// wide: the TS pair form's 256-row tiles (one accumulator buffer) instead of 192-row ones (two)
+int launch_tspair_form(int mode, int wfmt, int act, int wide, const Maps& m, const GemmParams& p, cudaStream_t st,
                        const char* who);
 
 }  // namespace gemm
