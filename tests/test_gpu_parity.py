@@ -297,14 +297,17 @@ def test_router_gemm_then_routing(dev, T, H, E, k, act):
     np.testing.assert_array_equal(w.cpu().numpy().view(np.uint32), np.asarray(ref_w, np.float32).view(np.uint32))
 
 
-@pytest.mark.parametrize("x_gather,adapter,rank", [(0, False, 16), (1, True, 16), (0, True, 40), (1, False, 64)])
-def test_lora_gather_bgmv_matches_oracle(dev, x_gather, adapter, rank):
+@pytest.mark.parametrize("x_gather,adapter,rank,T", [(0, False, 16, 37), (1, True, 16, 37), (0, True, 40, 37),
+                                                    (1, False, 64, 37), (0, True, 16, 600), (1, False, 16, 4200)])
+def test_lora_gather_bgmv_matches_oracle(dev, x_gather, adapter, rank, T):
     """Decode gather fold on slot-major rows: folded rows within tolerance of the
     oracle, every other row of base and xa untouched bit for bit. Expert ids
-    come from real routing; the last adapted expert lies past n_experts."""
+    come from real routing; the last adapted expert lies past n_experts. T=600
+    (2400 rows) takes the expert-grouped kernel over two compaction segments;
+    the others (fewer than 2048 rows, or 16800) the row-per-block kernel."""
     import torch
     from mixture_experts_grouped_gb300 import layer as L, moe
-    cfg = synth.MoeConfig("gather_fold", T=37, H=520, I=264, E=16, k=4, bs=16, router="normal",
+    cfg = synth.MoeConfig("gather_fold", T=T, H=520, I=264, E=16, k=4, bs=16, router="normal",
                           lora_rank=rank, lora_scale=2.0, seed=3)
     inp = synth.make_inputs(cfg)
     lora = dict(inp["lora"])
