@@ -68,8 +68,15 @@ extern "C" {
 #define MOE_MAX_EXPERTS 256 /* [ferrum] moe_align_block_size: compile-time MAX_NUM_EXPERTS */
 /* Split-K area of the grouped GEMM workspaces: fp32 partial sums of up to
  * MOE_SPLITK_CTAS CTAs (128 KB each) followed by 16 bytes of flags per CTA.
- * It must hold zeros before its first use (allocate it zeroed); every call
- * that finishes without a device error leaves it zeroed again. */
+ * A CTA that leaves partial sums marks them with a generation number the
+ * library draws for each call (nonzero, process-wide), and the CTA that adds
+ * them accepts only its own call's number, then clears the flag. So whatever
+ * an earlier call left there (a call that reported a device error, or
+ * uninitialised memory) is not mistaken for a finished piece. One exception:
+ * a replayed CUDA graph repeats the numbers of its capture, so after a replay
+ * that reported a device error, zero the area before the next replay.
+ * Allocating it zeroed is recommended (a stale flag equal to a future call's
+ * number is then impossible rather than unlikely). */
 #define MOE_SPLITK_CTAS 256
 #define MOE_SPLITK_BYTES ((size_t)MOE_SPLITK_CTAS * (131072 + 16))
 #define MOE_MAX_TOPK 16
@@ -153,8 +160,8 @@ uint64_t moe_launch_count(void);
  * kernels launched after this call (process-wide; 0 restores the default of
  * 2 s). A wait that runs out sets MOE_DEV_ERR_TIMEOUT in the call's err_word;
  * the kernel then lets its copies and MMAs in flight land, frees its tensor
- * memory and returns, so the context stays usable. Afterwards the caller
- * zeroes the GEMM workspaces' split-K areas before the next call. This is a
+ * memory and returns, so the context stays usable. (Partial sums it left in
+ * a split-K area are ignored by later calls; see MOE_SPLITK_BYTES.) This is a
  * testing hook (it lets a test make the waits run out on purpose, as the
  * pages' status-return error model asks of every failure); production
  * callers leave the default. Returns the previous limit.
@@ -267,7 +274,7 @@ int moe_align_block_size_noalloc(const int32_t* topk_ids, int32_t P, int32_t E, 
 
 /* Bytes of device workspace moe_grouped_gate_up needs: the gathered copy of
  * the activations in sorted-row order, rounded up to 256 bytes, then the
- * split-K area (MOE_SPLITK_BYTES, zeroed before first use). */
+ * split-K area (MOE_SPLITK_BYTES; allocating it zeroed is recommended). */
 size_t moe_gate_up_workspace_size(int32_t max_padded, int32_t H);
 
 /*
@@ -292,8 +299,7 @@ size_t moe_gate_up_workspace_size(int32_t max_padded, int32_t H);
  *   h_out             device act [max_padded, I] out
  *   err_word          device i32 or NULL
  *   workspace         device, >= moe_gate_up_workspace_size bytes, 128-byte aligned;
- *                     its split-K area zeroed before the first call, and again
- *                     after a call that reported a device error
+ *                     ends with a split-K area (see MOE_SPLITK_BYTES)
  * Requirements: H % 8 == 0, I % 8 == 0, E <= MOE_MAX_EXPERTS, all tensor
  * base addresses 16-byte aligned; GPTQ: group_size a multiple of 64 dividing
  * H and I % 32 == 0; NVFP4: H % 32 == 0 and I % 16 == 0; FP8: H % 16 == 0.
@@ -317,9 +323,9 @@ int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* w_gate_up,
  *   y                 device act [max_padded, H] out (padding rows and rows past
  *                     expert_offsets[E] are not guaranteed to be written)
  *   workspace         device, >= moe_down_workspace_size() bytes, 128-byte
- *                     aligned, zeroed before the first call (and again after a
- *                     call that reported a device error); the decode form cuts
- *                     tiles across CTAs (split-K) and adds partial sums there
+ *                     aligned: a split-K area (see MOE_SPLITK_BYTES); the
+ *                     decode form cuts tiles across CTAs and adds partial sums
+ *                     there
  * Requirements: I % 8 == 0, H % 8 == 0, 16-byte aligned tensors; GPTQ:
  * group_size a multiple of 64 dividing I and H % 32 == 0; NVFP4: I % 32 == 0
  * and H % 16 == 0; FP8: I % 16 == 0.

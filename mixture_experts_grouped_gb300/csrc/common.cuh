@@ -26,6 +26,7 @@ void count_launch(uint64_t n = 1);                     // kernels this library l
 int sm_count();                                        // SMs of the current device
 int set_smem_limit(const void* kernel, int bytes);     // opt in to > 48 KB dynamic smem
 uint64_t wait_limit_ns();                              // pipeline wait limit for the next launches
+uint32_t next_splitk_gen();                            // nonzero split-K generation for the next GEMM call
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -236,14 +237,14 @@ __device__ __forceinline__ void st_release_gpu(int* p, int v) {
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Wait until the global flag *f is nonzero, with the same limit and abort
-// rule as mbar_wait. Every calling thread observes the flag itself (acquire),
-// so each sees the data released before it.
-__device__ __forceinline__ bool flag_wait(const int* f, const WaitCtx& w) {
-    if (ld_acquire_gpu(f)) return true;
+// Wait until the global flag *f holds v, with the same limit and abort rule
+// as mbar_wait. Every calling thread observes the flag itself (acquire), so
+// each sees the data released before it.
+__device__ __forceinline__ bool flag_wait(const int* f, int v, const WaitCtx& w) {
+    if (ld_acquire_gpu(f) == v) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (ld_acquire_gpu(f)) return true;
+        if (ld_acquire_gpu(f) == v) return true;
         if (*w.abort) return false;
         if (globaltimer_ns() - t0 > w.limit_ns) {
             *w.abort = 1;

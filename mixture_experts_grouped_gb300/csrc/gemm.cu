@@ -332,6 +332,7 @@ extern "C" int moe_grouped_gate_up(const void* x, int32_t act, const MoeWeight* 
     p.group_size = w_gate_up->group_size;
     p.err = err_word;
     p.wait_ns = moe::wait_limit_ns();
+    p.sk_gen = static_cast<int>(moe::next_splitk_gen());
     p.block_size = block_size;
     moe::gemm::set_splitk(p, static_cast<uint8_t*>(workspace) + moe::gemm::gather_bytes(max_padded, H));
     return moe::gemm::dispatch<moe::gemm::MODE_GATE_UP>(w_gate_up->format, act, ntok, m, p, st, who);
@@ -376,6 +377,7 @@ extern "C" int moe_grouped_down(const void* h, int32_t act, const MoeWeight* w_d
     p.group_size = w_down->group_size;
     p.err = err_word;
     p.wait_ns = moe::wait_limit_ns();
+    p.sk_gen = static_cast<int>(moe::next_splitk_gen());
     p.block_size = block_size;
     moe::gemm::set_splitk(p, workspace);
     return moe::gemm::dispatch<moe::gemm::MODE_DOWN>(w_down->format, act, ntok, m, p, static_cast<cudaStream_t>(stream), who);

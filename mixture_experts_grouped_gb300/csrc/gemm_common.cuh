@@ -41,7 +41,8 @@ struct GemmParams {
     int pad_free;    // the kernel's tile height is a multiple of block_size: no tile holds padding only
     const float* row_scale;  // FP8: fp32 scale per weight row [E, n_w]
     float* sk_part;  // split-K partial sums: one slice of SK_SLICE_FLOATS per CTA (decode form)
-    int* sk_flag;    // split-K flags: 4 per CTA (one per epilogue warp), zero between launches
+    int* sk_flag;    // split-K flags: 4 per CTA (one per epilogue warp)
+    int sk_gen;      // this call's split-K generation (nonzero): the value a finished piece's flags hold
 };
 
 struct SmemTail {

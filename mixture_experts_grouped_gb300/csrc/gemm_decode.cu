@@ -44,10 +44,13 @@ __device__ __forceinline__ void decode_store_chunk(const float (&a)[16], const f
 
 // Epilogue of one piece of a tile cut by the stream-K partition, for the
 // calling epilogue warp (TMEM lane quarter q). A later piece (to_owner)
-// leaves its fp32 sums in this CTA's slice of the split-K area and raises the
-// CTA's flag for q; the owner waits for the flags of CTAs blockIdx.x + 1 ..
-// last_peer, adds their slices to its own sums and stores the chunk. Returns
-// false when a wait gave up.
+// leaves its fp32 sums in this CTA's slice of the split-K area and sets the
+// CTA's flag for q to the call's generation (p.sk_gen, nonzero, new for every
+// call); the owner waits until the flags of CTAs blockIdx.x + 1 .. last_peer
+// hold that generation, adds their slices to its own sums, stores the chunk
+// and sets the flags back to 0. A flag or slice left by an earlier call (one
+// that gave up, say) is never taken for this call's piece. Returns false
+// when a wait gave up.
 template <int MODE, int NTOK, int NACC>
 __device__ __forceinline__ bool decode_split_epilogue(const GemmParams& p, uint64_t* tfull, uint32_t aph,
                                                    const WaitCtx& wc, bool to_owner, int last_peer,
@@ -75,14 +78,14 @@ __device__ __forceinline__ bool decode_split_epilogue(const GemmParams& p, uint6
         // the slice is complete: publish it to the owner
         __threadfence();
         __syncwarp();
-        if (lane == 0) st_release_gpu(p.sk_flag + blockIdx.x * 4 + q, 1);
+        if (lane == 0) st_release_gpu(p.sk_flag + blockIdx.x * 4 + q, p.sk_gen);
         return true;
     }
     // owner: wait for the peers, fetch the first peer's first chunk while this
     // CTA's own MMAs may still run
     const int first_peer = blockIdx.x + 1;
     for (int pc = first_peer; pc <= last_peer; ++pc)
-        if (!flag_wait(p.sk_flag + pc * 4 + q, wc)) return false;
+        if (!flag_wait(p.sk_flag + pc * 4 + q, p.sk_gen, wc)) return false;
     const float4* peer0 = reinterpret_cast<const float4*>(p.sk_part) + first_peer * SLICE4 + lane_off;
     float4 nx[8];
 #pragma unroll

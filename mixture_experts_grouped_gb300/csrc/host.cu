@@ -51,6 +51,16 @@ void count_launch(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxe
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
+// Split-K generation: a nonzero number per GEMM call, process-wide. The
+// decode form's piece holders store it in their flags and owners accept only
+// their own call's number.
+static std::atomic<uint32_t> g_splitk_gen{0};
+uint32_t next_splitk_gen() {
+    uint32_t v = g_splitk_gen.fetch_add(1, std::memory_order_relaxed) + 1;
+    while (v == 0) v = g_splitk_gen.fetch_add(1, std::memory_order_relaxed) + 1;
+    return v;
+}
+
 int sm_count() {
     static int cached[64] = {0};
     int dev = 0;

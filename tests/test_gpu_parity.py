@@ -256,6 +256,28 @@ def test_split_k_repeatable(dev, name):
     assert not lay.gate_up_ws[-4096:].any() and not lay.down_ws[-4096:].any()
 
 
+@pytest.mark.parametrize("name", ["fine_grained@T1", "splitk_ragged_k"])
+def test_split_k_ignores_stale_areas(dev, name):
+    """Split-K partial sums and flags left in the workspaces by an earlier call
+    (here: every byte of both split-K areas overwritten with 0x7f, so every
+    flag and partial sum is stale) are not taken for the current call's: a
+    piece's flags hold the call's generation and the owner accepts only that.
+    The outputs are bit-identical to a clean run."""
+    import torch
+    cfg = LAYER_CASES[name]
+    inp = synth.make_inputs(cfg)
+    lay, x, logits = gpu_layer(cfg, inp, dev)
+    clean = [t.clone() for t in (lay.h, lay.y, lay.out)]
+    n = lay.down_ws.numel()  # the down workspace is exactly one split-K area; gate/up's ends with one
+    for ws in (lay.gate_up_ws, lay.down_ws):
+        ws[-n:].fill_(0x7f)
+    lay.forward(x, logits)
+    torch.cuda.synchronize()
+    assert int(lay.err.item()) == 0
+    for what, a, b in zip(("h", "y", "out"), clean, (lay.h, lay.y, lay.out)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"{what} differs from the clean run"
+
+
 @pytest.mark.parametrize("name", ["tiny", "fine_grained@T64", "gptq@T16", "nvfp4_lora@T2048", "skewed",
                                   "fp8@T2048"])
 def test_layer_end_to_end(dev, name):
