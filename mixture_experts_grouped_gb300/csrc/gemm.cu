@@ -82,11 +82,12 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sort
 
 // ---- host side -------------------------------------------------------------------
 
-// Activation rows per tile. 0 selects the prefill form (128 rows as the MMA's
-// M operand), used when experts average 128 or more rows. Otherwise the decode
-// form takes one align block per tile (rounded up to a power of two, at least
-// 16): spans are whole blocks and only a span's last block holds padding, so
-// no tile is padding only and the tiles spread evenly over the CTAs.
+// Activation rows per tile. 0 selects the prefill forms (CTA pairs, each
+// expert's valid rows as the MMA's N operand), used when experts average 128
+// or more rows. Otherwise the decode form takes one align block per tile
+// (rounded up to a power of two, at least 16): spans are whole blocks and
+// only a span's last block holds padding, so no tile is padding only and the
+// tiles spread evenly over the CTAs.
 int pick_ntok(long P, int E, int block_size) {
     const long touched = P < E ? P : E;
     const long avg = touched > 0 ? P / touched : 0;

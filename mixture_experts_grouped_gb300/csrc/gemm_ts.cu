@@ -1,5 +1,6 @@
-// Step a3 / a4 for quantised weights (GPTQ int4, NVFP4, FP8): the TS form,
-// weights dequantised by warps of the CTA into TMEM as the MMA's A operand.
+// Step a3 / a4 for quantised weights (GPTQ int4, NVFP4, FP8) at decode sizes:
+// the TS form, weights dequantised by warps of the CTA into TMEM as the MMA's
+// A operand (prefill runs the CTA-pair form of gemm_tspair.cu).
 #include "gemm_common.cuh"
 #include "gemm_dequant.cuh"
 
@@ -45,9 +46,9 @@ struct TsShape {
     // Dequantising warps: NSET sets of eight (one warp per TMEM lane quarter
     // and weight half) take the k blocks in turn, so that one set converts
     // while the other waits on its loads. Two sets measured 11-13% faster on
-    // GPTQ and NVFP4 decode layers and 2% on NVFP4 prefill; one set stays for
-    // FP8 (its conversion is short: two sets measured 4% slower) and GPTQ
-    // prefill (2% slower).
+    // GPTQ and NVFP4 decode layers; one set stays for FP8 (its conversion is
+    // short: two sets measured 4% slower) and for GPTQ at 128 tokens per tile
+    // (2% slower when this form also ran GPTQ prefill).
     static constexpr int NSET =
         WFMT == MOE_W_FP8_E4M3 || (WFMT == MOE_W_GPTQ_INT4 && NTOK >= 128) ? 1 : 2;
     static constexpr int NDQ = NSET * NUM_DQ_WARPS;
@@ -504,7 +505,7 @@ int launch_ts(const Maps& m, const GemmParams& p, cudaStream_t st, const char* w
     return check_launch(who);
 }
 
-// quantised weights: the TS form, NTOK tokens per tile (128 for the prefill form)
+// quantised weights at decode: the TS form, NTOK tokens (one align block) per tile
 template <int MODE, int WFMT, int ACT>
 int ts_by_ntok(int ntok, const Maps& m, const GemmParams& p, cudaStream_t st, const char* who) {
     switch (ntok) {
@@ -519,7 +520,7 @@ int ts_by_ntok(int ntok, const Maps& m, const GemmParams& p, cudaStream_t st, co
 
 int launch_ts_form(int mode, int wfmt, int act, int ntok, const Maps& m, const GemmParams& p, cudaStream_t st,
                    const char* who) {
-    const int nt = ntok ? ntok : 128;  // prefill: 128-token tiles
+    const int nt = ntok ? ntok : 128;  // (prefill, ntok 0, takes the TS pair form instead)
 #define MOE_TS_FMT(MODE)                                                                                     \
     do {                                                                                                     \
         if (wfmt == MOE_W_GPTQ_INT4)                                                                         \
