@@ -150,13 +150,13 @@ LAYER_CASES = {
     "nvfp4_f16_act": synth.MoeConfig("nvfp4_f16_act", T=40, H=256, I=192, E=8, k=2, bs=16, act="f16",
                                      wfmt="nvfp4", router="normal"),
     # a block size that does not divide the tile height: tiles may start on padding rows
-    # (decode form with 64-token tiles, CTA-pair prefill form, GPTQ with 128-token tiles)
+    # (decode form with 64-token tiles, CTA-pair prefill forms for bf16 and GPTQ)
     "block48_decode": synth.MoeConfig("block48_decode", T=200, H=256, I=128, E=8, k=2, bs=48, router="normal"),
     "block48_prefill": synth.MoeConfig("block48_prefill", T=500, H=256, I=256, E=4, k=2, bs=48, router="normal"),
     "block48_gptq": synth.MoeConfig("block48_gptq", T=300, H=256, I=256, E=4, k=2, bs=48, act="f16",
                                     wfmt="gptq", router="normal"),
-    # prefill form of the quantised kernels with the other activation type, an
-    # odd number of 64-deep k blocks (I=192) and a ragged last column tile (H=320)
+    # quantised prefill (CTA-pair form) with the other activation type, an odd
+    # number of 64-deep k blocks (I=192) and a ragged last column tile (H=320)
     "gptq_bf16_prefill": synth.MoeConfig("gptq_bf16_prefill", T=300, H=320, I=192, E=2, k=1, bs=16, act="bf16",
                                          wfmt="gptq", router="normal", group_size=64),
     "nvfp4_f16_prefill": synth.MoeConfig("nvfp4_f16_prefill", T=300, H=320, I=192, E=2, k=1, bs=16, act="f16",
@@ -166,17 +166,21 @@ LAYER_CASES = {
     # 40 and 8) and ragged last column tiles
     "splitk_ragged_k": synth.MoeConfig("splitk_ragged_k", T=6, H=1000, I=520, E=4, k=2, bs=16, router="normal"),
     # FP8 (E4M3) weights with row scales: decode (16-token tiles, four issuers), prefill
-    # (128-token tiles) with the other activation type, and a ragged I / K
+    # (CTA-pair form) with the other activation type, and a ragged I / K
     "fp8@T64": _cfg("fp8@T64"),
     "fp8_f16_prefill": synth.MoeConfig("fp8_f16_prefill", T=300, H=320, I=208, E=2, k=1, bs=16, act="f16",
                                        wfmt="fp8", router="normal"),
     "fp8_decode_ragged": synth.MoeConfig("fp8_decode_ragged", T=24, H=272, I=144, E=8, k=2, bs=16,
                                          wfmt="fp8", router="normal"),
-    # FP8 prefill form (128-token tiles) with bf16 activations, the path of the
-    # fp8 workload: >= 128 rows per expert, an odd number of 64-deep k blocks
+    # FP8 prefill (the CTA-pair form, 192-row geometry) with bf16 activations, the
+    # path of the fp8 workload: >= 128 rows per expert, an odd number of 64-deep k blocks
     # for gate/up (H=320), a ragged last k block for down (I=208) and a
     # ragged last column tile
     "fp8_bf16_prefill": synth.MoeConfig("fp8_bf16_prefill", T=300, H=320, I=208, E=2, k=1, bs=16,
+                                        wfmt="fp8", router="normal"),
+    # the same at about 300 rows per expert: the CTA-pair form's 256-row geometry
+    # (one accumulator buffer, eight weight stages), each expert cut into two row tiles
+    "fp8_wide_prefill": synth.MoeConfig("fp8_wide_prefill", T=600, H=320, I=208, E=2, k=1, bs=16,
                                         wfmt="fp8", router="normal"),
     # FP8 decode form with fp16 activations
     "fp8_f16_decode": synth.MoeConfig("fp8_f16_decode", T=24, H=272, I=144, E=8, k=2, bs=16, act="f16",
