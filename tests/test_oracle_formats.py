@@ -60,6 +60,30 @@ def test_f16_rounding_matches_torch():
     np.testing.assert_array_equal(got, want)
 
 
+def test_activation_storage_matches_torch():
+    # storage in both activation dtypes and the bf16 weight decode, against
+    # torch's own dtype conversions of f32 inputs
+    rng = np.random.default_rng(3)
+    vals = np.concatenate([rng.standard_normal(5000) * 3, rng.standard_normal(500) * 1e-5,
+                           np.array([0.0, -0.0, 1.0, -2.5, 65504.0])]).astype(np.float32)
+    t = torch.from_numpy(vals)
+    want_bf16 = t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got_bf16 = orc.f64_to_act(vals.astype(np.float64), "bf16")
+    assert got_bf16.dtype == np.uint16
+    np.testing.assert_array_equal(got_bf16, want_bf16)
+    np.testing.assert_array_equal(orc.act_to_f64(got_bf16, "bf16"),
+                                  t.to(torch.bfloat16).to(torch.float64).numpy())
+    np.testing.assert_array_equal(orc.dequant_bf16(got_bf16[:5500].reshape(55, 100)),
+                                  t[:5500].to(torch.bfloat16).to(torch.float64).numpy().reshape(55, 100))
+    got_f16 = orc.f64_to_act(vals.astype(np.float64), "f16")
+    assert got_f16.dtype == np.float16
+    np.testing.assert_array_equal(got_f16.view(np.uint16),
+                                  t.to(torch.float16).view(torch.int16).numpy().view(np.uint16))
+    np.testing.assert_array_equal(orc.act_to_f64(got_f16, "f16"), t.to(torch.float16).to(torch.float64).numpy())
+    with pytest.raises(ValueError):
+        orc.f64_to_act(vals.astype(np.float64), "f32")
+
+
 def test_e2m1_e4m3_tables_match_published_values():
     for fmt, code, val in _golden_values():
         fn = orc.e2m1_value if fmt == "e2m1" else orc.e4m3_value
